@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) implementation of SeKV's span-cache decode path.
+
+The compute runs in libsekv (CUDA kernels behind a C ABI, ``include/sekv.h``);
+``decode_attention_span_gb300.sekv`` is its ctypes binding.
+"""
+
+from . import sekv  # noqa: F401
+from .sekv import (  # noqa: F401
+    Config,
+    LayerCache,
+    Workspace,
+    SekvError,
+    route,
+    decode_attention,
+    decode_step,
+    fetch_bases,
+    record_size,
+    last_launch_count,
+    default_scale,
+)

@@ -1,0 +1,28 @@
+// Host-side helpers shared by the C-ABI translation units.
+#pragma once
+
+#include <cuda.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sekv.h"
+#include "sekv_common.cuh"
+
+namespace sekv {
+
+int device_sm_count();
+int decode_cg(const sekv_config* cfg, int sms);
+int route_chunks(const sekv_config* cfg);
+WsLayout ws_layout(const sekv_config* cfg, int sms);
+size_t ws_cta_bytes(const WsLayout& L);
+void count_launch(int n);
+void reset_launches();
+
+// 3-D tiled tensor map over [d2][d1][d0] elements of `elem_bytes` each,
+// dense rows, box {box0, box1, 1}, 128-byte swizzle, zero fill out of range.
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+               uint64_t d1, uint64_t d2, int elem_bytes, uint32_t box0, uint32_t box1);
+
+size_t build_workspace_size(const sekv_config* cfg, int64_t ctx_len);
+
+}  // namespace sekv

@@ -1,0 +1,461 @@
+// C-ABI entry points of libsekv (decode side).  Argument checking, workspace
+// layout, TMA tensor-map encoding and kernel launches.  No call allocates.
+#include <string.h>
+
+#include <mutex>
+
+#include "decode_attn.cuh"
+#include "host_common.h"
+#include "route_fetch.cuh"
+
+using namespace sekv;
+
+namespace {
+
+thread_local int32_t g_launches = 0;
+
+bool config_ok(const sekv_config* cfg, sekv_status* why) {
+  if (!cfg) { *why = SEKV_ERR_INVALID; return false; }
+  if (cfg->head_dim != 128 || cfg->route_dim != 64) { *why = SEKV_ERR_UNSUPPORTED; return false; }
+  if (cfg->batch < 1 || cfg->n_kv_heads < 1 || cfg->n_q_heads < 1 || cfg->n_sink < 0 ||
+      cfg->n_recent < 0 || cfg->max_spans < 64 || cfg->max_spans % 64 != 0 ||
+      cfg->n_q_heads % cfg->n_kv_heads != 0 || cfg->batch > 65535 || cfg->n_kv_heads > 65535) {
+    *why = SEKV_ERR_INVALID;
+    return false;
+  }
+  if (cfg->n_q_heads / cfg->n_kv_heads > SEKV_MAX_GROUP || cfg->rank_cap > SEKV_MAX_RANK) {
+    *why = SEKV_ERR_UNSUPPORTED;
+    return false;
+  }
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+namespace sekv {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// CTAs per (sequence, KV head) of the decode kernel.
+int decode_cg(const sekv_config* cfg, int sms) {
+  const int ng = cfg->batch * cfg->n_kv_heads;
+  int cg = sms / ng;
+  if (cg < 1) cg = 1;
+  // every CTA's span slice must fit the shared-memory span-info cache
+  const int64_t units = 2 * int64_t(cfg->n_sink + cfg->n_recent) + 4 * int64_t(cfg->max_spans);
+  while (cg < kMaxCgSmem && units / (2 * int64_t(cg)) + 16 > kInfoCap) ++cg;
+  return cg > kMaxCgSmem ? kMaxCgSmem : cg;
+}
+
+int route_chunks(const sekv_config* cfg) { return (cfg->max_spans + 1023) / 1024; }
+
+WsLayout ws_layout(const sekv_config* cfg, int sms) {
+  WsLayout L{};
+  L.ng = cfg->batch * cfg->n_kv_heads;
+  L.cg = decode_cg(cfg, sms);
+  L.route_chunks = route_chunks(cfg);
+  const size_t ng = L.ng, ms = cfg->max_spans;
+  size_t off = 0;
+  L.status = off;     off += align256(64);
+  L.groups = off;     off += align256(ng * sizeof(GroupState));
+  L.cta_n = off;      off += align256(ng * L.cg * 4);
+  L.entries = off;    off += align256(ng * ms * sizeof(ExpEntry));
+  L.info = off;       off += align256(ng * ms * 2);
+  L.partials = off;   off += align256(ng * L.cg * sizeof(Partial));
+  L.route_list = off; off += align256(ng * ms * 4);
+  L.route_cnt = off;  off += align256(ng * L.route_chunks * 4);
+  // cta_bytes lives after route_cnt
+  L.total = off + align256(ng * L.cg * 8);
+  return L;
+}
+
+size_t ws_cta_bytes(const WsLayout& L) { return L.total - align256(size_t(L.ng) * L.cg * 8); }
+
+void count_launch(int n) { g_launches += n; }
+void reset_launches() { g_launches = 0; }
+
+}  // namespace sekv
+
+
+namespace sekv {
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+               uint64_t d1, uint64_t d2, int elem_bytes, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace sekv
+
+extern "C" {
+
+int64_t sekv_record_size(int32_t body, int32_t rank_k, int32_t rank_v) {
+  if (body <= 0 || rank_k < 0 || rank_v < 0) return 0;
+  return record_bytes(body, rank_k, rank_v);
+}
+
+const char* sekv_status_string(sekv_status s) {
+  switch (s) {
+    case SEKV_OK: return "ok";
+    case SEKV_ERR_INVALID: return "invalid argument";
+    case SEKV_ERR_CAPACITY: return "buffer or workspace too small";
+    case SEKV_ERR_CUDA: return "CUDA runtime error";
+    case SEKV_ERR_TIMEOUT: return "bounded wait ran out";
+    case SEKV_ERR_UNSUPPORTED: return "unsupported size";
+    case SEKV_ERR_DEVICE: return "device reported bad data";
+  }
+  return "unknown status";
+}
+
+int32_t sekv_last_launch_count(void) { return g_launches; }
+
+size_t sekv_workspace_size(const sekv_config* cfg, int32_t which, int64_t ctx_len) {
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  if (which == SEKV_CALL_BUILD) return build_workspace_size(cfg, ctx_len);
+  return ws_layout(cfg, sms).total;
+}
+
+sekv_status sekv_workspace_init(void* workspace, size_t bytes, cudaStream_t stream) {
+  if (!workspace || bytes == 0) return SEKV_ERR_INVALID;
+  return cudaMemsetAsync(workspace, 0, bytes, stream) == cudaSuccess ? SEKV_OK : SEKV_ERR_CUDA;
+}
+
+sekv_status sekv_workspace_status(void* workspace, cudaStream_t stream, int32_t* code,
+                                  int32_t* detail) {
+  if (!workspace) return SEKV_ERR_INVALID;
+  int32_t h[2] = {0, 0};
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (cudaMemcpy(h, workspace, 8, cudaMemcpyDeviceToHost) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 8) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (code) *code = h[0];
+  if (detail) *detail = h[1];
+  if (h[0] == 0) return SEKV_OK;
+  return h[0] == DEV_WAIT_TIMEOUT ? SEKV_ERR_TIMEOUT : SEKV_ERR_DEVICE;
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------
+// decode launches
+// ----------------------------------------------------------------------------
+namespace {
+
+sekv_status check_cache(const sekv_config* cfg, const sekv_layer_cache* c, bool need_store) {
+  if (!c || !c->n_spans || !c->body_len || !c->k_full || !c->v_full || !c->k_sum || !c->v_sum ||
+      !c->rec_off || !c->rec_rank)
+    return SEKV_ERR_INVALID;
+  if (need_store && !c->store) return SEKV_ERR_INVALID;
+  if (!aligned16(c->k_full) || !aligned16(c->v_full) || !aligned16(c->k_sum) ||
+      !aligned16(c->v_sum) || !aligned16(c->body_len) || !aligned16(c->rec_off) ||
+      !aligned16(c->rec_rank) || (c->s_route && !aligned16(c->s_route)) ||
+      (c->store && !aligned16(c->store)))
+    return SEKV_ERR_INVALID;
+  (void)cfg;
+  return SEKV_OK;
+}
+
+sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* cache,
+                               const WsLayout& L, void* ws, DecodeParams& P, bool fused) {
+  const int ng = L.ng;
+  const uint64_t cap_full = uint64_t(cfg->n_sink) + cfg->max_spans + cfg->n_recent;
+  bool ok = true;
+  ok &= encode_3d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, 64, 64);
+  ok &= encode_3d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, 64, 64);
+  ok &= encode_3d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, 64, 64);
+  ok &= encode_3d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, 64, 64);
+  if (fused) {
+    ok &= encode_3d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, 32, 64);
+  } else {
+    P.tm_sroute = P.tm_ksum;
+  }
+  if (!ok) return SEKV_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  P.n_spans = cache->n_spans;
+  P.body_len = cache->body_len;
+  P.rec_off = cache->rec_off;
+  P.rec_rank = cache->rec_rank;
+  P.status = reinterpret_cast<int32_t*>(w + L.status);
+  P.groups = reinterpret_cast<GroupState*>(w + L.groups);
+  P.cta_n = reinterpret_cast<int32_t*>(w + L.cta_n);
+  P.cta_bytes = reinterpret_cast<int64_t*>(w + ws_cta_bytes(L));
+  P.entries = reinterpret_cast<ExpEntry*>(w + L.entries);
+  P.info = reinterpret_cast<const uint16_t*>(w + L.info);
+  P.partials = reinterpret_cast<Partial*>(w + L.partials);
+  P.B = cfg->batch;
+  P.Hq = cfg->n_q_heads;
+  P.Hkv = cfg->n_kv_heads;
+  P.G = cfg->n_q_heads / cfg->n_kv_heads;
+  P.n_sink = cfg->n_sink;
+  P.n_recent = cfg->n_recent;
+  P.max_spans = cfg->max_spans;
+  P.cap_full = int(cap_full);
+  P.cg = L.cg;
+  P.fused = fused ? 1 : 0;
+  return SEKV_OK;
+}
+
+sekv_status launch_decode(const DecodeParams& P, const WsLayout& L, const sekv_config* cfg,
+                          cudaStream_t stream, bool overlap) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return SEKV_ERR_CUDA;
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(L.cg, cfg->n_kv_heads, cfg->batch);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = kSmemAlloc;
+  lc.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = overlap ? 1 : 0;
+  if (cudaLaunchKernelEx(&lc, decode_kernel, P) != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(1);
+  return SEKV_OK;
+}
+
+sekv_status launch_prep(const sekv_config* cfg, const sekv_layer_cache* cache,
+                        const int32_t* expanded, const int32_t* n_expanded,
+                        const int64_t* staged_off, const WsLayout& L, void* ws,
+                        cudaStream_t stream) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PrepParams pp;
+  pp.n_spans = cache->n_spans;
+  pp.body_len = cache->body_len;
+  pp.rec_off = cache->rec_off;
+  pp.rec_rank = cache->rec_rank;
+  pp.expanded = expanded;
+  pp.n_expanded = n_expanded;
+  pp.staged_off = staged_off;
+  pp.status = reinterpret_cast<int32_t*>(w + L.status);
+  pp.groups = reinterpret_cast<GroupState*>(w + L.groups);
+  pp.cta_n = reinterpret_cast<int32_t*>(w + L.cta_n);
+  pp.cta_bytes = reinterpret_cast<int64_t*>(w + ws_cta_bytes(L));
+  pp.entries = reinterpret_cast<ExpEntry*>(w + L.entries);
+  pp.info = reinterpret_cast<uint16_t*>(w + L.info);
+  pp.Hkv = cfg->n_kv_heads;
+  pp.max_spans = cfg->max_spans;
+  pp.cg = L.cg;
+  prep_list_kernel<<<L.ng, 256, 0, stream>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(1);
+  return SEKV_OK;
+}
+
+}  // namespace
+
+extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                        const void* q, const float* W_r, const float* theta,
+                                        float scale, float* out, float* lse, int32_t* expanded,
+                                        int32_t* n_expanded, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  sekv_status st = check_cache(cfg, cache, true);
+  if (st != SEKV_OK) return st;
+  if (!q || !W_r || !theta || !out || !workspace || !cache->s_route) return SEKV_ERR_INVALID;
+  if (cache->store_on_host) return SEKV_ERR_UNSUPPORTED;
+  if (!aligned16(W_r) || !aligned16(q)) return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  const WsLayout L = ws_layout(cfg, sms);
+  if (workspace_bytes < L.total) return SEKV_ERR_CAPACITY;
+  DecodeParams P;
+  memset(&P, 0, sizeof(P));
+  st = fill_decode_params(cfg, cache, L, workspace, P, true);
+  if (st != SEKV_OK) return st;
+  P.store = static_cast<const uint8_t*>(cache->store);
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.W_r = W_r;
+  P.theta = theta;
+  P.out = out;
+  P.lse = lse;
+  P.expanded_out = expanded;
+  P.n_expanded_out = n_expanded;
+  P.scale_log2 = scale * kLog2e;
+  return launch_decode(P, L, cfg, stream, (cfg->flags & SEKV_FLAG_OVERLAP_PREVIOUS) != 0);
+}
+
+extern "C" sekv_status sekv_decode_attention(const sekv_config* cfg,
+                                             const sekv_layer_cache* cache, const void* q,
+                                             const int32_t* expanded, const int32_t* n_expanded,
+                                             const void* staging, const int64_t* staged_off,
+                                             float scale, float* out, float* lse,
+                                             void* workspace, size_t workspace_bytes,
+                                             cudaStream_t stream) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  const bool staged = staging != nullptr;
+  if (staged != (staged_off != nullptr)) return SEKV_ERR_INVALID;
+  sekv_status st = check_cache(cfg, cache, !staged);
+  if (st != SEKV_OK) return st;
+  if (!staged && cache->store_on_host) return SEKV_ERR_UNSUPPORTED;
+  if (!q || !expanded || !n_expanded || !out || !workspace) return SEKV_ERR_INVALID;
+  if (!aligned16(q) || (staged && !aligned16(staging))) return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  const WsLayout L = ws_layout(cfg, sms);
+  if (workspace_bytes < L.total) return SEKV_ERR_CAPACITY;
+  DecodeParams P;
+  memset(&P, 0, sizeof(P));
+  st = fill_decode_params(cfg, cache, L, workspace, P, false);
+  if (st != SEKV_OK) return st;
+  P.store = static_cast<const uint8_t*>(staged ? staging : cache->store);
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.out = out;
+  P.lse = lse;
+  P.scale_log2 = scale * kLog2e;
+  // prepare span info and entries from the list
+  st = launch_prep(cfg, cache, expanded, n_expanded, staged_off, L, workspace, stream);
+  if (st != SEKV_OK) return st;
+  return launch_decode(P, L, cfg, stream, false);
+}
+
+extern "C" sekv_status sekv_route(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                  const void* q, const float* W_r, const float* theta,
+                                  int32_t* expanded, int32_t* n_expanded, float* z_out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  if (!cache || !cache->n_spans || !cache->body_len || !cache->s_route) return SEKV_ERR_INVALID;
+  if (!q || !W_r || !theta || !expanded || !n_expanded || !workspace) return SEKV_ERR_INVALID;
+  if (!aligned16(cache->s_route) || !aligned16(W_r)) return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  const WsLayout L = ws_layout(cfg, sms);
+  if (workspace_bytes < L.total) return SEKV_ERR_CAPACITY;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  RouteParams P;
+  P.n_spans = cache->n_spans;
+  P.body_len = cache->body_len;
+  P.s_route = cache->s_route;
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.W_r = W_r;
+  P.theta = theta;
+  P.expanded = expanded;
+  P.n_expanded = n_expanded;
+  P.z_out = z_out;
+  P.status = reinterpret_cast<int32_t*>(w + L.status);
+  P.groups = reinterpret_cast<GroupState*>(w + L.groups);
+  P.list_scratch = reinterpret_cast<int32_t*>(w + L.route_list);
+  P.cnt_scratch = reinterpret_cast<int32_t*>(w + L.route_cnt);
+  P.B = cfg->batch;
+  P.Hq = cfg->n_q_heads;
+  P.Hkv = cfg->n_kv_heads;
+  P.G = cfg->n_q_heads / cfg->n_kv_heads;
+  P.max_spans = cfg->max_spans;
+  P.chunks = L.route_chunks;
+  route_kernel<<<dim3(L.route_chunks, cfg->n_kv_heads, cfg->batch), kRouteThreads, 0, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(1);
+  return SEKV_OK;
+}
+
+extern "C" sekv_status sekv_fetch_bases(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                        const int32_t* expanded, const int32_t* n_expanded,
+                                        void* staging, int64_t staging_per_group,
+                                        int64_t* staged_off, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  if (!cache || !cache->n_spans || !cache->body_len || !cache->rec_off || !cache->rec_rank ||
+      !cache->store)
+    return SEKV_ERR_INVALID;
+  if (!expanded || !n_expanded || !staging || !staged_off || !workspace) return SEKV_ERR_INVALID;
+  if (staging_per_group <= 0 || staging_per_group % 16 != 0 || !aligned16(staging) ||
+      !aligned16(cache->store))
+    return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  const WsLayout L = ws_layout(cfg, sms);
+  if (workspace_bytes < L.total) return SEKV_ERR_CAPACITY;
+  const void* dev_store = cache->store;
+  if (cache->store_on_host) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, cache->store) != cudaSuccess ||
+        pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) {
+      cudaGetLastError();
+      return SEKV_ERR_INVALID;  // not page-locked host memory the device can address
+    }
+    dev_store = pa.devicePointer;
+  }
+  FetchParams P;
+  P.n_spans = cache->n_spans;
+  P.body_len = cache->body_len;
+  P.rec_off = cache->rec_off;
+  P.rec_rank = cache->rec_rank;
+  P.store = static_cast<const uint8_t*>(dev_store);
+  P.expanded = expanded;
+  P.n_expanded = n_expanded;
+  P.staging = static_cast<uint8_t*>(staging);
+  P.per_group = staging_per_group;
+  P.staged_off = staged_off;
+  P.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.status);
+  P.Hkv = cfg->n_kv_heads;
+  P.max_spans = cfg->max_spans;
+  fetch_kernel<<<dim3(L.ng, kFetchParts), 256, 0, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(1);
+  return SEKV_OK;
+}
+
+namespace sekv {
+size_t build_workspace_size(const sekv_config* cfg, int64_t ctx_len) {
+  (void)cfg;
+  (void)ctx_len;
+  return 0;
+}
+}  // namespace sekv

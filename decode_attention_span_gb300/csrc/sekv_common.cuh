@@ -1,0 +1,199 @@
+// Shared device helpers for libsekv (sm_103a): inline PTX for mbarriers,
+// bulk and tensor TMA copies, ldmatrix, mma.sync and programmatic dependent
+// launch, plus the workspace layout that host and device code agree on.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sekv.h"
+
+namespace sekv {
+
+constexpr int kHeadDim = 128;
+constexpr int kRouteDim = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// device status codes (first error wins); detail carries an index or a count
+enum DeviceError : int32_t {
+  DEV_OK = 0,
+  DEV_BAD_LIST = 1,        // expansion list not ascending / out of range / empty body
+  DEV_WAIT_TIMEOUT = 2,    // a bounded spin ran out
+  DEV_STAGING_FULL = 3,    // fetch: a group's records exceed its staging share
+  DEV_BAD_RANK = 4,        // a record rank above the supported maximum
+};
+
+// ----------------------------------------------------------------------------
+// workspace layout (bytes, all offsets 256-aligned)
+// ----------------------------------------------------------------------------
+struct GroupState {        // one per (sequence, KV head); zero between calls
+  int32_t published;       // CTAs that have published their expansion entries
+  int32_t done;            // CTAs that have written their partial
+  int32_t route_done;      // route kernel: chunks finished
+  int32_t pad;
+};
+
+struct ExpEntry {          // one expanded span, 32 bytes
+  int32_t k;               // span ordinal
+  int32_t body;            // |S|
+  int32_t rank;            // rK | rV << 16
+  int32_t pad;
+  int64_t off;             // byte offset of its record (store or staging)
+  int64_t pad2;
+};
+
+struct Partial {           // one CTA's softmax state for up to 8 heads
+  float m[8];              // running max (log2 domain)
+  float l[8];              // sum of 2^(x - m)
+  float o[8][kHeadDim];    // sum of 2^(x - m) * value
+};
+
+struct WsLayout {
+  size_t status, groups, cta_n, entries, info, partials, route_list, route_cnt, total;
+  int ng, cg, route_chunks;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Non-blocking probe of a phase (test_wait never suspends the thread, so a
+// bounded loop of probes has a known duration).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false after `limit` polls (the caller flags an error).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared (box given by the tensor map)
+__device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, int x, int y,
+                                           int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D for one m16n8k16 bf16 tile; rows 8..15 of A are zero in this
+// library (at most 8 query heads), so only the first two accumulators (row
+// lane/4) are kept; the other two are fed zero and discarded.
+__device__ __forceinline__ void mma_bf16_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+  float z2, z3;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%10,%11};"
+      : "+f"(d0), "+f"(d1), "=f"(z2), "=f"(z3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void set_device_error(int32_t* status, int32_t code, int32_t detail) {
+  if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// byte address inside a 128B-swizzled box of 128-byte rows
+__device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int chunk16) {
+  return base + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+}
+
+__host__ __device__ inline int r4(int r) { return (r + 3) & ~3; }
+__host__ __device__ inline int64_t pad16(int64_t n) { return (n + 15) & ~int64_t(15); }
+
+__host__ __device__ inline int64_t record_bytes(int b, int rK, int rV) {
+  if (b <= 0) return 0;
+  return 16 + 8 * r4(rK) + 256 * int64_t(rK) + pad16(2 * int64_t(b) * rK) +
+         pad16(2 * int64_t(b) * rV) + 8 * r4(rV) + 256 * int64_t(rV);
+}
+
+}  // namespace sekv

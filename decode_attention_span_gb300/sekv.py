@@ -1,0 +1,292 @@
+"""Thin ctypes binding of libsekv (argument marshalling only).
+
+Every computation runs in the CUDA kernels behind the C ABI in
+``include/sekv.h``; this module checks tensor placement and dtypes, passes raw
+pointers and the current CUDA stream, and raises on a non-OK status.  There is
+no CPU fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+_c_i32, _c_f32, _c_vp, _c_sz, _c_i64 = (ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+                                        ctypes.c_size_t, ctypes.c_int64)
+
+SEKV_CALL_ROUTE, SEKV_CALL_FETCH, SEKV_CALL_DECODE, SEKV_CALL_BUILD = 0, 1, 2, 3
+FLAG_OVERLAP_PREVIOUS = 1
+STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SEKV_ERR_CUDA",
+          -4: "SEKV_ERR_TIMEOUT", -5: "SEKV_ERR_UNSUPPORTED", -6: "SEKV_ERR_DEVICE"}
+
+# every symbol include/sekv.h declares
+EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
+           "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
+           "sekv_decode_step", "sekv_status_string", "sekv_last_launch_count")
+
+
+class SekvError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+class SekvConfig(ctypes.Structure):
+    _fields_ = [("batch", _c_i32), ("n_q_heads", _c_i32), ("n_kv_heads", _c_i32),
+                ("head_dim", _c_i32), ("route_dim", _c_i32), ("n_sink", _c_i32),
+                ("n_recent", _c_i32), ("max_spans", _c_i32), ("rank_cap", _c_i32),
+                ("len_min", _c_i32), ("len_max", _c_i32), ("tau", _c_f32), ("flags", _c_i32)]
+
+
+class SekvLayerCache(ctypes.Structure):
+    _fields_ = [("n_spans", _c_vp), ("body_len", _c_vp), ("k_full", _c_vp), ("v_full", _c_vp),
+                ("s_route", _c_vp), ("k_sum", _c_vp), ("v_sum", _c_vp), ("rec_off", _c_vp),
+                ("rec_rank", _c_vp), ("store", _c_vp), ("store_on_host", _c_i32)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsekv; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsekv is not built ({path} missing); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(path)
+        L.sekv_record_size.restype = _c_i64
+        L.sekv_record_size.argtypes = [_c_i32, _c_i32, _c_i32]
+        L.sekv_workspace_size.restype = _c_sz
+        L.sekv_workspace_size.argtypes = [ctypes.POINTER(SekvConfig), _c_i32, _c_i64]
+        L.sekv_workspace_init.restype = _c_i32
+        L.sekv_workspace_init.argtypes = [_c_vp, _c_sz, _c_vp]
+        L.sekv_workspace_status.restype = _c_i32
+        L.sekv_workspace_status.argtypes = [_c_vp, _c_vp, ctypes.POINTER(_c_i32),
+                                            ctypes.POINTER(_c_i32)]
+        L.sekv_route.restype = _c_i32
+        L.sekv_route.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
+                                 _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+        L.sekv_fetch_bases.restype = _c_i32
+        L.sekv_fetch_bases.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
+                                       _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]
+        L.sekv_decode_attention.restype = _c_i32
+        L.sekv_decode_attention.argtypes = [ctypes.POINTER(SekvConfig),
+                                            ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp, _c_vp,
+                                            _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_sz,
+                                            _c_vp]
+        L.sekv_decode_step.restype = _c_i32
+        L.sekv_decode_step.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
+                                       _c_vp, _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       _c_vp, _c_sz, _c_vp]
+        L.sekv_status_string.restype = ctypes.c_char_p
+        L.sekv_status_string.argtypes = [_c_i32]
+        L.sekv_last_launch_count.restype = _c_i32
+        L.sekv_last_launch_count.argtypes = []
+        _LIB = L
+    return _LIB
+
+
+def _check(call: str, st: int):
+    if st != 0:
+        raise SekvError(call, st)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, cuda: bool = True):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+# ----------------------------------------------------------------------------
+# configuration, cache, workspace
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Config:
+    batch: int
+    n_q_heads: int
+    n_kv_heads: int
+    n_sink: int
+    n_recent: int
+    max_spans: int
+    rank_cap: int = 32
+    len_min: int = 4
+    len_max: int = 256
+    tau: float = 5.2
+    head_dim: int = 128
+    route_dim: int = 64
+    flags: int = 0
+
+    def c(self) -> SekvConfig:
+        return SekvConfig(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim,
+                          self.route_dim, self.n_sink, self.n_recent, self.max_spans,
+                          self.rank_cap, self.len_min, self.len_max, float(self.tau),
+                          self.flags)
+
+
+CACHE_FIELDS = ("n_spans", "body_len", "k_full", "v_full", "s_route", "k_sum", "v_sum",
+                "rec_off", "rec_rank", "store")
+
+
+class LayerCache:
+    """One layer of the span cache as torch tensors in the C-ABI layout."""
+
+    def __init__(self, tensors: Dict[str, torch.Tensor], store_on_host: bool = False):
+        self.t = {k: tensors[k] for k in CACHE_FIELDS if k in tensors}
+        self.store_on_host = store_on_host
+        for k, dt in (("n_spans", torch.int32), ("body_len", torch.int32),
+                      ("k_full", torch.bfloat16), ("v_full", torch.bfloat16),
+                      ("s_route", torch.float32), ("k_sum", torch.bfloat16),
+                      ("v_sum", torch.bfloat16), ("rec_off", torch.int64),
+                      ("rec_rank", torch.int32)):
+            _need(self.t[k], k, dt)
+        st = self.t["store"]
+        _need(st, "store", torch.uint8, cuda=not store_on_host)
+        if store_on_host and not st.is_pinned():
+            raise ValueError("store: host tier must be pinned memory")
+        self._c = SekvLayerCache(*[_ptr(self.t[k]) for k in CACHE_FIELDS], int(store_on_host))
+
+    @property
+    def c(self) -> SekvLayerCache:
+        return self._c
+
+
+class Workspace:
+    """Caller-owned scratch of sekv_workspace_size bytes, zeroed once."""
+
+    def __init__(self, cfg: Config, device=None, which: int = SEKV_CALL_DECODE, ctx_len: int = 0):
+        c = cfg.c()
+        n = int(lib().sekv_workspace_size(ctypes.byref(c), which, ctx_len))
+        if n == 0:
+            raise SekvError("sekv_workspace_size", -1)
+        self.nbytes = n
+        self.buf = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+        _check("sekv_workspace_init", lib().sekv_workspace_init(_ptr(self.buf), n, _stream()))
+
+    def ptr(self):
+        return _ptr(self.buf)
+
+    def status(self) -> Tuple[int, int]:
+        """Synchronise; return (device code, detail) and clear them."""
+        code, detail = _c_i32(0), _c_i32(0)
+        lib().sekv_workspace_status(self.ptr(), _stream(), ctypes.byref(code), ctypes.byref(detail))
+        return code.value, detail.value
+
+    def raise_on_error(self):
+        code, detail = self.status()
+        if code != 0:
+            raise RuntimeError(f"libsekv device status {code} (detail {detail})")
+
+
+def record_size(body: int, rank_k: int, rank_v: int) -> int:
+    return int(lib().sekv_record_size(body, rank_k, rank_v))
+
+
+def last_launch_count() -> int:
+    return int(lib().sekv_last_launch_count())
+
+
+# ----------------------------------------------------------------------------
+# calls
+# ----------------------------------------------------------------------------
+
+def route(cfg: Config, cache: LayerCache, q, W_r, theta, ws: Workspace, want_z: bool = False,
+          expanded=None, n_expanded=None, stream=None):
+    _need(q, "q", torch.bfloat16); _need(W_r, "W_r", torch.float32)
+    _need(theta, "theta", torch.float32)
+    dev = q.device
+    NG = cfg.batch * cfg.n_kv_heads
+    if expanded is None:
+        expanded = torch.empty(NG * cfg.max_spans, dtype=torch.int32, device=dev)
+    if n_expanded is None:
+        n_expanded = torch.empty(NG, dtype=torch.int32, device=dev)
+    z = (torch.zeros(cfg.batch * cfg.n_q_heads * cfg.max_spans, dtype=torch.float32, device=dev)
+         if want_z else None)
+    c = cfg.c()
+    _check("sekv_route", lib().sekv_route(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q),
+                                          _ptr(W_r), _ptr(theta), _ptr(expanded),
+                                          _ptr(n_expanded), _ptr(z), ws.ptr(), ws.nbytes,
+                                          _stream(stream)))
+    return expanded, n_expanded, z
+
+
+def decode_attention(cfg: Config, cache: LayerCache, q, expanded, n_expanded, scale: float,
+                     ws: Workspace, staging=None, staged_off=None, out=None, lse=None,
+                     stream=None):
+    _need(q, "q", torch.bfloat16); _need(expanded, "expanded", torch.int32)
+    _need(n_expanded, "n_expanded", torch.int32)
+    dev = q.device
+    if out is None:
+        out = torch.empty(cfg.batch, cfg.n_q_heads, 128, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(cfg.batch, cfg.n_q_heads, dtype=torch.float32, device=dev)
+    c = cfg.c()
+    _check("sekv_decode_attention",
+           lib().sekv_decode_attention(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q),
+                                       _ptr(expanded), _ptr(n_expanded), _ptr(staging),
+                                       _ptr(staged_off), float(scale), _ptr(out), _ptr(lse),
+                                       ws.ptr(), ws.nbytes, _stream(stream)))
+    return out, lse
+
+
+def decode_step(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float, ws: Workspace,
+                out=None, lse=None, want_list: bool = False, stream=None):
+    _need(q, "q", torch.bfloat16); _need(W_r, "W_r", torch.float32)
+    _need(theta, "theta", torch.float32)
+    dev = q.device
+    if out is None:
+        out = torch.empty(cfg.batch, cfg.n_q_heads, 128, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(cfg.batch, cfg.n_q_heads, dtype=torch.float32, device=dev)
+    NG = cfg.batch * cfg.n_kv_heads
+    expanded = n_expanded = None
+    if want_list:
+        expanded = torch.zeros(NG * cfg.max_spans, dtype=torch.int32, device=dev)
+        n_expanded = torch.zeros(NG, dtype=torch.int32, device=dev)
+    c = cfg.c()
+    _check("sekv_decode_step",
+           lib().sekv_decode_step(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q), _ptr(W_r),
+                                  _ptr(theta), float(scale), _ptr(out), _ptr(lse),
+                                  _ptr(expanded), _ptr(n_expanded), ws.ptr(), ws.nbytes,
+                                  _stream(stream)))
+    return out, lse, expanded, n_expanded
+
+
+def fetch_bases(cfg: Config, cache: LayerCache, expanded, n_expanded, staging, per_group: int,
+                staged_off, ws: Workspace, stream=None):
+    _need(staging, "staging", torch.uint8); _need(staged_off, "staged_off", torch.int64)
+    c = cfg.c()
+    _check("sekv_fetch_bases",
+           lib().sekv_fetch_bases(ctypes.byref(c), ctypes.byref(cache.c), _ptr(expanded),
+                                  _ptr(n_expanded), _ptr(staging), int(per_group),
+                                  _ptr(staged_off), ws.ptr(), ws.nbytes, _stream(stream)))
+    return staging, staged_off
+
+
+def default_scale() -> float:
+    return 1.0 / math.sqrt(128.0)

@@ -1,0 +1,252 @@
+/*
+ * sekv.h -- C ABI of libsekv, a GB300 (sm_103a) implementation of the
+ * decode hot path of SeKV ("SeKV: Resolution-Adaptive KV Cache with
+ * Hierarchical Semantic Memory for Long-Context LLM Inference"), and of the
+ * prefill build of its span cache.
+ *
+ * Sources, cited per call as "page, section":
+ *   [DE] gist.science, German explainer of the paper, "Technisches Resuemee":
+ *        Methodik 1 (entropy-guided span segmentation), 2 (dual-resolution
+ *        span representation), 3 (trained zoom-in, mixed-resolution
+ *        attention); Problemstellung (the problem statement).
+ *   [ZH] gist.science, Chinese explainer, "技术摘要": 方法论 1, 2, 3; 问题陈述.
+ *   [EN] the paper's English abstract.
+ *
+ * General rules
+ *   - Every pointer is caller-owned.  Device pointers are CUDA device
+ *     memory of the current device unless a field says "host".  The library
+ *     keeps no pointer after a call returns.
+ *   - No call allocates device memory.  Scratch comes from a caller-owned
+ *     workspace of sekv_workspace_size() bytes that must be zeroed once with
+ *     sekv_workspace_init(); every call leaves it ready for the next call.
+ *     One workspace serves one stream at a time: two calls that use the same
+ *     workspace must not overlap on the GPU.
+ *   - Calls are asynchronous on the given stream.  Argument errors are
+ *     detected on the host before any launch and returned; nothing is
+ *     launched then.  Errors the GPU detects (a bad index in a list, a
+ *     capacity overflow, a wait that ran out) set a status word in the
+ *     workspace; sekv_workspace_status() synchronises and reports it.
+ *   - Sizes are fixed: head_dim == 128, route_dim == 64, at most 8 query
+ *     heads per KV head, ranks at most 64.  Other values give
+ *     SEKV_ERR_UNSUPPORTED.
+ *   - bf16 means IEEE bfloat16 stored as 16-bit patterns.
+ */
+#ifndef SEKV_H_
+#define SEKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SEKV_HEAD_DIM 128
+#define SEKV_ROUTE_DIM 64
+#define SEKV_MAX_GROUP 8
+#define SEKV_MAX_RANK 64
+
+typedef enum sekv_status {
+  SEKV_OK = 0,
+  SEKV_ERR_INVALID = -1,      /* bad argument (null pointer, negative size, misalignment) */
+  SEKV_ERR_CAPACITY = -2,     /* a caller buffer or the workspace is too small */
+  SEKV_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+  SEKV_ERR_TIMEOUT = -4,      /* a bounded wait ran out (host or device) */
+  SEKV_ERR_UNSUPPORTED = -5,  /* a size the library does not implement */
+  SEKV_ERR_DEVICE = -6        /* the GPU flagged bad data (see sekv_workspace_status) */
+} sekv_status;
+
+/* Shapes and hyper-parameters shared by every call. */
+typedef struct sekv_config {
+  int32_t batch;       /* B: sequences */
+  int32_t n_q_heads;   /* Hq: query heads; a multiple of n_kv_heads, Hq/Hkv <= 8 */
+  int32_t n_kv_heads;  /* Hkv */
+  int32_t head_dim;    /* must be 128 */
+  int32_t route_dim;   /* must be 64 */
+  int32_t n_sink;      /* full-resolution tokens at the start of the context */
+  int32_t n_recent;    /* full-resolution tokens at the end of the context */
+  int32_t max_spans;   /* capacity of every per-sequence span array; a multiple of 64 */
+  int32_t rank_cap;    /* R: largest rank a span basis may keep (<= 64) */
+  int32_t len_min;     /* segmentation: shortest span (anchor included) unless cut by the end */
+  int32_t len_max;     /* segmentation: longest span (anchor included) */
+  float tau;           /* segmentation: surprisal threshold (strict >) */
+  int32_t flags;       /* SEKV_FLAG_* bits, 0 for none */
+} sekv_config;
+
+/* sekv_decode_step may start streaming this layer's cache (never q, W_r or
+ * theta) before the kernel that precedes it on the stream has finished
+ * (programmatic dependent launch).  Set it only when no preceding kernel on
+ * the stream writes this layer's cache; it hides launch gaps between layers. */
+#define SEKV_FLAG_OVERLAP_PREVIOUS 1
+
+/*
+ * One layer of the span cache.  [DE]/[ZH] Methodik 2 and 3: per span the GPU
+ * holds an anchor token at full resolution, a routing summary and (this
+ * build's reading of the "size-corrected summary") a summary key/value; the
+ * low-rank basis lives in the basis store, on the host or in device memory.
+ *
+ * Index names: b sequence, c KV head, k span ordinal, g = b*Hkv + c.
+ *   n_spans   int32 [B]                   spans of sequence b (<= max_spans)
+ *   body_len  int32 [B][max_spans]        |S_k|, tokens strictly between
+ *                                         anchor k and the next span's anchor;
+ *                                         0 means the span has no body
+ *   k_full,   bf16 [B][Hkv][n_full_cap][128], n_full_cap = n_sink + max_spans
+ *   v_full                                + n_recent.  Rows of group g: the
+ *                                         n_sink sinks, the n_spans[b] anchors
+ *                                         in span order, the n_recent recent
+ *                                         tokens; rows past those must hold
+ *                                         finite values (zero them)
+ *   s_route   f32  [B][Hkv][max_spans][64]  unit routing summaries
+ *   k_sum,    bf16 [B][Hkv][max_spans][128] summary keys / values (finite)
+ *   v_sum
+ *   rec_off   int64 [B][Hkv][max_spans]   byte offset of span k's basis
+ *                                         record in `store` (multiple of 16)
+ *   rec_rank  int32 [B][Hkv][max_spans]   rK | (rV << 16), the record's ranks
+ *   store     basis records; device memory, or host memory (store_on_host=1)
+ *             that the device can address (pinned and mapped)
+ *
+ * Basis record of a span with body b >= 1 and ranks rK, rV ([DE]/[ZH]
+ * Methodik 2: truncated SVD K_S ~ U_K diag(sigma_K g_K) Vt_K with soft gates
+ * g; likewise V).  All offsets relative to the record start, every field
+ * 16-byte aligned, r4(r) = r rounded up to a multiple of 4, pad16 = rounded
+ * up to 16 bytes; padding bytes are unspecified (writers zero them):
+ *   int32 b, rK, rV, 0                          16 bytes
+ *   f32  sigma_K[r4(rK)], f32 g_K[r4(rK)]       8*r4(rK)
+ *   bf16 Vt_K[rK][128]                          256*rK
+ *   bf16 U_K[b][rK]   (row-major)               pad16(2*b*rK)
+ *   bf16 U_V[b][rV]   (row-major)               pad16(2*b*rV)
+ *   f32  sigma_V[r4(rV)], f32 g_V[r4(rV)]       8*r4(rV)
+ *   bf16 Vt_V[rV][128]                          256*rV
+ * Record size = the sum of the right-hand column (sekv_record_size).
+ */
+typedef struct sekv_layer_cache {
+  const int32_t* n_spans;
+  const int32_t* body_len;
+  const void* k_full;
+  const void* v_full;
+  const float* s_route;
+  const void* k_sum;
+  const void* v_sum;
+  const int64_t* rec_off;
+  const int32_t* rec_rank;
+  const void* store;
+  int32_t store_on_host;
+} sekv_layer_cache;
+
+/* Which call a workspace is sized for. */
+typedef enum sekv_call {
+  SEKV_CALL_ROUTE = 0,
+  SEKV_CALL_FETCH = 1,
+  SEKV_CALL_DECODE = 2,   /* sekv_decode_attention and sekv_decode_step */
+  SEKV_CALL_BUILD = 3
+} sekv_call;
+
+/* Bytes of one basis record (0 when body <= 0); see the layout above. */
+int64_t sekv_record_size(int32_t body, int32_t rank_k, int32_t rank_v);
+
+/* Workspace bytes the given call needs for this configuration; ctx_len is
+ * used by SEKV_CALL_BUILD only.  Returns 0 for an invalid configuration. */
+size_t sekv_workspace_size(const sekv_config* cfg, int32_t which, int64_t ctx_len);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`).  Needed once, before the
+ * workspace's first use. */
+sekv_status sekv_workspace_init(void* workspace, size_t bytes, cudaStream_t stream);
+
+/* Synchronise `stream`, copy the workspace's device status into *code and
+ * *detail (either may be NULL) and clear it.  Returns SEKV_OK when the GPU
+ * flagged nothing, SEKV_ERR_DEVICE or SEKV_ERR_TIMEOUT when it did. */
+sekv_status sekv_workspace_status(void* workspace, cudaStream_t stream,
+                                  int32_t* code, int32_t* detail);
+
+/*
+ * sekv_route -- zoom-in routing of one layer.
+ * [DE]/[ZH] Methodik 3: the query is projected into the routing space of the
+ * span summaries; a sigmoid gate scores each span; a learned per-head,
+ * per-layer threshold decides whether it is expanded.  Readings: y_h =
+ * W_r[c] q_h for query head h of KV head c = h / (Hq/Hkv); z_{h,k} = y_h .
+ * s_route[b][c][k]; head h expands span k iff z_{h,k} > theta[h] (theta in
+ * logit space, so this is sigmoid(z) > sigmoid(theta)); KV head c expands
+ * the union over its query heads; spans with body_len 0 never expand.
+ *   q        bf16 [B][Hq][128]
+ *   W_r      f32  [Hkv][64][128]
+ *   theta    f32  [Hq]
+ *   expanded int32 [B][Hkv][max_spans]  out: ascending span ordinals
+ *   n_expanded int32 [B][Hkv]           out: list lengths
+ *   z_out    f32  [B][Hq][max_spans]    out, optional (NULL): the logits
+ * Deterministic: the lists are bit-reproducible.
+ */
+sekv_status sekv_route(const sekv_config* cfg, const sekv_layer_cache* cache,
+                       const void* q, const float* W_r, const float* theta,
+                       int32_t* expanded, int32_t* n_expanded, float* z_out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * sekv_fetch_bases -- copy the basis records of the expanded spans from the
+ * host tier into device staging memory.  [DE]/[ZH] Methodik 3: an expanded
+ * span's basis is loaded asynchronously from the CPU; the Bedeutung section
+ * names the CPU-GPU bandwidth as the method's cost.
+ * The cache's store must be host memory the device can address.  A gather
+ * kernel reads the records over the host link and writes them to `staging`:
+ * group g's records go to [g*staging_per_group, (g+1)*staging_per_group),
+ * packed in list order; staged_off[g][e] receives the byte offset of list
+ * entry e (relative to `staging`).  Runs on `stream`; use a side stream and
+ * an event to overlap it with other work.
+ *   expanded, n_expanded  device lists from sekv_route
+ *   staging               device, >= B*Hkv*staging_per_group bytes, 16-aligned
+ *   staged_off            int64 [B][Hkv][max_spans] (device, out)
+ * A group whose records exceed staging_per_group sets SEKV_ERR_CAPACITY in the
+ * workspace status and copies none of that group's records.
+ */
+sekv_status sekv_fetch_bases(const sekv_config* cfg, const sekv_layer_cache* cache,
+                             const int32_t* expanded, const int32_t* n_expanded,
+                             void* staging, int64_t staging_per_group,
+                             int64_t* staged_off, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * sekv_decode_attention -- mixed-resolution attention of one layer for a
+ * given expansion list.  [DE]/[ZH] Methodik 3: sink, anchor and recent rows
+ * enter with their full K/V; an unexpanded span with body >= 1 enters once
+ * with its summary key/value and the size correction ln|S| added to its
+ * logit; an expanded span enters with every token of its body rebuilt from
+ * its basis, khat = U_K diag(sigma_K g_K) Vt_K (likewise vhat).  The kernel
+ * scores expanded spans in factor space and never forms khat or vhat.
+ *   q          bf16 [B][Hq][128]
+ *   expanded, n_expanded  ascending lists (device), e.g. from sekv_route
+ *   staging, staged_off   NULL: records are read from cache->store (device);
+ *                         else the record of list entry e of group g is at
+ *                         staging + staged_off[g*max_spans + e]
+ *   scale      logit scale (1/sqrt(128) for standard attention)
+ *   out        f32 [B][Hq][128]; lse f32 [B][Hq] (natural log; may be NULL)
+ */
+sekv_status sekv_decode_attention(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                  const void* q, const int32_t* expanded,
+                                  const int32_t* n_expanded, const void* staging,
+                                  const int64_t* staged_off, float scale, float* out,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/*
+ * sekv_decode_step -- routing and mixed-resolution attention of one layer in
+ * one kernel, bases read from device memory (cache->store_on_host == 0).
+ * Same results as sekv_route followed by sekv_decode_attention.  Optional
+ * outputs expanded/n_expanded (NULL to skip) receive the ascending lists.
+ */
+sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
+                             const void* q, const float* W_r, const float* theta,
+                             float scale, float* out, float* lse, int32_t* expanded,
+                             int32_t* n_expanded, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/* Human-readable name of a status. */
+const char* sekv_status_string(sekv_status status);
+
+/* Number of kernels the last successful call on this thread launched. */
+int32_t sekv_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEKV_H_ */
