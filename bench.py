@@ -1,0 +1,521 @@
+"""Decode-step benchmark of the SeKV span-cache hot path on GB300.
+
+One step = routing + mixed-resolution attention of every layer, in layer
+order, for one decode token (Llama-3-8B shape at 128K context: 32 layers, 32
+query / 8 KV heads, about 5% of spans expanded), inputs resident in HBM, all
+32 fused launches captured in one CUDA graph.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sekv|reference]
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = steps of all ranks / max time.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (there is no other implementation of this method to run).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import gen  # noqa: E402
+
+METRIC = "decode steps/s at 128K ctx; achieved HBM GB/s vs ~8 TB/s roofline"
+UNIT = "steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="sekv", choices=["sekv", "reference"])
+    ap.add_argument("--config", default="llama3_8b_128k")
+    ap.add_argument("--layers", type=int, default=0, help="override layer count (tests only)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# peaks and clocks
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(d, lst, cnt, cfg) -> int:
+    """Bytes the method must touch for one layer (one launch of the kernel).
+
+    Per (sequence, KV head): 512 B per full-resolution row (K + V bf16),
+    256 + 16 B per span (routing summary fp32 + body length, ranks and record
+    offset), 512 B per unexpanded non-empty span (summary K + V bf16), and per
+    expanded span its factors: U_K, U_V (b x r bf16), Vt_K, Vt_V (r x 128 bf16),
+    sigma and g (r fp32 each), for keys and values.  Padding, record headers and
+    the masked summary rows of expanded spans are not counted.
+    """
+    B, Hkv, ms = cfg.batch, cfg.n_kv_heads, cfg.max_spans
+    n_sp = d["n_spans"].long()                                        # [B]
+    body = d["body_len"].long()                                       # [B][ms]
+    nonempty = (body > 0).sum(1)                                      # [B]
+    n_full = cfg.n_sink + n_sp + cfg.n_recent
+    cnt = cnt.view(B, Hkv).long()
+    fixed = (512 * n_full[:, None] + 272 * n_sp[:, None] + 512 * (nonempty[:, None] - cnt)).sum()
+    lst = lst.view(B, Hkv, ms).long()
+    idx = torch.arange(ms, device=lst.device)[None, None, :]
+    valid = idx < cnt[:, :, None]
+    k = torch.where(valid, lst, torch.zeros_like(lst))
+    bb = torch.gather(body[:, None, :].expand(B, Hkv, ms), 2, k)
+    rr = torch.gather(d["rec_rank"].long(), 2, k)
+    r_sum = (rr & 0xFFFF) + ((rr >> 16) & 0xFFFF)
+    fac = (2 * bb * r_sum + 264 * r_sum) * valid
+    return int((fixed + fac.sum()).item())
+
+
+def record_bytes_fetched(d, lst, cnt, cfg) -> int:
+    B, Hkv, ms = cfg.batch, cfg.n_kv_heads, cfg.max_spans
+    cnt = cnt.view(B, Hkv).long()
+    lst = lst.view(B, Hkv, ms).long()
+    idx = torch.arange(ms, device=lst.device)[None, None, :]
+    valid = idx < cnt[:, :, None]
+    k = torch.where(valid, lst, torch.zeros_like(lst))
+    bb = torch.gather(d["body_len"].long()[:, None, :].expand(B, Hkv, ms), 2, k)
+    rr = torch.gather(d["rec_rank"].long(), 2, k)
+    return int((gen.record_size(bb, rr & 0xFFFF, (rr >> 16) & 0xFFFF) * valid).sum().item())
+
+
+def build_workload(sk, w, dev, n_layers):
+    ms = gen.max_spans_for(w)
+    cfg = sk.Config(w.batch, w.n_q_heads, w.n_kv_heads, w.n_sink, w.n_recent, ms, w.rank_cap,
+                    w.len_min, w.len_max, w.tau, flags=sk.sekv.FLAG_OVERLAP_PREVIOUS)
+    ws = sk.Workspace(cfg, dev)
+    p_head = gen.per_head_fraction(w.expand_frac, w.group)
+    layers = []
+    for l in range(n_layers):
+        d = gen.decode_cache(w, l, device=dev, max_spans=ms)
+        tens = {k: v for k, v in d.items() if isinstance(v, torch.Tensor)}
+        cache = sk.LayerCache(tens)
+        g = gen._gen(w.seed * 7919 + 101 * l + 1, dev)
+        q = gen.query(g, w.batch, w.n_q_heads, dev)
+        W = gen.routing_weights(g, w.n_kv_heads, dev).contiguous()
+        inf = torch.full((w.n_q_heads,), float("inf"), device=dev)
+        _, _, z = sk.route(cfg, cache, q, W, inf, ws, want_z=True)
+        z = z.view(w.batch, w.n_q_heads, ms).cpu().numpy()
+        nsp = d["n_spans"].cpu().numpy()
+        theta = np.array([gen.pick_threshold(np.concatenate([z[b, h, :nsp[b]]
+                                                             for b in range(w.batch)]), p_head)
+                          for h in range(w.n_q_heads)], np.float32)
+        theta_t = torch.from_numpy(theta).to(dev)
+        lst, cnt, _ = sk.route(cfg, cache, q, W, theta_t, ws)
+        nbytes = algorithmic_bytes(tens, lst, cnt, cfg)
+        fetched = record_bytes_fetched(tens, lst, cnt, cfg)
+        n_ne = int((d["body_len"] > 0).sum().item()) * w.n_kv_heads
+        layers.append(dict(t=tens, cache=cache, q=q, W=W, theta=theta_t, theta_np=theta,
+                           out=torch.empty(w.batch, w.n_q_heads, 128, device=dev),
+                           lse=torch.empty(w.batch, w.n_q_heads, device=dev),
+                           bytes=nbytes, fetched=fetched, n_exp=int(cnt.sum().item()),
+                           n_nonempty=n_ne))
+    torch.cuda.synchronize()
+    ws.raise_on_error()
+    return cfg, ws, layers
+
+
+# ----------------------------------------------------------------------------
+# timed runs
+# ----------------------------------------------------------------------------
+
+def time_graph(step_fn, steps, warmup, stream, ws_n, clocks=None):
+    with torch.cuda.stream(stream):
+        step_fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step_fn()
+    for _ in range(max(warmup, 3)):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    ck = clocks.stop() if clocks else None
+    return e0.elapsed_time(e1), ck
+
+
+def run_resident(sk, cfg, ws, layers, steps, warmup, ws_n, clocks):
+    scale = sk.default_scale()
+
+    def step():
+        for L in layers:
+            sk.decode_step(cfg, L["cache"], L["q"], L["W"], L["theta"], scale, ws,
+                           out=L["out"], lse=L["lse"])
+
+    stream = torch.cuda.Stream()
+    ms, ck = time_graph(step, steps, warmup, stream, ws_n, clocks)
+    code, detail = ws.status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail}) after the timed run")
+    return ms, ck
+
+
+def run_tiered(sk, cfg, layers, steps, warmup, ws_n, dev):
+    """End to end through the C ABI: per step, every layer's query goes H2D from
+    pinned memory, routing runs on the GPU, the expanded spans' bases are
+    fetched from the pinned host tier over the host link, attention runs on
+    the staged bases, and the outputs come back D2H."""
+    scale = sk.default_scale()
+    cfg_t = sk.Config(**{**cfg.__dict__, "flags": 0})
+    ws = sk.Workspace(cfg_t, dev)
+    L_n, B, Hq = len(layers), cfg.batch, cfg.n_q_heads
+    NG = B * cfg.n_kv_heads
+    q_host = torch.stack([L["q"].cpu() for L in layers]).pin_memory()
+    q_dev = torch.empty_like(q_host, device=dev)
+    out_dev = torch.empty(L_n, B, Hq, 128, device=dev)
+    out_host = torch.empty(L_n, B, Hq, 128).pin_memory()
+    caches = []
+    for L in layers:
+        host = dict(L["t"])
+        host["store"] = L["t"]["store"].cpu().pin_memory()
+        caches.append(sk.LayerCache(host, store_on_host=True))
+    per_group = 16 << 20
+    staging = torch.empty(NG * per_group, dtype=torch.uint8, device=dev)
+    staged_off = torch.empty(NG * cfg.max_spans, dtype=torch.int64, device=dev)
+    lst = torch.empty(NG * cfg.max_spans, dtype=torch.int32, device=dev)
+    cnt = torch.empty(NG, dtype=torch.int32, device=dev)
+    launches = [0]
+
+    def step():
+        n = 0
+        q_dev.copy_(q_host, non_blocking=True)
+        for i, L in enumerate(layers):
+            sk.route(cfg_t, caches[i], q_dev[i], L["W"], L["theta"], ws, expanded=lst,
+                     n_expanded=cnt)
+            n += sk.last_launch_count()
+            sk.fetch_bases(cfg_t, caches[i], lst, cnt, staging, per_group, staged_off, ws)
+            n += sk.last_launch_count()
+            sk.decode_attention(cfg_t, caches[i], q_dev[i], lst, cnt, scale, ws,
+                                staging=staging, staged_off=staged_off, out=out_dev[i])
+            n += sk.last_launch_count()
+        out_host.copy_(out_dev, non_blocking=True)
+        launches[0] = n
+
+    stream = torch.cuda.Stream()
+    ms, _ = time_graph(step, steps, warmup, stream, ws_n, None)
+    code, detail = ws.status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail}) after the tiered run")
+    ref = torch.stack([L["out"] for L in layers]).cpu()
+    err = float((out_host - ref).abs().max())
+    h2d = q_host.numel() * 2 + sum(L["fetched"] for L in layers)
+    d2h = out_host.numel() * 4
+    return ms, h2d, d2h, launches[0], err
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (bench's cpu_baseline leg and the --impl reference arm)
+# ----------------------------------------------------------------------------
+
+def _group_arrays(arr, b, c):
+    """ABI arrays of one (sequence, KV head) as a batch-1, one-KV-head layer."""
+    out = dict(arr)
+    out["n_spans"] = arr["n_spans"][b:b + 1]
+    out["body_len"] = arr["body_len"][b:b + 1]
+    for k in ("k_full", "v_full", "s_route", "k_sum", "v_sum", "rec_off", "rec_rank"):
+        out[k] = arr[k][b:b + 1, c:c + 1]
+    return out
+
+
+def oracle_sample(w, layer_arrays, seconds: float):
+    """Time the oracle's routing + attention on (layer, group) units until
+    `seconds` of CPU work; returns (mean seconds per unit, units, description).
+
+    Thresholds for each unit are placed with the oracle's own logits (same
+    recipe as the GPU run: per-head quantile with a 1e-3 margin)."""
+    import oracle
+    from oracle import layout
+    G = w.group
+    p_head = gen.per_head_fraction(w.expand_frac, G)
+    times = []
+    t_start = time.perf_counter()
+    unit = 0
+    for (l, arr, q, W) in layer_arrays:
+        for b in range(w.batch):
+            for c in range(w.n_kv_heads):
+                sub = _group_arrays(arr, b, c)
+                cache = layout.unpack_layer(sub, w.n_sink, w.n_recent)
+                qg = q[b:b + 1, c * G:(c + 1) * G]
+                Wg = W[c:c + 1]
+                z = oracle.route_logits(qg, Wg, cache)
+                theta = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)])
+                t0 = time.perf_counter()
+                E, _ = oracle.route(qg, Wg, cache, theta)
+                oracle.decode_attention(qg, cache, E, 1.0 / math.sqrt(128.0))
+                times.append(time.perf_counter() - t0)
+                unit += 1
+                if time.perf_counter() - t_start > seconds:
+                    break
+            else:
+                continue
+            break
+        else:
+            continue
+        break
+    desc = (f"oracle routing + attention (fp64 numpy) on {unit} (layer, sequence, KV head) "
+            f"units of the workload, first layer(s) in order; steps/s = 1 / (mean unit time "
+            f"x {w.batch * w.n_kv_heads} units x {w.layers} layers)")
+    return float(np.mean(times)), unit, desc
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, w, ws_n, rank):
+    """The oracle, as it stands, on host cores.  Each step is one (layer,
+    sequence, KV head) unit of the workload (units of the first layer,
+    reused cyclically); the full-step time is extrapolated from the mean."""
+    if rank != 0:
+        return
+    import oracle
+    from oracle import layout
+    from synth.gen import abi_to_numpy
+    G = w.group
+    p_head = gen.per_head_fraction(w.expand_frac, G)
+    d = gen.decode_cache(w, 0, device="cpu")
+    g = gen._gen(w.seed * 7919 + 1)
+    q = gen.query(g, w.batch, w.n_q_heads).float().numpy()
+    W = gen.routing_weights(g, w.n_kv_heads).numpy()
+    arr = abi_to_numpy(d)
+    units = []
+    for b in range(w.batch):
+        for c in range(w.n_kv_heads):
+            if len(units) >= min(8, args.steps + args.warmup):
+                break
+            cache = layout.unpack_layer(_group_arrays(arr, b, c), w.n_sink, w.n_recent)
+            qg, Wg = q[b:b + 1, c * G:(c + 1) * G], W[c:c + 1]
+            z = oracle.route_logits(qg, Wg, cache)
+            theta = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)])
+            units.append((cache, qg, Wg, theta))
+    times = []
+    for i in range(args.warmup + args.steps):
+        cache, qg, Wg, theta = units[i % len(units)]
+        t0 = time.perf_counter()
+        E, _ = oracle.route(qg, Wg, cache, theta)
+        oracle.decode_attention(qg, cache, E, 1.0 / math.sqrt(128.0))
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = float(np.mean(times)) * w.batch * w.n_kv_heads * w.layers
+    value = 1.0 / per_step
+    desc = (f"oracle routing + attention (fp64 numpy), {args.steps} timed units of one "
+            f"(layer, sequence, KV head) each, cycling over {len(units)} units of layer 0; "
+            f"steps/s = 1 / (mean unit time x {w.batch * w.n_kv_heads} units x {w.layers} layers)")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch,
+                       "ctx": w.ctx, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                       "expand_frac": w.expand_frac},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    ws_n, rank, local = dist_setup(args)
+    w = synth.get_config(args.config)
+    if args.layers:
+        w = synth.get_config(args.config, layers=args.layers)
+    if args.impl == "reference":
+        run_reference(args, w, ws_n, rank)
+        return
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (sekv) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg, ws, layers = build_workload(sk, w, dev, w.layers)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    ms_total, ck = run_resident(sk, cfg, ws, layers, args.steps, args.warmup, ws_n, clocks)
+    ms_total = max_over_ranks(ms_total, ws_n)
+    ms_step = ms_total / args.steps
+    value = ws_n * args.steps / (ms_total / 1e3)
+    bytes_step = sum(L["bytes"] for L in layers)
+    per_launch = bytes_step / len(layers)
+    launch_s = ms_total / 1e3 / (args.steps * len(layers))
+    peak, peak_kind = measured_peaks()
+    achieved = per_launch / launch_s / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "ctx": w.ctx,
+                       "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                       "expand_frac_target": w.expand_frac,
+                       "expand_frac": sum(L["n_exp"] for L in layers) /
+                       max(1, sum(L["n_nonempty"] for L in layers)),
+                       "bases": "hbm-resident", "l2": "inputs larger than L2 "
+                       f"({bytes_step / 1e9:.2f} GB touched per step, distinct per layer)",
+                       "parallelism": f"replicas x{ws_n}",
+                       "graph": "one CUDA graph per step, programmatic dependent launch"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": peak_kind, "kernel": "sekv::decode_kernel",
+                         "bytes_per_launch": per_launch,
+                         "avg_launch_us": launch_s * 1e6},
+            "clocks": ck, "gpu_launches": args.steps * len(layers)}
+    if not args.no_e2e:
+        e_steps = max(10, args.steps // 4)
+        ms_e, h2d, d2h, nl, err = run_tiered(sk, cfg, layers, e_steps, args.warmup, ws_n, dev)
+        ms_e = max_over_ranks(ms_e, ws_n)
+        line["e2e"] = {"value": ws_n * e_steps / (ms_e / 1e3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "path": "tiered: q H2D, route, fetch bases from pinned host over the "
+                               "host link, attend, out D2H; one CUDA graph per step",
+                       "h2d_gbs": h2d / (ms_e / e_steps / 1e3) / 1e9,
+                       "steps": e_steps, "max_abs_vs_resident": err}
+        line["gpu_launches"] += e_steps * nl
+    if not args.no_cpu_baseline and rank == 0:
+        from synth.gen import abi_to_numpy
+        la = []
+        for l in range(min(2, len(layers))):
+            L = layers[l]
+            la.append((l, abi_to_numpy(L["t"]), L["q"].float().cpu().numpy(),
+                       L["W"].cpu().numpy()))
+        mean_t, units, desc = oracle_sample(w, la, args.cpu_seconds)
+        v = 1.0 / (mean_t * w.batch * w.n_kv_heads * w.layers)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

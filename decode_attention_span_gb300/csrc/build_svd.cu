@@ -1,0 +1,369 @@
+// Batched truncated SVD of span bodies (one CTA per body, persistent CTAs).
+//
+// SeKV, technical summary, Methodik 2 (gist.science, German page) / 方法论 2
+// (Chinese page): each span keeps a low-rank SVD basis whose components
+// carry soft gates.  For a body M (b x 128, bf16) the kernel forms the Gram
+// matrix on the small side (M M^T when b <= 128, else M^T M), diagonalises it
+// with the cyclic Jacobi method (Jacobi 1846; rotation formulas as in Golub &
+// Van Loan, "Matrix Computations", the symmetric Schur decomposition),
+// takes sigma_j = sqrt(lambda_j) in descending order, recovers the other
+// factor by projection (v_j = M^T u_j / sigma_j, resp. u_j = M v_j / sigma_j),
+// flips each pair so that the largest-magnitude entry of v_j is positive,
+// and writes the gated rank-r part into the span's record.
+#include "build.cuh"
+
+namespace sekv {
+
+namespace {
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) s += red[w];
+  return s;
+}
+
+// Circle-method pairing: round r of a tournament among nn (even) players;
+// pair k in [0, nn/2).
+__device__ __forceinline__ void jacobi_pair(int nn, int r, int k, int& p, int& q) {
+  const int m = nn - 1;
+  if (k == 0) {
+    p = nn - 1;
+    q = r;
+  } else {
+    p = (r + k) % m;
+    q = (r - k + m) % m;
+  }
+  if (p > q) {
+    const int t = p;
+    p = q;
+    q = t;
+  }
+}
+
+}  // namespace
+
+template <int NMAX, int NT, bool LARGE>
+__global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  constexpr int LD = NMAX + 1;
+  constexpr int MROWS = LARGE ? 32 : NMAX;                    // body rows staged at once
+  float* G = reinterpret_cast<float*>(sm);                    // NMAX x LD
+  float* Q = G + NMAX * LD;                                   // NMAX x LD (eigenvectors)
+  __nv_bfloat16* Ms = reinterpret_cast<__nv_bfloat16*>(Q + NMAX * LD);  // MROWS x 128
+  float* Vs = reinterpret_cast<float*>(Ms + MROWS * kHeadDim);          // LARGE: rank x 128
+  float* aux = Vs + (LARGE ? P.rank_cap * kHeadDim : 0);
+  float* cs = aux;             // [NMAX/2 + 1]
+  float* sn = cs + 72;
+  int* pp = reinterpret_cast<int*>(sn + 72);
+  int* qq = pp + 72;
+  int* ord = qq + 72;          // [NMAX]
+  float* red = reinterpret_cast<float*>(ord + 136);  // [32]
+  __shared__ int s_item;
+  const int tid = threadIdx.x;
+  const int count = P.counters[cls];
+  const int32_t* list = P.cls_list + size_t(cls) * P.cls_cap;
+
+  for (;;) {
+    __syncthreads();
+    if (tid == 0) s_item = atomicAdd(&P.counters[4 + cls], 1);
+    __syncthreads();
+    const int item = s_item;
+    if (item >= count || item >= P.cls_cap) break;
+    const int code = list[item];
+    const int which = code & 1;
+    const size_t gk = size_t(code >> 1);
+    const int g = int(gk / P.max_spans), k = int(gk % P.max_spans);
+    const int b = g / P.Hkv;
+    const int bl = P.body_len[size_t(b) * P.max_spans + k];
+    const int rank = P.rec_rank[gk];
+    const int rK = rank & 0xffff, rV = (rank >> 16) & 0xffff;
+    const int r = which ? rV : rK;
+    const int t0 = P.starts[size_t(b) * P.max_spans + k] + 1;
+    const __nv_bfloat16* M = (which ? P.V : P.K) + (size_t(g) * P.T + t0) * kHeadDim;
+    const int n = LARGE ? kHeadDim : bl;
+    uint8_t* rec = P.store + P.gbase[g] + P.rel_off[gk];
+
+    // ---- Gram matrix on the small side -----------------------------------
+    if (!LARGE) {
+      const int4* src = reinterpret_cast<const int4*>(M);
+      int4* dst = reinterpret_cast<int4*>(Ms);
+      for (int i = tid; i < bl * 16; i += NT) dst[i] = src[i];
+      __syncthreads();
+      for (int e = tid; e < n * n; e += NT) {
+        const int i = e / n, j = e % n;
+        if (j < i) continue;
+        const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(Ms + i * kHeadDim);
+        const __nv_bfloat162* c = reinterpret_cast<const __nv_bfloat162*>(Ms + j * kHeadDim);
+        float acc = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < kHeadDim / 2; ++d) {
+          const float2 x = __bfloat1622float2(a[(d + i) & 63]);
+          const float2 y = __bfloat1622float2(c[(d + i) & 63]);
+          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+        G[i * LD + j] = acc;
+        G[j * LD + i] = acc;
+      }
+    } else {
+      // M^T M (128 x 128), rows streamed through Ms in chunks of NMAX rows
+      constexpr int PAIRS = (kHeadDim * (kHeadDim + 1) / 2 + NT - 1) / NT;
+      float acc[PAIRS];
+      int pi[PAIRS], pj[PAIRS];
+#pragma unroll
+      for (int t = 0; t < PAIRS; ++t) {
+        acc[t] = 0.f;
+        int e = tid + t * NT, i = 0;
+        // map e to (i, j) with i <= j in the upper triangle, row-major
+        while (e >= kHeadDim - i && i < kHeadDim) {
+          e -= kHeadDim - i;
+          ++i;
+        }
+        pi[t] = i;
+        pj[t] = i + e;
+      }
+      for (int r0 = 0; r0 < bl; r0 += MROWS) {
+        const int rows = min(MROWS, bl - r0);
+        __syncthreads();
+        const int4* src = reinterpret_cast<const int4*>(M + size_t(r0) * kHeadDim);
+        int4* dst = reinterpret_cast<int4*>(Ms);
+        for (int i = tid; i < rows * 16; i += NT) dst[i] = src[i];
+        __syncthreads();
+        for (int rr = 0; rr < rows; ++rr) {
+          const __nv_bfloat16* row = Ms + rr * kHeadDim;
+#pragma unroll
+          for (int t = 0; t < PAIRS; ++t)
+            if (pi[t] < kHeadDim)
+              acc[t] = fmaf(__bfloat162float(row[pi[t]]), __bfloat162float(row[pj[t]]), acc[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < PAIRS; ++t)
+        if (pi[t] < kHeadDim) {
+          G[pi[t] * LD + pj[t]] = acc[t];
+          G[pj[t] * LD + pi[t]] = acc[t];
+        }
+    }
+    for (int e = tid; e < n * n; e += NT) Q[(e / n) * LD + (e % n)] = (e / n == e % n) ? 1.f : 0.f;
+    __syncthreads();
+
+    // ---- cyclic Jacobi, parallel (tournament) ordering ---------------------
+    const int nn = (n + 1) & ~1;
+    for (int sweep = 0; sweep < 24; ++sweep) {
+      float off = 0.f, dg = 0.f;
+      for (int e = tid; e < n * n; e += NT) {
+        const int i = e / n, j = e % n;
+        const float v = G[i * LD + j];
+        if (i == j) dg += v * v; else off += v * v;
+      }
+      off = block_sum(off, red);
+      dg = block_sum(dg, red);
+      if (!(off > 1e-14f * dg)) break;
+      for (int rd = 0; rd < nn - 1; ++rd) {
+        __syncthreads();
+        for (int kk = tid; kk < nn / 2; kk += NT) {
+          int p, q;
+          jacobi_pair(nn, rd, kk, p, q);
+          float c = 1.f, s = 0.f;
+          if (q < n) {
+            const float apq = G[p * LD + q];
+            if (apq != 0.f) {
+              const float theta = (G[q * LD + q] - G[p * LD + p]) / (2.f * apq);
+              float t;
+              if (fabsf(theta) > 1e18f) {
+                t = 0.5f / theta;
+              } else {
+                t = 1.f / (fabsf(theta) + sqrtf(theta * theta + 1.f));
+                if (theta < 0.f) t = -t;
+              }
+              c = 1.f / sqrtf(t * t + 1.f);
+              s = t * c;
+            }
+          }
+          cs[kk] = c;
+          sn[kk] = s;
+          pp[kk] = p;
+          qq[kk] = q;
+        }
+        __syncthreads();
+        // rows: (J^T A)
+        for (int e = tid; e < (nn / 2) * n; e += NT) {
+          const int kk = e / n, j = e % n;
+          const int p = pp[kk], q = qq[kk];
+          if (q >= n) continue;
+          const float c = cs[kk], s = sn[kk];
+          const float gp = G[p * LD + j], gq = G[q * LD + j];
+          G[p * LD + j] = c * gp - s * gq;
+          G[q * LD + j] = s * gp + c * gq;
+        }
+        __syncthreads();
+        // columns: (A J) and the eigenvectors (Q J)
+        for (int e = tid; e < (nn / 2) * n; e += NT) {
+          const int kk = e / n, i = e % n;
+          const int p = pp[kk], q = qq[kk];
+          if (q >= n) continue;
+          const float c = cs[kk], s = sn[kk];
+          const float gp = G[i * LD + p], gq = G[i * LD + q];
+          G[i * LD + p] = c * gp - s * gq;
+          G[i * LD + q] = s * gp + c * gq;
+          const float vp = Q[i * LD + p], vq = Q[i * LD + q];
+          Q[i * LD + p] = c * vp - s * vq;
+          Q[i * LD + q] = s * vp + c * vq;
+        }
+      }
+      __syncthreads();
+    }
+    __syncthreads();
+    // ---- order eigenvalues descending (ties by index) ----------------------
+    for (int i = tid; i < n; i += NT) {
+      const float li = G[i * LD + i];
+      int rk = 0;
+      for (int m = 0; m < n; ++m) {
+        const float lm = G[m * LD + m];
+        rk += (lm > li) || (lm == li && m < i);
+      }
+      ord[rk] = i;
+    }
+    __syncthreads();
+
+    // ---- factors, signs, record -------------------------------------------
+    const int r4v = r4(r);
+    uint8_t* part;       // sigma/g/Vt of this side
+    __nv_bfloat16* Ud;   // U of this side
+    if (which == 0) {
+      if (tid == 0) {
+        int4* h = reinterpret_cast<int4*>(rec);
+        *h = make_int4(bl, rK, rV, 0);
+        P.rec_off[gk] = P.gbase[g] + P.rel_off[gk];
+      }
+      part = rec + 16;
+      Ud = reinterpret_cast<__nv_bfloat16*>(rec + 16 + 8 * r4(rK) + 256 * rK);
+    } else {
+      uint8_t* uk = rec + 16 + 8 * r4(rK) + 256 * rK;
+      Ud = reinterpret_cast<__nv_bfloat16*>(uk + pad16(2 * int64_t(bl) * rK));
+      part = reinterpret_cast<uint8_t*>(Ud) + pad16(2 * int64_t(bl) * rV);
+    }
+    float* sig = reinterpret_cast<float*>(part);
+    float* gat = sig + r4v;
+    __nv_bfloat16* Vt = reinterpret_cast<__nv_bfloat16*>(part + 8 * r4v);
+    const float* gin = P.gates + ((size_t(b) * P.Hkv + (g % P.Hkv)) * 2 * P.max_spans +
+                                  size_t(which) * P.max_spans + k) * P.rank_cap;
+    for (int j = tid; j < r4v; j += NT) {
+      const float lam = j < r ? G[ord[j] * LD + ord[j]] : 0.f;
+      sig[j] = j < r ? sqrtf(fmaxf(lam, 0.f)) : 0.f;
+      gat[j] = j < r ? gin[j] : 0.f;
+    }
+    // zero the padding tail of U (16-byte rounding)
+    {
+      const int64_t ub = 2 * int64_t(bl) * r, up = pad16(ub);
+      for (int64_t x = ub + tid; x < up; x += NT) reinterpret_cast<uint8_t*>(Ud)[x] = 0;
+    }
+    for (int j = 0; j < r; ++j) {
+      const int col = ord[j];
+      const float sj = sqrtf(fmaxf(G[col * LD + col], 0.f));
+      const float inv = sj > 1e-30f ? 1.f / sj : 0.f;
+      // v_j (128 dims): projection (small side) or the eigenvector (large side)
+      float v[(kHeadDim + NT - 1) / NT];
+      float best = -1.f;
+      int bidx = kHeadDim;
+#pragma unroll
+      for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t) {
+        const int d = tid + t * NT;
+        float x = 0.f;
+        if (d < kHeadDim) {
+          if (!LARGE) {
+            for (int i = 0; i < bl; ++i)
+              x = fmaf(Q[i * LD + col], __bfloat162float(Ms[i * kHeadDim + d]), x);
+            x *= inv;
+          } else {
+            x = sj > 1e-30f ? Q[d * LD + col] : 0.f;
+          }
+          if (fabsf(x) > best || (fabsf(x) == best && d < bidx)) {
+            best = fabsf(x);
+            bidx = d;
+          }
+        }
+        v[t] = x;
+      }
+      // arg max |v_j| over the block (lowest index on ties)
+      {
+        const int lane = tid & 31, wid = tid >> 5;
+        for (int o = 16; o; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+          if (ob > best || (ob == best && oi < bidx)) {
+            best = ob;
+            bidx = oi;
+          }
+        }
+        __syncthreads();
+        if (lane == 0) {
+          red[wid] = best;
+          reinterpret_cast<int*>(red)[16 + wid] = bidx;
+        }
+        __syncthreads();
+        best = red[0];
+        bidx = reinterpret_cast<int*>(red)[16];
+        for (int w = 1; w < NT / 32; ++w) {
+          const float ob = red[w];
+          const int oi = reinterpret_cast<int*>(red)[16 + w];
+          if (ob > best || (ob == best && oi < bidx)) {
+            best = ob;
+            bidx = oi;
+          }
+        }
+      }
+      // sign of the winning entry: recompute it from the owner's value
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t)
+        if (tid + t * NT == bidx) red[8] = v[t];
+      __syncthreads();
+      const float sgn = red[8] < 0.f ? -1.f : 1.f;
+#pragma unroll
+      for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t) {
+        const int d = tid + t * NT;
+        if (d < kHeadDim) {
+          Vt[j * kHeadDim + d] = __float2bfloat16_rn(sgn * v[t]);
+          if (LARGE) Vs[j * kHeadDim + d] = sgn * v[t];
+        }
+      }
+      if (!LARGE) {
+        for (int i = tid; i < bl; i += NT) Ud[size_t(i) * r + j] = __float2bfloat16_rn(sgn * Q[i * LD + col]);
+      }
+    }
+    if (LARGE && r > 0) {
+      // u_j = M v_j / sigma_j, rows streamed through Ms
+      __syncthreads();
+      for (int r0 = 0; r0 < bl; r0 += MROWS) {
+        const int rows = min(MROWS, bl - r0);
+        __syncthreads();
+        const int4* src = reinterpret_cast<const int4*>(M + size_t(r0) * kHeadDim);
+        int4* dst = reinterpret_cast<int4*>(Ms);
+        for (int i = tid; i < rows * 16; i += NT) dst[i] = src[i];
+        __syncthreads();
+        for (int e = tid; e < rows * r; e += NT) {
+          const int i = e / r, j = e % r;
+          const int col = ord[j];
+          const float sj = sqrtf(fmaxf(G[col * LD + col], 0.f));
+          float acc = 0.f;
+          for (int d = 0; d < kHeadDim; ++d)
+            acc = fmaf(__bfloat162float(Ms[i * kHeadDim + d]), Vs[j * kHeadDim + d], acc);
+          Ud[size_t(r0 + i) * r + j] = __float2bfloat16_rn(sj > 1e-30f ? acc / sj : 0.f);
+        }
+      }
+    }
+  }
+}
+
+template __global__ void svd_kernel<32, 64, false>(const BuildParams, int);
+template __global__ void svd_kernel<64, 128, false>(const BuildParams, int);
+template __global__ void svd_kernel<128, 256, false>(const BuildParams, int);
+template __global__ void svd_kernel<128, 256, true>(const BuildParams, int);
+
+}  // namespace sekv

@@ -239,6 +239,50 @@ sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cac
                              int32_t* n_expanded, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
 
+/* Outputs of sekv_build_spans: one layer of the cache (layouts as in
+ * sekv_layer_cache; every array with its full capacity) plus the device
+ * basis store and its capacity in bytes. */
+typedef struct sekv_cache_out {
+  int32_t* n_spans;
+  int32_t* body_len;
+  void* k_full;
+  void* v_full;
+  float* s_route;
+  void* k_sum;
+  void* v_sum;
+  int64_t* rec_off;
+  int32_t* rec_rank;
+  void* store;
+  int64_t store_capacity;
+} sekv_cache_out;
+
+/*
+ * sekv_build_spans -- prefill build of one layer's span cache.
+ * [DE]/[ZH] Methodik 1: surprisal H_t = -log p(x_t | x_<t) from the prefill
+ * pass (an input here) marks span boundaries; boundary tokens are anchors kept
+ * at full resolution; a span is the run of tokens between two anchors.
+ * Readings: the first middle token (index n_sink) opens span 0; token t opens
+ * a new span iff (H_t > tau and t - s >= len_min) or t - s == len_max, s the
+ * current span's anchor; the last span ends at ctx_len - n_recent.
+ * [DE]/[ZH] Methodik 2: per span a routing summary s = u / |u| with
+ * u = sum_i H_i W_r k_i over the body, summary key/value = the body means
+ * (bf16, round to nearest even), and a truncated SVD basis per K and V with
+ * the caller's soft gates: rank = longest prefix of components (descending
+ * sigma) whose gate exceeds 0.5, at most min(rank_cap, |S|).
+ *   K, V   bf16 [B][Hkv][ctx_len][128]    H f32 [B][ctx_len]
+ *   W_r    f32 [Hkv][64][128]
+ *   gates  f32 [B][Hkv][2][max_spans][rank_cap] (index 0 keys, 1 values)
+ * Records are packed group by group in span order from the start of
+ * out->store.  More than max_spans spans in a sequence, or records beyond
+ * store_capacity, set a device status (SEKV_ERR_DEVICE from
+ * sekv_workspace_status); the cache is then incomplete.
+ * Workspace: sekv_workspace_size(cfg, SEKV_CALL_BUILD, ctx_len).
+ */
+sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len, const void* K,
+                             const void* V, const float* H, const float* W_r,
+                             const float* gates, const sekv_cache_out* out, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status. */
 const char* sekv_status_string(sekv_status status);
 
