@@ -14,6 +14,8 @@ from .sekv import (  # noqa: F401
     decode_attention,
     decode_step,
     fetch_bases,
+    build_spans,
+    alloc_cache,
     record_size,
     last_launch_count,
     default_scale,

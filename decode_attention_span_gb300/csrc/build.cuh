@@ -50,8 +50,7 @@ __global__ void seg_kernel(const BuildParams P);
 __global__ void plan_kernel(const BuildParams P);
 __global__ void gather_kernel(const BuildParams P);
 __global__ void summary_kernel(const BuildParams P);
-template <int NMAX, int NT, bool LARGE>
-__global__ void svd_kernel(const BuildParams P, int cls);
+cudaError_t launch_svd_all(const BuildParams& P, int sms, cudaStream_t stream);
 
 // shared memory bytes of one svd_kernel CTA
 __host__ __device__ constexpr int svd_smem_bytes(int nmax, bool large, int rcap) {

@@ -31,20 +31,6 @@ BuildWs build_ws(const sekv_config* cfg) {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <int NMAX, int NT, bool LARGE>
-cudaError_t launch_svd(const BuildParams& P, int cls, int sms, cudaStream_t stream) {
-  const int smem = svd_smem_bytes(NMAX, LARGE, P.rank_cap);
-  auto kern = svd_kernel<NMAX, NT, LARGE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  kern<<<sms * per_sm, NT, smem, stream>>>(P, cls);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 namespace sekv {
@@ -133,11 +119,7 @@ extern "C" sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len,
   gather_kernel<<<dim3(ng, 32), 256, 0, stream>>>(P);
   summary_kernel<<<dim3(cfg->max_spans / 8, ng), 256, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
-  if (launch_svd<32, 64, false>(P, 0, sms, stream) != cudaSuccess ||
-      launch_svd<64, 128, false>(P, 1, sms, stream) != cudaSuccess ||
-      launch_svd<128, 256, false>(P, 2, sms, stream) != cudaSuccess ||
-      launch_svd<128, 256, true>(P, 3, sms, stream) != cudaSuccess)
-    return SEKV_ERR_CUDA;
+  if (launch_svd_all(P, sms, stream) != cudaSuccess) return SEKV_ERR_CUDA;
   count_launch(8);
   return SEKV_OK;
 }

@@ -361,9 +361,29 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
   }
 }
 
-template __global__ void svd_kernel<32, 64, false>(const BuildParams, int);
-template __global__ void svd_kernel<64, 128, false>(const BuildParams, int);
-template __global__ void svd_kernel<128, 256, false>(const BuildParams, int);
-template __global__ void svd_kernel<128, 256, true>(const BuildParams, int);
+namespace {
+template <int NMAX, int NT, bool LARGE>
+cudaError_t launch_svd(const BuildParams& P, int cls, int sms, cudaStream_t stream) {
+  const int smem = svd_smem_bytes(NMAX, LARGE, P.rank_cap);
+  auto kern = svd_kernel<NMAX, NT, LARGE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  kern<<<sms * per_sm, NT, smem, stream>>>(P, cls);
+  return cudaGetLastError();
+}
+}  // namespace
+
+// One persistent launch per size class (the class lists come from plan_kernel).
+cudaError_t launch_svd_all(const BuildParams& P, int sms, cudaStream_t stream) {
+  cudaError_t e = launch_svd<32, 64, false>(P, 0, sms, stream);
+  if (e == cudaSuccess) e = launch_svd<64, 128, false>(P, 1, sms, stream);
+  if (e == cudaSuccess) e = launch_svd<128, 256, false>(P, 2, sms, stream);
+  if (e == cudaSuccess) e = launch_svd<128, 256, true>(P, 3, sms, stream);
+  return e;
+}
 
 }  // namespace sekv

@@ -452,10 +452,4 @@ extern "C" sekv_status sekv_fetch_bases(const sekv_config* cfg, const sekv_layer
   return SEKV_OK;
 }
 
-namespace sekv {
-size_t build_workspace_size(const sekv_config* cfg, int64_t ctx_len) {
-  (void)cfg;
-  (void)ctx_len;
-  return 0;
-}
-}  // namespace sekv
+

@@ -29,7 +29,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 # every symbol include/sekv.h declares
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
-           "sekv_decode_step", "sekv_status_string", "sekv_last_launch_count")
+           "sekv_decode_step", "sekv_build_spans", "sekv_status_string",
+           "sekv_last_launch_count")
 
 
 class SekvError(RuntimeError):
@@ -43,6 +44,12 @@ class SekvConfig(ctypes.Structure):
                 ("head_dim", _c_i32), ("route_dim", _c_i32), ("n_sink", _c_i32),
                 ("n_recent", _c_i32), ("max_spans", _c_i32), ("rank_cap", _c_i32),
                 ("len_min", _c_i32), ("len_max", _c_i32), ("tau", _c_f32), ("flags", _c_i32)]
+
+
+class SekvCacheOut(ctypes.Structure):
+    _fields_ = [("n_spans", _c_vp), ("body_len", _c_vp), ("k_full", _c_vp), ("v_full", _c_vp),
+                ("s_route", _c_vp), ("k_sum", _c_vp), ("v_sum", _c_vp), ("rec_off", _c_vp),
+                ("rec_rank", _c_vp), ("store", _c_vp), ("store_capacity", _c_i64)]
 
 
 class SekvLayerCache(ctypes.Structure):
@@ -91,6 +98,10 @@ def lib() -> ctypes.CDLL:
         L.sekv_decode_step.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_sz, _c_vp]
+        L.sekv_build_spans.restype = _c_i32
+        L.sekv_build_spans.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
+                                       _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_sz,
+                                       _c_vp]
         L.sekv_status_string.restype = ctypes.c_char_p
         L.sekv_status_string.argtypes = [_c_i32]
         L.sekv_last_launch_count.restype = _c_i32
@@ -286,6 +297,38 @@ def fetch_bases(cfg: Config, cache: LayerCache, expanded, n_expanded, staging, p
                                   _ptr(n_expanded), _ptr(staging), int(per_group),
                                   _ptr(staged_off), ws.ptr(), ws.nbytes, _stream(stream)))
     return staging, staged_off
+
+
+def alloc_cache(cfg: Config, store_bytes: int, device=None) -> Dict[str, torch.Tensor]:
+    """Zeroed tensors for one layer of the cache in the C-ABI layout."""
+    dev = device or "cuda"
+    B, Hkv, ms = cfg.batch, cfg.n_kv_heads, cfg.max_spans
+    cap = cfg.n_sink + ms + cfg.n_recent
+    z = lambda *shape, dt: torch.zeros(*shape, dtype=dt, device=dev)  # noqa: E731
+    return dict(n_spans=z(B, dt=torch.int32), body_len=z(B, ms, dt=torch.int32),
+                k_full=z(B, Hkv, cap, 128, dt=torch.bfloat16),
+                v_full=z(B, Hkv, cap, 128, dt=torch.bfloat16),
+                s_route=z(B, Hkv, ms, 64, dt=torch.float32),
+                k_sum=z(B, Hkv, ms, 128, dt=torch.bfloat16),
+                v_sum=z(B, Hkv, ms, 128, dt=torch.bfloat16),
+                rec_off=z(B, Hkv, ms, dt=torch.int64), rec_rank=z(B, Hkv, ms, dt=torch.int32),
+                store=z(store_bytes, dt=torch.uint8))
+
+
+def build_spans(cfg: Config, K, V, H, W_r, gates, out: Dict[str, torch.Tensor], ws: Workspace,
+                stream=None) -> Dict[str, torch.Tensor]:
+    """Prefill build of one layer into `out` (tensors from alloc_cache)."""
+    _need(K, "K", torch.bfloat16); _need(V, "V", torch.bfloat16)
+    _need(H, "H", torch.float32); _need(W_r, "W_r", torch.float32)
+    _need(gates, "gates", torch.float32)
+    T = K.shape[2]
+    o = SekvCacheOut(*[_ptr(out[k]) for k in CACHE_FIELDS], out["store"].numel())
+    c = cfg.c()
+    _check("sekv_build_spans",
+           lib().sekv_build_spans(ctypes.byref(c), T, _ptr(K), _ptr(V), _ptr(H), _ptr(W_r),
+                                  _ptr(gates), ctypes.byref(o), ws.ptr(), ws.nbytes,
+                                  _stream(stream)))
+    return out
 
 
 def default_scale() -> float:
