@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
     const int t0 = P.starts[size_t(b) * P.max_spans + k] + 1;
     const __nv_bfloat16* M = (which ? P.V : P.K) + (size_t(g) * P.T + t0) * kHeadDim;
     const int n = LARGE ? kHeadDim : bl;
+    // records past the store capacity are skipped (plan_kernel flagged them)
+    if (P.gbase[g] + P.rel_off[gk] + record_bytes(bl, rK, rV) > P.store_capacity) continue;
     uint8_t* rec = P.store + P.gbase[g] + P.rel_off[gk];
 
     // ---- Gram matrix on the small side -----------------------------------
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
     __syncthreads();
 
     // ---- factors, signs, record -------------------------------------------
-    const int r4v = r4(r);
+    const int r4v = r4(r), rs = r8(r);  // U rows hold r8(r) columns, the last ones zero
+    const RecordLayout RL = record_layout(bl, rK, rV);
     uint8_t* part;       // sigma/g/Vt of this side
     __nv_bfloat16* Ud;   // U of this side
     if (which == 0) {
@@ -242,11 +245,10 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
         P.rec_off[gk] = P.gbase[g] + P.rel_off[gk];
       }
       part = rec + 16;
-      Ud = reinterpret_cast<__nv_bfloat16*>(rec + 16 + 8 * r4(rK) + 256 * rK);
+      Ud = reinterpret_cast<__nv_bfloat16*>(rec + RL.uk);
     } else {
-      uint8_t* uk = rec + 16 + 8 * r4(rK) + 256 * rK;
-      Ud = reinterpret_cast<__nv_bfloat16*>(uk + pad16(2 * int64_t(bl) * rK));
-      part = reinterpret_cast<uint8_t*>(Ud) + pad16(2 * int64_t(bl) * rV);
+      part = rec + RL.vpart;
+      Ud = reinterpret_cast<__nv_bfloat16*>(rec + RL.uv);
     }
     float* sig = reinterpret_cast<float*>(part);
     float* gat = sig + r4v;
@@ -258,11 +260,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       sig[j] = j < r ? sqrtf(fmaxf(lam, 0.f)) : 0.f;
       gat[j] = j < r ? gin[j] : 0.f;
     }
-    // zero the padding tail of U (16-byte rounding)
-    {
-      const int64_t ub = 2 * int64_t(bl) * r, up = pad16(ub);
-      for (int64_t x = ub + tid; x < up; x += NT) reinterpret_cast<uint8_t*>(Ud)[x] = 0;
-    }
+    for (int e = tid; e < bl * (rs - r); e += NT)  // zero padding columns of U
+      Ud[size_t(e / (rs - r)) * rs + r + e % (rs - r)] = __float2bfloat16_rn(0.f);
     for (int j = 0; j < r; ++j) {
       const int col = ord[j];
       const float sj = sqrtf(fmaxf(G[col * LD + col], 0.f));
@@ -334,7 +333,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
         }
       }
       if (!LARGE) {
-        for (int i = tid; i < bl; i += NT) Ud[size_t(i) * r + j] = __float2bfloat16_rn(sgn * Q[i * LD + col]);
+        for (int i = tid; i < bl; i += NT) Ud[size_t(i) * rs + j] = __float2bfloat16_rn(sgn * Q[i * LD + col]);
       }
     }
     if (LARGE && r > 0) {
@@ -354,7 +353,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
           float acc = 0.f;
           for (int d = 0; d < kHeadDim; ++d)
             acc = fmaf(__bfloat162float(Ms[i * kHeadDim + d]), Vs[j * kHeadDim + d], acc);
-          Ud[size_t(r0 + i) * r + j] = __float2bfloat16_rn(sj > 1e-30f ? acc / sj : 0.f);
+          Ud[size_t(r0 + i) * rs + j] = __float2bfloat16_rn(sj > 1e-30f ? acc / sj : 0.f);
         }
       }
     }

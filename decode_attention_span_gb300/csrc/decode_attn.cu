@@ -93,9 +93,6 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
   const size_t gs = size_t(g) * P.max_spans;
   uint16_t* infoc = reinterpret_cast<uint16_t*>(smem + kOffInfo);
-  uint8_t* scratch = smem + kOffScratch + w * kScratchPerWarp;
-  float* cbuf = reinterpret_cast<float*>(scratch);
-  float* pbuf = reinterpret_cast<float*>(scratch + 2048);
   float* qs = reinterpret_cast<float*>(smem + kOffScratch);         // prologue only
   float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages only
 
@@ -115,8 +112,8 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   for (int t = 0; t < 16; ++t) A.o[t][0] = A.o[t][1] = 0.f;
   A.m_row = kNegInf;
   A.l_part = 0.f;
-#pragma unroll
-  for (int h = 0; h < 8; ++h) A.w[h][0] = A.w[h][1] = 0.f;
+  ExpAcc X;
+  X.had = false;
 
   if (P.fused) {
     for (int i = tid; i < 8 * kHeadDim; i += kConsumers)
@@ -143,7 +140,6 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
 
   int slot = 0;
   uint32_t phase = 0;
-  bool had = false;
   for (;;) {
     if (!mbar_wait(&ms->full[slot], phase, kWaitLimit)) {
       if (tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
@@ -178,16 +174,10 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       case PG_SUM:
         consume_kv_tile(A, pu, pu + 16384, d.n, infoc + (d.a - k0), P.scale_log2);
         break;
-      case PG_EXPA:
-        consume_expa(A, page, d.rk, cbuf, P.scale_log2);
-        had = false;
-        break;
-      case PG_EXPU:
-        had |= consume_expu(A, page, d.n, d.rk, d.rv, G, cbuf, pbuf);
-        break;
-      case PG_EXPB:
-        if (had) consume_expb(A, page, d.rv, G, scratch);
-        __syncwarp();
+      case PG_EXP:
+        if (d.off_a >= 0) exp_key(A, X, page + d.off_a, d.rk, P.scale_log2);
+        if (d.n > 0) exp_tokens(A, X, page + d.off_uk, page + d.off_uv, d.n, d.rk, d.rv);
+        if (d.off_b >= 0) exp_value(A, X, page + d.off_b, d.rv);
         break;
       default:
         break;

@@ -49,19 +49,19 @@ constexpr int kMiscBytes = 4096;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
-enum PageType : int {
-  PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4,
-  PG_EXPA = 5, PG_EXPU = 6, PG_EXPB = 7, PG_END = 8
-};
+enum PageType : int { PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4, PG_EXP = 5, PG_END = 6 };
 
 struct PageDesc {
   int type;
-  int n;      // rows / spans in this page
-  int a;      // first row / span ordinal / first U row
-  int rk, rv;
-  int body;
-  int flag;   // ROUTE: last routing page
-  int pad;
+  int n;       // rows / spans / body tokens in this page
+  int a;       // first row / first span ordinal / first body token
+  int rk, rv;  // expanded span: ranks
+  int flag;    // ROUTE: last routing page
+  int off_a;   // EXP: byte offset of the key part (header..Vt_K) or -1
+  int off_uk;  // EXP: byte offset of U_K rows [a, a+n)
+  int off_uv;  // EXP: byte offset of U_V rows [a, a+n)
+  int off_b;   // EXP: byte offset of the value part (sigma_V..Vt_V) or -1
+  int pad0, pad1;
 };
 
 struct DecodeParams {

@@ -5,52 +5,63 @@
 
 namespace sekv {
 
-// Issue the pages of one expanded span: the key part (header, sigma_K, g_K,
-// Vt_K), the U rows in tiles, the value part (sigma_V, g_V, Vt_V).
+// Issue the pages of one expanded span.  A record that fits a page goes in
+// one copy; a larger one as its key part, its U rows in tiles, its value part.
 __device__ __forceinline__ bool issue_expanded(uint8_t* smem, SmemMisc* ms, Ring& r,
                                                const DecodeParams& P, const ExpEntry& e,
                                                uint32_t* last_par, bool* filled) {
   bool ok = true;
   const int b = e.body, rK = e.rank & 0xFFFF, rV = (e.rank >> 16) & 0xFFFF;
   const uint8_t* rec = P.store + e.off;
+  const RecordLayout L = record_layout(b, rK, rV);
   PageDesc d{};
-  // key part
-  {
-    const uint32_t bytes = 16 + 8 * r4(rK) + 256 * rK;
-    d.type = PG_EXPA; d.n = 0; d.a = e.k; d.rk = rK; d.rv = rV; d.body = b;
-    uint8_t* pg = push_page(smem, ms, r, d, bytes, P.status, ok);
+  d.type = PG_EXP;
+  d.rk = rK;
+  d.rv = rV;
+  if (L.total <= kPageData) {
+    d.n = b; d.a = 0;
+    d.off_a = 0; d.off_uk = int(L.uk); d.off_uv = int(L.uv); d.off_b = int(L.vpart);
+    uint8_t* pg = push_page(smem, ms, r, d, uint32_t(L.total), P.status, ok);
     if (!ok) return false;
-    bulk_g2s(pg, rec, bytes, &ms->full[r.slot]);
+    bulk_g2s(pg, rec, uint32_t(L.total), &ms->full[r.slot]);
+    filled[r.slot] = true;
+    last_par[r.slot] = r.phase;
+    advance(r);
+    return true;
+  }
+  // key part
+  d.n = 0; d.a = 0; d.off_a = 0; d.off_uk = 0; d.off_uv = 0; d.off_b = -1;
+  {
+    uint8_t* pg = push_page(smem, ms, r, d, uint32_t(L.uk), P.status, ok);
+    if (!ok) return false;
+    bulk_g2s(pg, rec, uint32_t(L.uk), &ms->full[r.slot]);
     filled[r.slot] = true;
     last_par[r.slot] = r.phase;
     advance(r);
   }
-  // U tiles: rows [i0, i0 + n), n * r * 2 bytes of U_K at +0, of U_V at +16384
-  const int rmax = rK > rV ? rK : rV;
-  int rows = rmax > 0 ? (16384 / (2 * rmax)) & ~7 : 512;
+  // U rows: [i0, i0 + n) of U_K at +0 and of U_V at +16384
+  const int rmax = r8(rK) > r8(rV) ? r8(rK) : r8(rV);
+  int rows = rmax > 0 ? (16384 / (2 * rmax)) & ~15 : 512;
   if (rows > 512) rows = 512;
-  const uint8_t* uk = rec + 16 + 8 * r4(rK) + 256 * rK;
-  const uint8_t* uv = uk + pad16(2 * int64_t(b) * rK);
   for (int i0 = 0; i0 < b; i0 += rows) {
     const int n = (b - i0) < rows ? (b - i0) : rows;
-    const uint32_t bk = uint32_t(pad16(2 * int64_t(n) * rK));
-    const uint32_t bv = uint32_t(pad16(2 * int64_t(n) * rV));
-    d.type = PG_EXPU; d.n = n; d.a = i0;
+    const uint32_t bk = uint32_t(2 * n * r8(rK)), bv = uint32_t(2 * n * r8(rV));
+    d.n = n; d.a = i0; d.off_a = -1; d.off_uk = 0; d.off_uv = 16384; d.off_b = -1;
     uint8_t* pg = push_page(smem, ms, r, d, bk + bv, P.status, ok);
     if (!ok) return false;
-    if (bk) bulk_g2s(pg, uk + 2 * int64_t(i0) * rK, bk, &ms->full[r.slot]);
-    if (bv) bulk_g2s(pg + 16384, uv + 2 * int64_t(i0) * rV, bv, &ms->full[r.slot]);
+    if (bk) bulk_g2s(pg, rec + L.uk + 2 * int64_t(i0) * r8(rK), bk, &ms->full[r.slot]);
+    if (bv) bulk_g2s(pg + 16384, rec + L.uv + 2 * int64_t(i0) * r8(rV), bv, &ms->full[r.slot]);
     filled[r.slot] = true;
     last_par[r.slot] = r.phase;
     advance(r);
   }
   // value part
   {
-    const uint32_t bytes = 8 * r4(rV) + 256 * rV;
-    d.type = PG_EXPB; d.n = 0; d.a = e.k;
+    const uint32_t bytes = uint32_t(L.total - L.vpart);
+    d.n = 0; d.a = 0; d.off_a = -1; d.off_b = 0;
     uint8_t* pg = push_page(smem, ms, r, d, bytes, P.status, ok);
     if (!ok) return false;
-    if (bytes) bulk_g2s(pg, uv + pad16(2 * int64_t(b) * rV), bytes, &ms->full[r.slot]);
+    if (bytes) bulk_g2s(pg, rec + L.vpart, bytes, &ms->full[r.slot]);
     filled[r.slot] = true;
     last_par[r.slot] = r.phase;
     advance(r);

@@ -188,12 +188,25 @@ __device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int chunk16) 
 }
 
 __host__ __device__ inline int r4(int r) { return (r + 3) & ~3; }
+__host__ __device__ inline int r8(int r) { return (r + 7) & ~7; }
 __host__ __device__ inline int64_t pad16(int64_t n) { return (n + 15) & ~int64_t(15); }
+
+// Basis record layout (see sekv.h): byte offsets of its parts.
+struct RecordLayout {
+  int64_t uk, uv, vpart, total;
+};
+__host__ __device__ inline RecordLayout record_layout(int b, int rK, int rV) {
+  RecordLayout L;
+  L.uk = 16 + 8 * r4(rK) + 256 * int64_t(rK);
+  L.uv = L.uk + 2 * int64_t(b) * r8(rK);
+  L.vpart = L.uv + 2 * int64_t(b) * r8(rV);
+  L.total = L.vpart + 8 * r4(rV) + 256 * int64_t(rV);
+  return L;
+}
 
 __host__ __device__ inline int64_t record_bytes(int b, int rK, int rV) {
   if (b <= 0) return 0;
-  return 16 + 8 * r4(rK) + 256 * int64_t(rK) + pad16(2 * int64_t(b) * rK) +
-         pad16(2 * int64_t(b) * rV) + 8 * r4(rV) + 256 * int64_t(rV);
+  return record_layout(b, rK, rV).total;
 }
 
 }  // namespace sekv

@@ -109,13 +109,14 @@ typedef struct sekv_config {
  * Basis record of a span with body b >= 1 and ranks rK, rV ([DE]/[ZH]
  * Methodik 2: truncated SVD K_S ~ U_K diag(sigma_K g_K) Vt_K with soft gates
  * g; likewise V).  All offsets relative to the record start, every field
- * 16-byte aligned, r4(r) = r rounded up to a multiple of 4, pad16 = rounded
- * up to 16 bytes; padding bytes are unspecified (writers zero them):
+ * 16-byte aligned, r4(r) / r8(r) = r rounded up to a multiple of 4 / 8.
+ * Padding entries must be zero (the GPU reads them):
  *   int32 b, rK, rV, 0                          16 bytes
  *   f32  sigma_K[r4(rK)], f32 g_K[r4(rK)]       8*r4(rK)
  *   bf16 Vt_K[rK][128]                          256*rK
- *   bf16 U_K[b][rK]   (row-major)               pad16(2*b*rK)
- *   bf16 U_V[b][rV]   (row-major)               pad16(2*b*rV)
+ *   bf16 U_K[b][r8(rK)]  (row-major, columns    2*b*r8(rK)
+ *                         rK.. zero)
+ *   bf16 U_V[b][r8(rV)]                         2*b*r8(rV)
  *   f32  sigma_V[r4(rV)], f32 g_V[r4(rV)]       8*r4(rV)
  *   bf16 Vt_V[rV][128]                          256*rV
  * Record size = the sum of the right-hand column (sekv_record_size).

@@ -22,15 +22,15 @@ def _r4(r: int) -> int:
     return (r + 3) // 4 * 4
 
 
-def _pad16(nbytes: int) -> int:
-    return (nbytes + 15) // 16 * 16
+def _r8(r: int) -> int:
+    return (r + 7) // 8 * 8
 
 
 def record_size(b: int, rK: int, rV: int) -> int:
     """Bytes of one basis record (header, key part, U blocks, value part)."""
     if b <= 0:
         return 0
-    return (16 + 8 * _r4(rK) + 256 * rK + _pad16(2 * b * rK) + _pad16(2 * b * rV)
+    return (16 + 8 * _r4(rK) + 256 * rK + 2 * b * _r8(rK) + 2 * b * _r8(rV)
             + 8 * _r4(rV) + 256 * rV)
 
 
@@ -69,8 +69,10 @@ def pack_record(F: SpanFactors) -> bytes:
     gk = np.zeros(_r4(rK), np.float32); gk[:rK] = F.gK
     put(sk, 4 * _r4(rK)); put(gk, 4 * _r4(rK))
     put(bf16_bits(F.VtK).reshape(-1), 256 * rK)
-    put(bf16_bits(F.UK).reshape(-1), _pad16(2 * b * rK))
-    put(bf16_bits(F.UV).reshape(-1), _pad16(2 * b * rV))
+    uk = np.zeros((b, _r8(rK)), np.uint16); uk[:, :rK] = bf16_bits(F.UK)
+    uv = np.zeros((b, _r8(rV)), np.uint16); uv[:, :rV] = bf16_bits(F.UV)
+    put(uk.reshape(-1), 2 * b * _r8(rK))
+    put(uv.reshape(-1), 2 * b * _r8(rV))
     sv = np.zeros(_r4(rV), np.float32); sv[:rV] = F.sV
     gv = np.zeros(_r4(rV), np.float32); gv[:rV] = F.gV
     put(sv, 4 * _r4(rV)); put(gv, 4 * _r4(rV))
@@ -96,8 +98,8 @@ def unpack_record(buf: np.ndarray, off: int, b_expected: Optional[int] = None) -
     sK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
     gK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
     VtK = bits_bf16(take(256 * rK, 256 * rK, np.uint16)).reshape(rK, HEAD_DIM)
-    UK = bits_bf16(take(2 * b * rK, _pad16(2 * b * rK), np.uint16)).reshape(b, rK)
-    UV = bits_bf16(take(2 * b * rV, _pad16(2 * b * rV), np.uint16)).reshape(b, rV)
+    UK = bits_bf16(take(2 * b * _r8(rK), 2 * b * _r8(rK), np.uint16)).reshape(b, _r8(rK))[:, :rK]
+    UV = bits_bf16(take(2 * b * _r8(rV), 2 * b * _r8(rV), np.uint16)).reshape(b, _r8(rV))[:, :rV]
     sV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
     gV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
     VtV = bits_bf16(take(256 * rV, 256 * rV, np.uint16)).reshape(rV, HEAD_DIM)

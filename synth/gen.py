@@ -286,9 +286,9 @@ def record_size(b, rK, rV):
     def r4(r):
         return (r + 3) // 4 * 4
 
-    def p16(n):
-        return (n + 15) // 16 * 16
-    size = (16 + 8 * r4(rK) + 256 * rK + p16(2 * b * rK) + p16(2 * b * rV)
+    def r8(r):
+        return (r + 7) // 8 * 8
+    size = (16 + 8 * r4(rK) + 256 * rK + 2 * b * r8(rK) + 2 * b * r8(rV)
             + 8 * r4(rV) + 256 * rV)
     if isinstance(b, (int, np.integer)):
         return int(size) if b > 0 else 0
@@ -363,8 +363,8 @@ def decode_cache(cfg: WorkloadConfig, layer: int, device="cpu",
     def r4(r):
         return (r + 3) // 4 * 4
 
-    def p16(n):
-        return (n + 15) // 16 * 16
+    def r8(r):
+        return (r + 7) // 8 * 8
 
     def put_sigma_gate(base_bytes, r, rho_, scale_row):
         # sigma_j = c * exp(-j / (2 r)), g_j = sigmoid(2 (rho - j - 0.5)); zero pad to r4
@@ -389,8 +389,29 @@ def decode_cache(cfg: WorkloadConfig, layer: int, device="cpu",
         return 1.0 / torch.sqrt(prof.clamp(min=1e-30))
 
     put_sigma_gate(o + 16, rK_r, rhoK, scale_for(rK_r, b_r))
-    vpart = o + 16 + 8 * r4(rK_r) + 256 * rK_r + p16(2 * b_r * rK_r) + p16(2 * b_r * rV_r)
+    uk_off = o + 16 + 8 * r4(rK_r) + 256 * rK_r
+    uv_off = uk_off + 2 * b_r * r8(rK_r)
+    vpart = uv_off + 2 * b_r * r8(rV_r)
     put_sigma_gate(vpart, rV_r, rhoV, scale_for(rV_r, b_r))
+    bf = store.view(torch.bfloat16)
+
+    def zero_u_padding(base_bytes, b_, r_):
+        # U rows hold r8(r) columns; columns r.. must be zero
+        pad = r8(r_) - r_
+        sel = (pad > 0) & (b_ > 0)
+        base_bytes, b_, r_, pad = base_bytes[sel], b_[sel], r_[sel], pad[sel]
+        n_el = b_ * pad
+        if n_el.numel() == 0 or int(n_el.sum().item()) == 0:
+            return
+        rec_i = torch.repeat_interleave(torch.arange(len(n_el), device=device), n_el)
+        start = torch.cumsum(n_el, 0) - n_el
+        e = torch.arange(int(n_el.sum().item()), device=device) - start[rec_i]
+        row, colp = e // pad[rec_i], e % pad[rec_i]
+        idx = base_bytes[rec_i] // 2 + row * r8(r_)[rec_i] + r_[rec_i] + colp
+        bf[idx] = 0
+
+    zero_u_padding(uk_off, b_r, rK_r)
+    zero_u_padding(uv_off, b_r, rV_r)
     rec_off = off.reshape(B, Hkv, max_spans).contiguous()
     rec_rank = (rK | (rV << 16)).int().contiguous()
     return dict(n_spans=n_spans.to(device), body_len=body.int().to(device).contiguous(),
