@@ -7,10 +7,11 @@
 #include "decode_attn.cuh"
 #include "host_common.h"
 #include "route_fetch.cuh"
+#include "decode_host.h"
 
 using namespace sekv;
 
-namespace {
+namespace sekv {
 
 thread_local int32_t g_launches = 0;
 
@@ -32,7 +33,7 @@ bool config_ok(const sekv_config* cfg, sekv_status* why) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-}  // namespace
+}  // namespace sekv
 
 namespace sekv {
 
@@ -183,7 +184,7 @@ sekv_status sekv_workspace_status(void* workspace, cudaStream_t stream, int32_t*
 // ----------------------------------------------------------------------------
 // decode launches
 // ----------------------------------------------------------------------------
-namespace {
+namespace sekv {
 
 sekv_status check_cache(const sekv_config* cfg, const sekv_layer_cache* c, bool need_store) {
   if (!c || !c->n_spans || !c->body_len || !c->k_full || !c->v_full || !c->k_sum || !c->v_sum ||
@@ -291,7 +292,7 @@ sekv_status launch_prep(const sekv_config* cfg, const sekv_layer_cache* cache,
   return SEKV_OK;
 }
 
-}  // namespace
+}  // namespace sekv
 
 extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
                                         const void* q, const float* W_r, const float* theta,

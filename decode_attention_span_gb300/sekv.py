@@ -29,8 +29,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 # every symbol include/sekv.h declares
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
-           "sekv_decode_step", "sekv_build_spans", "sekv_status_string",
-           "sekv_last_launch_count")
+           "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_build_spans",
+           "sekv_status_string", "sekv_last_launch_count")
 
 
 class SekvError(RuntimeError):
@@ -98,6 +98,10 @@ def lib() -> ctypes.CDLL:
         L.sekv_decode_step.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_sz, _c_vp]
+        L.sekv_decode_step_noalloc.restype = _c_i32
+        L.sekv_decode_step_noalloc.argtypes = [ctypes.POINTER(SekvConfig),
+                                               ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp,
+                                               _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]
         L.sekv_build_spans.restype = _c_i32
         L.sekv_build_spans.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_sz,
@@ -285,6 +289,37 @@ def decode_step(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float, ws:
                                   _ptr(theta), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(expanded), _ptr(n_expanded), ws.ptr(), ws.nbytes,
                                   _stream(stream)))
+    return out, lse, expanded, n_expanded
+
+
+def decode_step_noalloc(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float, out=None,
+                        lse=None, want_list: bool = False, stream=None):
+    """sekv_decode_step_noalloc: the decode step with no workspace argument.
+
+    For callers that cannot allocate device memory: the library's fixed 8 MiB
+    device scratch array stands in for the workspace (shapes needing more
+    raise SekvError with SEKV_ERR_CAPACITY).  Calls share that array, so they
+    must not overlap on the GPU.  The outputs here are allocated by torch only
+    when the caller passes none.
+    """
+    _need(q, "q", torch.bfloat16); _need(W_r, "W_r", torch.float32)
+    _need(theta, "theta", torch.float32)
+    dev = q.device
+    if out is None:
+        out = torch.empty(cfg.batch, cfg.n_q_heads, 128, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(cfg.batch, cfg.n_q_heads, dtype=torch.float32, device=dev)
+    NG = cfg.batch * cfg.n_kv_heads
+    expanded = n_expanded = None
+    if want_list:
+        expanded = torch.zeros(NG * cfg.max_spans, dtype=torch.int32, device=dev)
+        n_expanded = torch.zeros(NG, dtype=torch.int32, device=dev)
+    c = cfg.c()
+    _check("sekv_decode_step_noalloc",
+           lib().sekv_decode_step_noalloc(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q),
+                                          _ptr(W_r), _ptr(theta), float(scale), _ptr(out),
+                                          _ptr(lse), _ptr(expanded), _ptr(n_expanded),
+                                          _stream(stream)))
     return out, lse, expanded, n_expanded
 
 

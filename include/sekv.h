@@ -240,6 +240,39 @@ sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cac
                              int32_t* n_expanded, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
 
+/*
+ * sekv_decode_step_noalloc -- sekv_decode_step without a caller workspace.
+ * The SeKV pages have no counterpart for this call; it exists for callers
+ * that cannot allocate device memory and have no spare buffer to lend: for
+ * example a plugin inside a serving engine that has already handed every byte
+ * of the GPU to its own memory pool, or a decode loop that must not call
+ * cudaMalloc (which can synchronise the whole device) between tokens.
+ * Instead of a workspace the call uses one scratch array of
+ * SEKV_NOALLOC_SCRATCH_BYTES (8 MiB) that the library keeps in device memory
+ * on every GPU that loads it, for the life of the process; nothing is
+ * allocated or freed, by the library or anything it calls.
+ *   - Limit: the configuration must need at most SEKV_NOALLOC_SCRATCH_BYTES of
+ *     scratch, i.e. sekv_workspace_size(cfg, SEKV_CALL_DECODE, 0) <= 8 MiB
+ *     (e.g. batch 1 x 8 KV heads x 4 160 spans needs about 2 MiB); larger
+ *     shapes return SEKV_ERR_CAPACITY before anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents; every call clears the counters it needs.  Calls that
+ *     overlap on the GPU (other streams, other threads) race on it and give
+ *     wrong results: serialise them.
+ *   - Errors the GPU detects are not reported by this call (the status word
+ *     lives in the shared array); diagnose with sekv_decode_step.
+ * Arguments, layouts and results are those of sekv_decode_step; flags in
+ * cfg are ignored (no overlap with the preceding kernel).
+ */
+#define SEKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+sekv_status sekv_decode_step_noalloc(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                     const void* q, const float* W_r, const float* theta,
+                                     float scale, float* out, float* lse, int32_t* expanded,
+                                     int32_t* n_expanded, cudaStream_t stream);
+
 /* Outputs of sekv_build_spans: one layer of the cache (layouts as in
  * sekv_layer_cache; every array with its full capacity) plus the device
  * basis store and its capacity in bytes. */
