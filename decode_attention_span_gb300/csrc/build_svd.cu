@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t) {
         const int d = tid + t * NT;
         if (d < kHeadDim) {
-          Vt[j * kHeadDim + d] = __float2bfloat16_rn(sgn * v[t]);
+          // rows are stored with their 16-byte chunks swizzled by (row & 7)
+          Vt[j * kHeadDim + ((((d >> 3) ^ (j & 7)) << 3) | (d & 7))] = __float2bfloat16_rn(sgn * v[t]);
           if (LARGE) Vs[j * kHeadDim + d] = sgn * v[t];
         }
       }

@@ -11,7 +11,7 @@ namespace sekv {
 // entry array together with their record size prefix.
 __device__ __forceinline__ void consume_route(const uint8_t* page, const PageDesc& d, int k0,
                                               const DecodeParams& P, SmemMisc* ms,
-                                              uint16_t* infoc, const float* ys, size_t gs) {
+                                              float* infoc, const float* ys, size_t gs) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int kk = 32 * w + lane;
   const bool valid = kk < d.n;
@@ -34,8 +34,10 @@ __device__ __forceinline__ void consume_route(const uint8_t* page, const PageDes
                                                         (((dc & 7) ^ (row & 7)) << 4));
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const float4 y = y4[h * 16 + dc];
-        z[h] = fmaf(s.x, y.x, fmaf(s.y, y.y, fmaf(s.z, y.z, fmaf(s.w, y.w, z[h]))));
+        if (h < P.G) {
+          const float4 y = y4[h * 16 + dc];
+          z[h] = fmaf(s.x, y.x, fmaf(s.y, y.y, fmaf(s.z, y.z, fmaf(s.w, y.w, z[h]))));
+        }
       }
     }
   }
@@ -44,7 +46,7 @@ __device__ __forceinline__ void consume_route(const uint8_t* page, const PageDes
   for (int h = 0; h < 8; ++h)
     if (h < P.G) hit |= z[h] > ms->theta[h];
   const bool ex = valid && body > 0 && hit;
-  if (valid) infoc[d.a - k0 + kk] = uint16_t((body & 0x7fff) | (ex ? 0x8000 : 0));
+  if (valid) infoc[d.a - k0 + kk] = (body > 0 && !ex) ? log2f(float(body)) : kNegInf;
   long long size = ex ? record_bytes(body, rank & 0xffff, (rank >> 16) & 0xffff) : 0;
   // inclusive warp scan of sizes
   long long incl = size;
@@ -92,7 +94,7 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   int f0, f1, k0, k1;
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
   const size_t gs = size_t(g) * P.max_spans;
-  uint16_t* infoc = reinterpret_cast<uint16_t*>(smem + kOffInfo);
+  float* infoc = reinterpret_cast<float*>(smem + kOffInfo);  // summary bias per span
   float* qs = reinterpret_cast<float*>(smem + kOffScratch);         // prologue only
   float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages only
 
@@ -120,16 +122,22 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       qs[i] = (i / kHeadDim) < G ? __bfloat162float(qg[i]) : 0.f;
     if (tid < 8) ms->theta[tid] = tid < G ? P.theta[c * G + tid] : 0.f;
     named_bar(1, kConsumers);
-    // y_h = W_r[c] q_h, one routing coordinate per thread and two heads per pass
+    // y_h = W_r[c] q_h from the staged rows (padded stride: conflict-free
+    // 16-byte loads), one routing coordinate per thread, heads hh, hh+2, ...
+    if (!mbar_wait(&ms->wr_bar, 0, kWaitLimit) && tid == 0)
+      set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
     const int jr = tid & 63, hh = tid >> 6;
-    const float4* wrow = reinterpret_cast<const float4*>(P.W_r + (size_t(c) * kRouteDim + jr) * kHeadDim);
+    const float4* wrow = reinterpret_cast<const float4*>(smem + kOffWr + jr * kWrStride);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int d4 = 0; d4 < 32; ++d4) {
-      const float4 wv = __ldg(wrow + d4);
+      const float4 wv = wrow[d4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 qv = reinterpret_cast<const float4*>(qs + (hh + 2 * i) * kHeadDim)[d4];
-        acc[i] = fmaf(wv.x, qv.x, fmaf(wv.y, qv.y, fmaf(wv.z, qv.z, fmaf(wv.w, qv.w, acc[i]))));
+        if (hh + 2 * i < G) {
+          const float4 qv = reinterpret_cast<const float4*>(qs + (hh + 2 * i) * kHeadDim)[d4];
+          acc[i] = fmaf(wv.x, qv.x, fmaf(wv.y, qv.y, fmaf(wv.z, qv.z, fmaf(wv.w, qv.w, acc[i]))));
+        }
       }
     }
     named_bar(1, kConsumers);  // qs is dead; ys may overwrite nothing it needs
@@ -164,7 +172,10 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
         break;
       case PG_INFO: {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(page);
-        for (int i = tid; i < d.n; i += kConsumers) infoc[i] = src[i];
+        for (int i = tid; i < d.n; i += kConsumers) {
+          const int inf = src[i], body = inf & 0x7fff;
+          infoc[i] = (body > 0 && !(inf & 0x8000)) ? log2f(float(body)) : kNegInf;
+        }
         named_bar(1, kConsumers);
         break;
       }
@@ -174,10 +185,22 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       case PG_SUM:
         consume_kv_tile(A, pu, pu + 16384, d.n, infoc + (d.a - k0), P.scale_log2);
         break;
-      case PG_EXP:
+      case PG_EXP:  // one large record, split over pages; all warps share its tokens
         if (d.off_a >= 0) exp_key(A, X, page + d.off_a, d.rk, P.scale_log2);
-        if (d.n > 0) exp_tokens(A, X, page + d.off_uk, page + d.off_uv, d.n, d.rk, d.rv);
+        if (d.n > 0)
+          exp_tokens(A, X, page + d.off_uk, page + d.off_uv, d.n, d.rk, d.rv, 16 * w,
+                     16 * kConsumerWarps);
         if (d.off_b >= 0) exp_value(A, X, page + d.off_b, d.rv);
+        break;
+      case PG_EXPM:  // several small records: warp w takes records w, w+4, ...
+        for (int i = w; i < d.n; i += kConsumerWarps) {
+          const RecInfo ri = ms->rec[slot][i];
+          const uint8_t* part = page + ri.off;
+          const RecordLayout RL = record_layout(ri.b, ri.rk, ri.rv);
+          exp_key(A, X, part, ri.rk, P.scale_log2);
+          exp_tokens(A, X, part + RL.uk, part + RL.uv, ri.b, ri.rk, ri.rv, 0, 16);
+          exp_value(A, X, part + RL.vpart, ri.rv);
+        }
         break;
       default:
         break;
@@ -271,8 +294,17 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   }
   named_bar(1, kConsumers);
   for (int h = 0; h < G; ++h) {
-    float O = 0.f;
-    for (int jj = 0; jj < cg; ++jj) O = fmaf(__ldcg(&parts[jj].o[h][tid]), sm_s[jj * 8 + h], O);
+    float Oa[4] = {0.f, 0.f, 0.f, 0.f};
+    int jj = 0;
+    for (; jj + 4 <= cg; jj += 4) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(&parts[jj + u].o[h][tid]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Oa[u] = fmaf(v[u], sm_s[(jj + u) * 8 + h], Oa[u]);
+    }
+    for (; jj < cg; ++jj) Oa[0] = fmaf(__ldcg(&parts[jj].o[h][tid]), sm_s[jj * 8 + h], Oa[0]);
+    const float O = (Oa[0] + Oa[1]) + (Oa[2] + Oa[3]);
     const float L = sm_ML[8 + h];
     const size_t row = size_t(b) * P.Hq + size_t(c) * G + h;
     P.out[row * kHeadDim + tid] = L > 0.f ? O / L : 0.f;
@@ -321,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms->full[s], 1);
       mbar_init(&ms->empty[s], kConsumerWarps);
     }
+    mbar_init(&ms->wr_bar, 1);
     ms->n_local = 0;
     ms->bytes_local = 0;
     ms->is_last = 0;

@@ -42,14 +42,26 @@ constexpr int kRouteSpans = 128;     // spans per routing page
 constexpr int kTileRows = 64;        // rows per full/summary page
 constexpr int kMaxCgSmem = 256;      // CTAs per KV head the producer can index
 
+constexpr int kMaxRecPerPage = 8;   // small basis records packed into one page
+constexpr int kWrStride = 528;      // W_r rows in shared memory (512 B + 16 B pad)
+
 constexpr int kOffScratch = kPages * kPageStride;
 constexpr int kOffInfo = kOffScratch + kConsumerWarps * kScratchPerWarp;
-constexpr int kOffMisc = kOffInfo + kInfoCap * 2;
-constexpr int kMiscBytes = 4096;
+constexpr int kOffWr = kOffInfo + kInfoCap * 4;   // info cache: one float per span
+constexpr int kOffMisc = kOffWr + kRouteDim * kWrStride;
+constexpr int kMiscBytes = 4608;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
-enum PageType : int { PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4, PG_EXP = 5, PG_END = 6 };
+enum PageType : int {
+  PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4, PG_EXP = 5, PG_END = 6, PG_EXPM = 7
+};
+
+// One basis record inside a PG_EXPM page (several small records per page).
+struct RecInfo {
+  int off;  // byte offset in the page
+  int b, rk, rv;
+};
 
 struct PageDesc {
   int type;
@@ -138,8 +150,10 @@ __host__ __device__ inline void fixed_range(int j, int cg, int n_full, int n_sp,
 
 struct SmemMisc {
   PageDesc desc[kPages];
+  RecInfo rec[kPages][kMaxRecPerPage];
   uint64_t full[kPages];
   uint64_t empty[kPages];
+  uint64_t wr_bar;   // W_r rows staged in shared memory (fused mode)
   int n_local;
   int wcnt[kConsumerWarps];
   int is_last;
@@ -168,16 +182,20 @@ __device__ __forceinline__ uint8_t* page_ptr(uint8_t* smem, int slot) {
   return smem + slot * kPageStride;
 }
 
-// Wait for a free slot, publish the descriptor, arm the full barrier.
+// Wait for a free slot, publish the descriptor (and the record table of a
+// multi-record page) and only then arm the full barrier, so that the
+// consumers' acquire on the barrier covers both.
 __device__ __forceinline__ uint8_t* push_page(uint8_t* smem, SmemMisc* ms, Ring& r,
                                               const PageDesc& d, uint32_t bytes,
-                                              int32_t* status, bool& ok) {
+                                              int32_t* status, bool& ok,
+                                              const RecInfo* tab = nullptr, int ntab = 0) {
   if (!mbar_wait(&ms->empty[r.slot], r.phase ^ 1u, kWaitLimit)) {
     set_device_error(status, DEV_WAIT_TIMEOUT, 1);
     ok = false;
     return nullptr;
   }
   ms->desc[r.slot] = d;
+  for (int i = 0; i < ntab; ++i) ms->rec[r.slot][i] = tab[i];
   mbar_arrive_expect_tx(&ms->full[r.slot], bytes);
   return page_ptr(smem, r.slot);
 }

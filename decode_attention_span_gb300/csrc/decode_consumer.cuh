@@ -43,14 +43,15 @@ __device__ __forceinline__ void softmax_rescale(float m_old, float m_new, float&
 
 // One 64-row page of keys (full rows or summaries): warp w takes rows
 // 16w..16w+15.  kb: shared address of the key boxes (dims 0-63 at +0, 64-127
-// at +8192), vb likewise for values.  info: span info of the page's first
-// row for summary pages (nullptr for full rows).
+// at +8192), vb likewise for values.  bias: for summary pages, the logit bias
+// of the page's first span onward (log2|S|, or -inf for a span that does not
+// enter as a summary); nullptr for full rows.
 __device__ __forceinline__ void consume_kv_tile(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
-                                                const uint16_t* info, float scale_log2) {
+                                                const float* bias_row, float scale_log2) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int rbase = 16 * w;
   if (rbase >= n) return;
-  float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, s2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t box = kb + (i >> 1) * 8192;
@@ -60,8 +61,13 @@ __device__ __forceinline__ void consume_kv_tile(WarpAcc& A, uint32_t kb, uint32_
       ldsm_x4(swz128(box, rbase + 8 * nt + (lane & 7), (i & 1) * 4 + (lane >> 3)), b0, b1, b2,
               b3);
       mma_bf16_rows8(s[nt][0], s[nt][1], A.qa[2 * i][0], A.qa[2 * i][1], b0, b1);
-      mma_bf16_rows8(s[nt][0], s[nt][1], A.qa[2 * i + 1][0], A.qa[2 * i + 1][1], b2, b3);
+      mma_bf16_rows8(s2[nt][0], s2[nt][1], A.qa[2 * i + 1][0], A.qa[2 * i + 1][1], b2, b3);
     }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    s[nt][0] += s2[nt][0];
+    s[nt][1] += s2[nt][1];
   }
   float x[2][2];
   float mx = kNegInf;
@@ -72,11 +78,9 @@ __device__ __forceinline__ void consume_kv_tile(WarpAcc& A, uint32_t kb, uint32_
       const int key = rbase + 8 * nt + 2 * (lane & 3) + e;
       bool valid = key < n;
       float bias = 0.f;
-      if (info != nullptr && valid) {
-        const int inf = info[key];
-        const int body = inf & 0x7fff;
-        valid = body > 0 && !(inf & 0x8000);
-        bias = valid ? log2f(float(body)) : 0.f;
+      if (bias_row != nullptr && valid) {
+        bias = bias_row[key];
+        valid = bias != kNegInf;
       }
       x[nt][e] = valid ? fmaf(s[nt][e], scale_log2, bias) : kNegInf;
       mx = fmaxf(mx, x[nt][e]);
@@ -143,23 +147,29 @@ __device__ __forceinline__ void exp_key(WarpAcc& A, ExpAcc& X, const uint8_t* pa
   const float* sig = reinterpret_cast<const float*>(part + 16);
   const float* gat = sig + r4(rK);
   const uint32_t vt = smem_u32(part + 16 + 8 * r4(rK));
-  float cv[8][2];
+  // eight independent accumulation chains (one per 8 ranks), k-steps outside
+  float cv[8][2], cw[8][2];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) cv[nt][0] = cv[nt][1] = cw[nt][0] = cw[nt][1] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      if (8 * nt < rK) {
+        uint32_t b0, b1, b2, b3;
+        const int row = 8 * nt + (lane & 7), chunk = 4 * i + (lane >> 3);
+        ldsm_x4(vt + row * 256 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_rows8(cv[nt][0], cv[nt][1], A.qa[2 * i][0], A.qa[2 * i][1], b0, b1);
+        mma_bf16_rows8(cw[nt][0], cw[nt][1], A.qa[2 * i + 1][0], A.qa[2 * i + 1][1], b2, b3);
+      }
+    }
+  }
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
-    cv[nt][0] = cv[nt][1] = 0.f;
-    if (8 * nt < rK) {
-      float c0 = 0.f, c1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(vt + (8 * nt + (lane & 7)) * 256 + (32 * i + 8 * (lane >> 3)) * 2, b0, b1, b2, b3);
-        mma_bf16_rows8(c0, c1, A.qa[2 * i][0], A.qa[2 * i][1], b0, b1);
-        mma_bf16_rows8(c0, c1, A.qa[2 * i + 1][0], A.qa[2 * i + 1][1], b2, b3);
-      }
-      const int j0 = 8 * nt + 2 * (lane & 3);
-      cv[nt][0] = j0 < rK ? c0 * sig[j0] * gat[j0] * scale_log2 : 0.f;
-      cv[nt][1] = j0 + 1 < rK ? c1 * sig[j0 + 1] * gat[j0 + 1] * scale_log2 : 0.f;
-    }
+    const int j0 = 8 * nt + 2 * (lane & 3);
+    cv[nt][0] = j0 < rK ? (cv[nt][0] + cw[nt][0]) * sig[j0] * gat[j0] * scale_log2 : 0.f;
+    cv[nt][1] = j0 + 1 < rK ? (cv[nt][1] + cw[nt][1]) * sig[j0 + 1] * gat[j0 + 1] * scale_log2
+                            : 0.f;
   }
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks) {
@@ -175,14 +185,15 @@ __device__ __forceinline__ void exp_key(WarpAcc& A, ExpAcc& X, const uint8_t* pa
 // strides r8(rK), r8(rV) bf16).  Rows or ranks past the valid ones read
 // neighbouring shared memory and are masked with selects, never multiplied.
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc& X, const uint8_t* uk,
-                                           const uint8_t* uv, int n, int rK, int rV) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+                                           const uint8_t* uv, int n, int rK, int rV, int start,
+                                           int step) {
+  const int lane = threadIdx.x & 31;
   const int sk = 2 * r8(rK), sv = 2 * r8(rV);  // row strides in bytes
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
   const int mi = lane >> 3;
-  for (int rbase = 16 * w; rbase < n; rbase += 16 * kConsumerWarps) {
+  for (int rbase = start; rbase < n; rbase += step) {
     X.had = true;
-    float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, sl[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       if (16 * ks < rK) {
@@ -196,10 +207,15 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc& X, const uint8_t*
           b0 &= m0; b2 &= m0; b1 &= m1; b3 &= m1;
         }
         mma_bf16_rows8(s[0][0], s[0][1], X.ch[ks][0], X.ch[ks][1], b0, b1);
-        mma_bf16_rows8(s[0][0], s[0][1], X.cl[ks][0], X.cl[ks][1], b0, b1);
+        mma_bf16_rows8(sl[0][0], sl[0][1], X.cl[ks][0], X.cl[ks][1], b0, b1);
         mma_bf16_rows8(s[1][0], s[1][1], X.ch[ks][0], X.ch[ks][1], b2, b3);
-        mma_bf16_rows8(s[1][0], s[1][1], X.cl[ks][0], X.cl[ks][1], b2, b3);
+        mma_bf16_rows8(sl[1][0], sl[1][1], X.cl[ks][0], X.cl[ks][1], b2, b3);
       }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] += sl[nt][0];
+      s[nt][1] += sl[nt][1];
     }
     float x[2][2], mx = kNegInf;
 #pragma unroll
@@ -280,7 +296,7 @@ __device__ __forceinline__ void exp_value(WarpAcc& A, ExpAcc& X, const uint8_t* 
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vt + j * 256 + (2 * dp + (mi >> 1)) * 16, b0, b1, b2, b3);
+        ldsm_x4_t(vt + j * 256 + (((2 * dp + (mi >> 1)) ^ (j & 7)) << 4), b0, b1, b2, b3);
         if (tail) { b0 &= m0; b2 &= m0; b1 &= m1; b3 &= m1; }
         mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], h0, h2, b0, b1);
         mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], l0, l2, b0, b1);

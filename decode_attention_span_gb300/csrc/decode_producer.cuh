@@ -69,6 +69,36 @@ __device__ __forceinline__ bool issue_expanded(uint8_t* smem, SmemMisc* ms, Ring
   return true;
 }
 
+// Small records waiting to be packed into one page (producer lane 0).
+struct Batch {
+  int n = 0;
+  int64_t bytes = 0;
+  int64_t src[kMaxRecPerPage];
+  RecInfo tab[kMaxRecPerPage];
+};
+
+__device__ __forceinline__ bool flush_batch(uint8_t* smem, SmemMisc* ms, Ring& r,
+                                            const DecodeParams& P, Batch& bat,
+                                            uint32_t* last_par, bool* filled) {
+  if (bat.n == 0) return true;
+  bool ok = true;
+  PageDesc d{};
+  d.type = PG_EXPM;
+  d.n = bat.n;
+  uint8_t* pg = push_page(smem, ms, r, d, uint32_t(bat.bytes), P.status, ok, bat.tab, bat.n);
+  if (!ok) return false;
+  for (int i = 0; i < bat.n; ++i) {
+    const int64_t sz = record_bytes(bat.tab[i].b, bat.tab[i].rk, bat.tab[i].rv);
+    bulk_g2s(pg + bat.tab[i].off, P.store + bat.src[i], uint32_t(sz), &ms->full[r.slot]);
+  }
+  filled[r.slot] = true;
+  last_par[r.slot] = r.phase;
+  advance(r);
+  bat.n = 0;
+  bat.bytes = 0;
+  return true;
+}
+
 __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P, int g, int j,
                               int b, int c) {
   const int lane = threadIdx.x & 31;
@@ -83,6 +113,7 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
   for (int s = 0; s < kPages; ++s) { filled[s] = false; last_par[s] = 0; }
   bool ok = true;
   const size_t gs = size_t(g) * P.max_spans;
+  Batch bat;
 
   // list mode reads what the preparation kernel wrote: wait for it first
   if (!P.fused) pdl_wait();
@@ -91,7 +122,14 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
     prefetch_tmap(&P.tm_vfull);
     prefetch_tmap(&P.tm_ksum);
     prefetch_tmap(&P.tm_vsum);
-    if (P.fused) prefetch_tmap(&P.tm_sroute);
+    if (P.fused) {
+      prefetch_tmap(&P.tm_sroute);
+      // routing weights of this KV head, rows padded to kWrStride bytes
+      mbar_arrive_expect_tx(&ms->wr_bar, kRouteDim * kHeadDim * 4);
+      for (int row = 0; row < kRouteDim; ++row)
+        bulk_g2s(smem + kOffWr + row * kWrStride,
+                 P.W_r + (size_t(c) * kRouteDim + row) * kHeadDim, kHeadDim * 4, &ms->wr_bar);
+    }
     PageDesc d{};
     // 1. routing pages (fused) or the span-info page (list mode)
     if (P.fused) {
@@ -228,12 +266,27 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
           x.body = __shfl_sync(0xffffffffu, en.body, src_lane);
           x.rank = __shfl_sync(0xffffffffu, en.rank, src_lane);
           x.off = __shfl_sync(0xffffffffu, en.off, src_lane);
-          if (lane == 0) ok = issue_expanded(smem, ms, r, P, x, last_par, filled);
+          if (lane == 0) {
+            const int xr = x.rank & 0xFFFF, xv = (x.rank >> 16) & 0xFFFF;
+            const int64_t sz = record_bytes(x.body, xr, xv);
+            if (sz > kPageData) {  // too big for a page: split path
+              ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
+              if (ok) ok = issue_expanded(smem, ms, r, P, x, last_par, filled);
+            } else {
+              if (bat.n == kMaxRecPerPage || bat.bytes + sz > kPageData)
+                ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
+              bat.src[bat.n] = x.off;
+              bat.tab[bat.n] = RecInfo{int(bat.bytes), x.body, xr, xv};
+              bat.bytes += sz;
+              ++bat.n;
+            }
+          }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
       }
     }
   }
+  if (lane == 0 && ok) ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
   if (lane == 0) {
     PageDesc d{};
     d.type = PG_END;

@@ -74,10 +74,11 @@ typedef struct sekv_config {
   int32_t flags;       /* SEKV_FLAG_* bits, 0 for none */
 } sekv_config;
 
-/* sekv_decode_step may start streaming this layer's cache (never q, W_r or
- * theta) before the kernel that precedes it on the stream has finished
- * (programmatic dependent launch).  Set it only when no preceding kernel on
- * the stream writes this layer's cache; it hides launch gaps between layers. */
+/* sekv_decode_step may start streaming this layer's cache and its routing
+ * weights W_r (never q or theta) before the kernel that precedes it on the
+ * stream has finished (programmatic dependent launch).  Set it only when no
+ * preceding kernel on the stream writes this layer's cache or W_r; it hides
+ * launch gaps between layers. */
 #define SEKV_FLAG_OVERLAP_PREVIOUS 1
 
 /*
@@ -119,6 +120,10 @@ typedef struct sekv_config {
  *   bf16 U_V[b][r8(rV)]                         2*b*r8(rV)
  *   f32  sigma_V[r4(rV)], f32 g_V[r4(rV)]       8*r4(rV)
  *   bf16 Vt_V[rV][128]                          256*rV
+ * Vt rows are stored swizzled: row j's 128 values form sixteen 16-byte
+ * chunks (chunk c = columns 8c..8c+7), and chunk c is stored at chunk
+ * position c ^ (j & 7) of the row (so that eight consecutive rows read the
+ * same columns from eight different shared-memory banks).
  * Record size = the sum of the right-hand column (sekv_record_size).
  */
 typedef struct sekv_layer_cache {

@@ -34,6 +34,18 @@ def record_size(b: int, rK: int, rV: int) -> int:
             + 8 * _r4(rV) + 256 * rV)
 
 
+def swizzle_vt(vt: np.ndarray) -> np.ndarray:
+    """Chunk permutation of Vt rows (its own inverse): for row j, the 16-byte
+    chunk c (columns 8c..8c+7) goes to chunk position c ^ (j & 7)."""
+    r = vt.shape[0]
+    out = np.empty_like(vt)
+    for j in range(r):
+        for c in range(16):
+            p = c ^ (j & 7)
+            out[j, 8 * p:8 * p + 8] = vt[j, 8 * c:8 * c + 8]
+    return out
+
+
 def bf16_bits(x) -> np.ndarray:
     """uint16 patterns of values that are already bfloat16-representable."""
     x = np.asarray(x, np.float64)
@@ -68,7 +80,7 @@ def pack_record(F: SpanFactors) -> bytes:
     sk = np.zeros(_r4(rK), np.float32); sk[:rK] = F.sK
     gk = np.zeros(_r4(rK), np.float32); gk[:rK] = F.gK
     put(sk, 4 * _r4(rK)); put(gk, 4 * _r4(rK))
-    put(bf16_bits(F.VtK).reshape(-1), 256 * rK)
+    put(swizzle_vt(bf16_bits(F.VtK).reshape(rK, HEAD_DIM)).reshape(-1), 256 * rK)
     uk = np.zeros((b, _r8(rK)), np.uint16); uk[:, :rK] = bf16_bits(F.UK)
     uv = np.zeros((b, _r8(rV)), np.uint16); uv[:, :rV] = bf16_bits(F.UV)
     put(uk.reshape(-1), 2 * b * _r8(rK))
@@ -76,7 +88,7 @@ def pack_record(F: SpanFactors) -> bytes:
     sv = np.zeros(_r4(rV), np.float32); sv[:rV] = F.sV
     gv = np.zeros(_r4(rV), np.float32); gv[:rV] = F.gV
     put(sv, 4 * _r4(rV)); put(gv, 4 * _r4(rV))
-    put(bf16_bits(F.VtV).reshape(-1), 256 * rV)
+    put(swizzle_vt(bf16_bits(F.VtV).reshape(rV, HEAD_DIM)).reshape(-1), 256 * rV)
     assert pos == len(out)
     return bytes(out)
 
@@ -97,12 +109,12 @@ def unpack_record(buf: np.ndarray, off: int, b_expected: Optional[int] = None) -
 
     sK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
     gK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
-    VtK = bits_bf16(take(256 * rK, 256 * rK, np.uint16)).reshape(rK, HEAD_DIM)
+    VtK = swizzle_vt(bits_bf16(take(256 * rK, 256 * rK, np.uint16)).reshape(rK, HEAD_DIM))
     UK = bits_bf16(take(2 * b * _r8(rK), 2 * b * _r8(rK), np.uint16)).reshape(b, _r8(rK))[:, :rK]
     UV = bits_bf16(take(2 * b * _r8(rV), 2 * b * _r8(rV), np.uint16)).reshape(b, _r8(rV))[:, :rV]
     sV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
     gV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
-    VtV = bits_bf16(take(256 * rV, 256 * rV, np.uint16)).reshape(rV, HEAD_DIM)
+    VtV = swizzle_vt(bits_bf16(take(256 * rV, 256 * rV, np.uint16)).reshape(rV, HEAD_DIM))
     return SpanFactors(UK=UK, sK=sK, gK=gK, VtK=VtK, UV=UV, sV=sV, gV=gV, VtV=VtV)
 
 

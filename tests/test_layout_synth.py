@@ -30,7 +30,8 @@ def test_record_bytes_by_hand():
     want += struct.pack("<4f", 1.5, 0.5, 0, 0)                  # sigma_V
     want += struct.pack("<4f", 1.0, 0.625, 0, 0)                # g_V
     want += bf(0.0) + bf(1.0) + bf(0.0) * 126                   # Vt_V row 0
-    want += bf(0.0) * 2 + bf(-0.25) + bf(0.0) * 125             # Vt_V row 1
+    # Vt_V row 1: chunk 0 (columns 0..7) is stored at chunk position 0 ^ 1 = 1
+    want += bf(0.0) * 10 + bf(-0.25) + bf(0.0) * 117            # Vt_V row 1
     got = layout.pack_record(F)
     assert got == want
     assert len(want) == layout.record_size(1, 1, 2) == gen.record_size(1, 1, 2)
