@@ -5,84 +5,93 @@
 
 namespace sekv {
 
-// Routing page: lane = span.  z_h = y_h . s_S (fp32), span expands iff its
-// body is non-empty and some head of the group has z_h > theta_h.  Expanded
-// spans are appended, in ascending order, to this CTA's private slice of the
-// entry array together with their record size prefix.
+// Routing page (64 spans), processed by one warp: z_h = y_h . s_S on the
+// tensor cores, then two spans per lane for the bookkeeping.  A span expands
+// iff its body is non-empty and some head of the group has z_h > theta_h.
+// The page's expanded spans get compact entries from the page's first span
+// ordinal on; the page keeps a bit mask of them and their record bytes.
 __device__ __forceinline__ void consume_route(const uint8_t* page, const PageDesc& d, int k0,
-                                              const DecodeParams& P, SmemMisc* ms,
-                                              float* infoc, const float* ys, size_t gs) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int kk = 32 * w + lane;
-  const bool valid = kk < d.n;
-  int body = 0, rank = 0;
-  long long off = 0;
-  float z[8];
+                                              const DecodeParams& P, SmemMisc* ms, float* infoc,
+                                              const float* ys, size_t gs) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long hits = route_hits(page, d.n, ys, ms->theta, P.G);
+  // expanded spans of this page: entries compacted at [d.a, d.a + count), in
+  // span order, each with the record bytes of the ones before it (cum)
+  int body[2], rank[2];
+  long long off[2], size[2];
+  bool ex[2];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) z[h] = 0.f;
-  if (valid) {
-    body = reinterpret_cast<const int*>(page + kAuxBody)[kk];
-    rank = reinterpret_cast<const int*>(page + kAuxRank)[kk];
-    off = reinterpret_cast<const long long*>(page + kAuxOff)[kk];
-    const int row = kk & 63;
-    const uint8_t* rbox = page + (kk >> 6) * 2 * 8192;
-    const float4* y4 = reinterpret_cast<const float4*>(ys);
-#pragma unroll 4
-    for (int dc = 0; dc < 16; ++dc) {
-      const uint8_t* box = rbox + (dc >> 3) * 8192;
-      const float4 s = *reinterpret_cast<const float4*>(box + row * 128 +
-                                                        (((dc & 7) ^ (row & 7)) << 4));
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        if (h < P.G) {
-          const float4 y = y4[h * 16 + dc];
-          z[h] = fmaf(s.x, y.x, fmaf(s.y, y.y, fmaf(s.z, y.z, fmaf(s.w, y.w, z[h]))));
-        }
-      }
-    }
+  for (int half = 0; half < 2; ++half) {
+    const int kk = lane + 32 * half;
+    const bool valid = kk < d.n;
+    body[half] = valid ? reinterpret_cast<const int*>(page + kAuxBody)[kk] : 0;
+    rank[half] = valid ? reinterpret_cast<const int*>(page + kAuxRank)[kk] : 0;
+    off[half] = valid ? reinterpret_cast<const long long*>(page + kAuxOff)[kk] : 0;
+    ex[half] = valid && body[half] > 0 && ((hits >> kk) & 1ull);
+    if (valid) infoc[d.a - k0 + kk] = (body[half] > 0 && !ex[half]) ? log2f(float(body[half])) : kNegInf;
+    size[half] = ex[half] ? record_bytes(body[half], rank[half] & 0xffff, (rank[half] >> 16) & 0xffff) : 0;
   }
-  bool hit = false;
-#pragma unroll
-  for (int h = 0; h < 8; ++h)
-    if (h < P.G) hit |= z[h] > ms->theta[h];
-  const bool ex = valid && body > 0 && hit;
-  if (valid) infoc[d.a - k0 + kk] = (body > 0 && !ex) ? log2f(float(body)) : kNegInf;
-  long long size = ex ? record_bytes(body, rank & 0xffff, (rank >> 16) & 0xffff) : 0;
-  // inclusive warp scan of sizes
-  long long incl = size;
+  const uint32_t b0 = __ballot_sync(0xffffffffu, ex[0]), b1 = __ballot_sync(0xffffffffu, ex[1]);
+  const uint32_t lt = (1u << lane) - 1u;
+  long long incl0 = size[0], incl1 = size[1];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    long long v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  const uint32_t bal = __ballot_sync(0xffffffffu, ex);
-  if (lane == 31) ms->wbytes[w] = incl;
-  if (lane == 0) ms->wcnt[w] = __popc(bal);
-  named_bar(1, kConsumers);
-  int base_n = ms->n_local;
-  long long base_b = ms->bytes_local;
-  for (int ww = 0; ww < w; ++ww) {
-    base_n += ms->wcnt[ww];
-    base_b += ms->wbytes[ww];
-  }
-  if (ex) {
-    const int pos = base_n + __popc(bal & ((1u << lane) - 1u));
-    const long long cum = base_b + incl - size;
-    int4* dst = reinterpret_cast<int4*>(P.entries + gs + k0 + pos);
-    dst[0] = make_int4(d.a + kk, body, rank, 0);
-    dst[1] = make_int4(int(uint32_t(off)), int(off >> 32), int(uint32_t(cum)), int(cum >> 32));
-  }
-  named_bar(1, kConsumers);
-  if (tid == 0) {
-    int tn = 0;
-    long long tb = 0;
-    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      tn += ms->wcnt[ww];
-      tb += ms->wbytes[ww];
+    const long long v0 = __shfl_up_sync(0xffffffffu, incl0, o);
+    const long long v1 = __shfl_up_sync(0xffffffffu, incl1, o);
+    if (lane >= o) {
+      incl0 += v0;
+      incl1 += v1;
     }
-    ms->n_local += tn;
-    ms->bytes_local += tb;
   }
+  const long long tot0 = __shfl_sync(0xffffffffu, incl0, 31);
+  const long long tot1 = __shfl_sync(0xffffffffu, incl1, 31);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (ex[half]) {
+      const int idx = half ? __popc(b0) + __popc(b1 & lt) : __popc(b0 & lt);
+      const long long cum = half ? tot0 + incl1 - size[1] : incl0 - size[0];
+      int4* dst = reinterpret_cast<int4*>(P.entries + gs + d.a + idx);
+      dst[0] = make_int4(d.a + lane + 32 * half, body[half], rank[half], 0);
+      dst[1] = make_int4(int(uint32_t(off[half])), int(off[half] >> 32), int(uint32_t(cum)),
+                         int(cum >> 32));
+    }
+  }
+  const unsigned long long mask = (unsigned long long)b0 | ((unsigned long long)b1 << 32);
+  const long long bytes = tot0 + tot1;
+  if (lane == 0) {
+    ms->rmask[d.flag] = mask;
+    ms->rbytes[d.flag] = bytes;
+  }
+}
+
+// After every warp has passed its routing pages: publish this CTA's
+// expansion summary (per-page masks and bytes, totals) for the producers of
+// all CTAs of this KV head.  Warp 0 only.
+__device__ __forceinline__ void publish_routes(const DecodeParams& P, SmemMisc* ms, int g, int j,
+                                               int np) {
+  const int lane = threadIdx.x & 31;
+  int cnt = 0;
+  long long bytes = 0;
+  const size_t pb = (size_t(g) * P.cg + j) * kMaxRoutePages;
+  for (int p = lane; p < np; p += 32) {
+    const unsigned long long m = ms->rmask[p];
+    P.pmask[pb + p] = m;
+    P.pbytes[pb + p] = ms->rbytes[p];
+    cnt += __popcll(m);
+    bytes += ms->rbytes[p];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+  }
+  if (lane == 0) {
+    P.cta_n[size_t(g) * P.cg + j] = cnt;
+    P.cta_bytes[size_t(g) * P.cg + j] = bytes;
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(&P.groups[g].published, 1);
 }
 
 __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& P, int g, int j,
@@ -96,18 +105,24 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   const size_t gs = size_t(g) * P.max_spans;
   float* infoc = reinterpret_cast<float*>(smem + kOffInfo);  // summary bias per span
   float* qs = reinterpret_cast<float*>(smem + kOffScratch);         // prologue only
-  float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages only
+  float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages
 
   pdl_wait();
   WarpAcc A;
   const __nv_bfloat16* qg = P.q + (size_t(b) * P.Hq + size_t(c) * G) * kHeadDim;
+  // query A fragments of this lane (rows 0..7 = heads, zero past G), grouped
+  // by 32 head dims; stored to the warp's scratch once the prologue is done
+  uint4 qf[4];
   {
     const int r0 = lane >> 2;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int k = 16 * s + 2 * (lane & 3);
-      A.qa[s][0] = r0 < G ? *reinterpret_cast<const uint32_t*>(qg + r0 * kHeadDim + k) : 0u;
-      A.qa[s][1] = r0 < G ? *reinterpret_cast<const uint32_t*>(qg + r0 * kHeadDim + k + 8) : 0u;
+    for (int i = 0; i < 4; ++i) {
+      const int k = 32 * i + 2 * (lane & 3);
+      const __nv_bfloat16* qr = qg + r0 * kHeadDim + k;
+      qf[i].x = r0 < G ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+      qf[i].y = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+      qf[i].z = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 16) : 0u;
+      qf[i].w = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 24) : 0u;
     }
   }
 #pragma unroll
@@ -122,16 +137,16 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       qs[i] = (i / kHeadDim) < G ? __bfloat162float(qg[i]) : 0.f;
     if (tid < 8) ms->theta[tid] = tid < G ? P.theta[c * G + tid] : 0.f;
     named_bar(1, kConsumers);
-    // y_h = W_r[c] q_h from the staged rows (padded stride: conflict-free
-    // 16-byte loads), one routing coordinate per thread, heads hh, hh+2, ...
+    // y_h = W_r[c] q_h from the swizzled W_r boxes (box x: dims 32x..32x+31,
+    // 64 rows of 128 B), one routing coordinate per thread, heads hh, hh+2, ...
     if (!mbar_wait(&ms->wr_bar, 0, kWaitLimit) && tid == 0)
       set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
     const int jr = tid & 63, hh = tid >> 6;
-    const float4* wrow = reinterpret_cast<const float4*>(smem + kOffWr + jr * kWrStride);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int d4 = 0; d4 < 32; ++d4) {
-      const float4 wv = wrow[d4];
+      const float4 wv = *reinterpret_cast<const float4*>(
+          smem + kOffWr + (d4 >> 3) * 8192 + jr * 128 + (((d4 & 7) ^ (jr & 7)) << 4));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (hh + 2 * i < G) {
@@ -140,78 +155,76 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
         }
       }
     }
-    named_bar(1, kConsumers);  // qs is dead; ys may overwrite nothing it needs
 #pragma unroll
     for (int i = 0; i < 4; ++i) ys[(hh + 2 * i) * kRouteDim + jr] = acc[i];
     named_bar(1, kConsumers);
   }
 
-  int slot = 0;
-  uint32_t phase = 0;
+  // the routing weights are consumed: their space becomes per-warp scratch
+  A.qfrag = smem_u32(smem + kOffWr + w * 8192);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sts128(A.qfrag + (i * 32 + lane) * 16, qf[i]);
+  __syncwarp();
+
+  // this warp's ring: slots 2w, 2w+1
+  Ring R;
+  bool routed = false;  // passed the routing barrier
+  const int np = (k1 - k0 + kRouteSpans - 1) / kRouteSpans;
   for (;;) {
-    if (!mbar_wait(&ms->full[slot], phase, kWaitLimit)) {
-      if (tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
+    const int slot = w * kSlotsPerWarp + R.s;
+    if (!mbar_wait(&ms->full[slot], R.phase, kWaitLimit)) {
+      if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
+      if (!routed) named_bar(2, kConsumers);
       break;
     }
     const PageDesc d = ms->desc[slot];
-    const uint8_t* page = smem + slot * kPageStride;
+    const uint8_t* page = slot_ptr(smem, slot);
     const uint32_t pu = smem_u32(page);
-    switch (d.type) {
-      case PG_ROUTE:
-        consume_route(page, d, k0, P, ms, infoc, ys, gs);
-        if (d.flag) {
-          __threadfence();
-          named_bar(1, kConsumers);
-          if (tid == 0) {
-            P.cta_n[size_t(g) * P.cg + j] = ms->n_local;
-            P.cta_bytes[size_t(g) * P.cg + j] = ms->bytes_local;
-            __threadfence();
-            atomicAdd(&P.groups[g].published, 1);
-          }
-        }
-        break;
-      case PG_INFO: {
-        const uint16_t* src = reinterpret_cast<const uint16_t*>(page);
-        for (int i = tid; i < d.n; i += kConsumers) {
-          const int inf = src[i], body = inf & 0x7fff;
-          infoc[i] = (body > 0 && !(inf & 0x8000)) ? log2f(float(body)) : kNegInf;
-        }
-        named_bar(1, kConsumers);
-        break;
+    if (!routed && (d.type == PG_SYNC || d.type == PG_END)) {
+      // all routing pages of the CTA are done past this barrier
+      if (P.fused) __threadfence();
+      named_bar(2, kConsumers);
+      routed = true;
+      if (P.fused && w == 0 && d.type == PG_SYNC) publish_routes(P, ms, g, j, np);
+    }
+    // one call site per page routine keeps the kernel's code small
+    if (d.type == PG_ROUTE) {
+      consume_route(page, d, k0, P, ms, infoc, ys, gs);
+    } else if (d.type == PG_INFO) {
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(page);
+      for (int i = lane; i < d.n; i += 32) {
+        const int inf = src[i], body = inf & 0x7fff;
+        infoc[i] = (body > 0 && !(inf & 0x8000)) ? log2f(float(body)) : kNegInf;
       }
-      case PG_FULL:
-        consume_kv_tile(A, pu, pu + 16384, d.n, nullptr, P.scale_log2);
-        break;
-      case PG_SUM:
-        consume_kv_tile(A, pu, pu + 16384, d.n, infoc + (d.a - k0), P.scale_log2);
-        break;
-      case PG_EXP:  // one large record, split over pages; all warps share its tokens
-        if (d.off_a >= 0) exp_key(A, X, page + d.off_a, d.rk, P.scale_log2);
-        if (d.n > 0)
-          exp_tokens(A, X, page + d.off_uk, page + d.off_uv, d.n, d.rk, d.rv, 16 * w,
-                     16 * kConsumerWarps);
-        if (d.off_b >= 0) exp_value(A, X, page + d.off_b, d.rv);
-        break;
-      case PG_EXPM:  // several small records: warp w takes records w, w+4, ...
-        for (int i = w; i < d.n; i += kConsumerWarps) {
+    } else if (d.type == PG_FULL || d.type == PG_SUM) {
+      consume_kv_page(A, pu, pu + 2 * kBoxBytes, d.n,
+                      d.type == PG_SUM ? infoc + (d.a - k0) : nullptr, P.scale_log2);
+    } else if (d.type == PG_EXP || d.type == PG_EXPM) {
+      // PG_EXP: one part of a record split over pages; PG_EXPM: whole records
+      const int nrec = d.type == PG_EXPM ? d.n : 1;
+      for (int i = 0; i < nrec; ++i) {
+        int off_a = d.off_a, off_uk = d.off_uk, off_uv = d.off_uv, off_b = d.off_b;
+        int n = d.n, rk = d.rk, rv = d.rv;
+        if (d.type == PG_EXPM) {
           const RecInfo ri = ms->rec[slot][i];
-          const uint8_t* part = page + ri.off;
           const RecordLayout RL = record_layout(ri.b, ri.rk, ri.rv);
-          exp_key(A, X, part, ri.rk, P.scale_log2);
-          exp_tokens(A, X, part + RL.uk, part + RL.uv, ri.b, ri.rk, ri.rv, 0, 16);
-          exp_value(A, X, part + RL.vpart, ri.rv);
+          off_a = ri.off;
+          off_uk = ri.off + int(RL.uk);
+          off_uv = ri.off + int(RL.uv);
+          off_b = ri.off + int(RL.vpart);
+          n = ri.b;
+          rk = ri.rk;
+          rv = ri.rv;
         }
-        break;
-      default:
-        break;
+        if (off_a >= 0) exp_key(A, X, page + off_a, rk, P.scale_log2);
+        if (n > 0) exp_tokens(A, X, page + off_uk, page + off_uv, n, rk, rv);
+        if (off_b >= 0) exp_value(A, X, page + off_b, rv);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->empty[slot]);
     if (d.type == PG_END) break;
-    if (++slot == kPages) {
-      slot = 0;
-      phase ^= 1u;
-    }
+    ring_advance(R);
   }
 
   // ---- merge the four warps' states into this CTA's partial --------------
@@ -312,25 +325,34 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       P.lse[row] = L > 0.f ? (sm_ML[h] + log2f(L)) * kLn2 : kNegInf;
   }
   if (P.expanded_out != nullptr && P.fused) {
-    // concatenate the CTAs' ascending slices
-    int* pre = reinterpret_cast<int*>(sm_ML + 16);
-    if (tid == 0) {
-      int acc = 0;
-      for (int jj = 0; jj < cg; ++jj) {
-        pre[jj] = acc;
-        acc += __ldcg(P.cta_n + size_t(g) * cg + jj);
-      }
-      pre[cg] = acc;
-    }
-    named_bar(1, kConsumers);
+    // the CTAs' routing pages in order; page p of CTA jj covers spans
+    // sk0 + 64p + (0..63), bit i of its mask marks span sk0 + 64p + i
+    int* pre = reinterpret_cast<int*>(sm_ML + 16);  // [kMaxRoutePages + 1]
+    int base = 0;
     for (int jj = 0; jj < cg; ++jj) {
-      int a0, a1, sk0, a2;
-      fixed_range(jj, cg, n_full, n_sp, 1, a0, a1, sk0, a2);
-      const int cnt = pre[jj + 1] - pre[jj];
-      for (int i = tid; i < cnt; i += kConsumers)
-        P.expanded_out[gs + pre[jj] + i] = __ldcg(&P.entries[gs + sk0 + i].k);
+      int a0, a1, sk0, sk1;
+      fixed_range(jj, cg, n_full, n_sp, 1, a0, a1, sk0, sk1);
+      const int npj = (sk1 - sk0 + kRouteSpans - 1) / kRouteSpans;
+      const uint64_t* pm = P.pmask + (size_t(g) * cg + jj) * kMaxRoutePages;
+      if (tid == 0) {
+        int acc = 0;
+        for (int p = 0; p < npj; ++p) {
+          pre[p] = acc;
+          acc += __popcll(__ldcg(reinterpret_cast<const unsigned long long*>(pm) + p));
+        }
+        pre[npj] = acc;
+      }
+      named_bar(1, kConsumers);
+      for (int t = tid; t < npj * 64; t += kConsumers) {
+        const int p = t >> 6, i = t & 63;
+        const unsigned long long m = __ldcg(reinterpret_cast<const unsigned long long*>(pm) + p);
+        if ((m >> i) & 1ull)
+          P.expanded_out[gs + base + pre[p] + __popcll(m & ((1ull << i) - 1ull))] = sk0 + 64 * p + i;
+      }
+      base += pre[npj];
+      named_bar(1, kConsumers);
     }
-    if (tid == 0 && P.n_expanded_out != nullptr) P.n_expanded_out[g] = pre[cg];
+    if (tid == 0 && P.n_expanded_out != nullptr) P.n_expanded_out[g] = base;
   }
   named_bar(1, kConsumers);
   if (tid == 0) {
@@ -349,13 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int g = b * P.Hkv + c;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&ms->full[s], 1);
-      mbar_init(&ms->empty[s], kConsumerWarps);
+      mbar_init(&ms->empty[s], 1);  // each slot belongs to one consumer warp
     }
     mbar_init(&ms->wr_bar, 1);
-    ms->n_local = 0;
-    ms->bytes_local = 0;
     ms->is_last = 0;
     fence_mbar_init();
   }

@@ -9,18 +9,20 @@
 // in factor space: c = diag(sigma g) Vt_K q, logits = U_K c; then
 // w = U_V^T p and o += Vt_V^T diag(sigma g) w; khat/vhat are never formed.
 //
-// Structure (one CTA per (sequence, KV head, chunk); 1 CTA per SM):
-//   warp 4 (producer): streams fixed-size pages into a 4-slot shared-memory
-//     ring with TMA (3-D tiled copies, 128B swizzle, for full-resolution
-//     rows, summary rows and routing summaries; 1-D bulk copies for basis
-//     records), tracked by full/empty mbarriers.
-//   warps 0-3 (consumers): route (fused mode), then run an online softmax
-//     over the pages with mma.sync (query heads of the GQA group as the M
-//     rows, keys as N), FMA for the U factors.
-//   Split-KV: every CTA owns an equal share of the fixed bytes (routing
-//     summaries, full rows, summary rows); the expanded spans of a KV head
-//     are shared out by bytes once all its CTAs have published what they
-//     expand; the last CTA of a KV head merges the partial softmax states.
+// Structure (one CTA per (sequence, KV head, chunk); one CTA per SM):
+//   warp 4 (producer): streams pages into per-warp rings (two 19 KB slots per
+//     consumer warp) with TMA: 3-D tiled copies with 128B swizzle for
+//     full-resolution rows, summary rows, routing summaries and W_r; 1-D
+//     bulk copies for basis records.  Full/empty mbarriers per slot.
+//   warps 0-3 (consumers): each consumes its own ring independently and keeps
+//     its own online-softmax state (query heads of the GQA group as the M rows
+//     of mma.sync; keys, tokens or ranks as N).  The four states and then the
+//     CTAs' partial states are merged at the end.
+//   Work split: every CTA owns an equal share of the fixed bytes (routing
+//     summaries, full rows, summary rows), dealt to its warps round-robin; the
+//     expanded spans of a KV head are shared out among its CTAs by bytes once
+//     all of them have published what they expand, and inside a CTA each
+//     record goes to the least-loaded warp.
 #pragma once
 
 #include "sekv_common.cuh"
@@ -30,31 +32,32 @@ namespace sekv {
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kPages = 4;
-constexpr int kPageData = 32768;
-constexpr int kPageStride = 34816;  // 32 KB data + 2 KB aux, 1024-aligned
-constexpr int kAuxBody = 32768;
-constexpr int kAuxRank = 33280;
-constexpr int kAuxOff = 33792;
-constexpr int kScratchPerWarp = 3072;
-constexpr int kInfoCap = 2048;       // span-info cache entries per CTA
-constexpr int kRouteSpans = 128;     // spans per routing page
-constexpr int kTileRows = 64;        // rows per full/summary page
-constexpr int kMaxCgSmem = 256;      // CTAs per KV head the producer can index
+constexpr int kSlotsPerWarp = 2;
+constexpr int kSlots = kConsumerWarps * kSlotsPerWarp;
+constexpr int kSlotBytes = 19456;     // 18 KB data + 1 KB routing aux, 1024-aligned
+constexpr int kPageData = 18432;      // bytes of data a page may hold
+constexpr int kAuxBody = 18432;       // routing page: body lengths (64 x int32)
+constexpr int kAuxRank = 18688;       //               ranks (64 x int32)
+constexpr int kAuxOff = 18944;        //               record offsets (64 x int64)
+constexpr int kTileRows = 32;         // rows per full / summary page
+constexpr int kBoxBytes = kTileRows * 128;  // one 128B-swizzled box: 32 rows x 64 bf16
+constexpr int kRouteSpans = 64;       // spans per routing page
+constexpr int kInfoCap = 2048;        // span-info cache entries per CTA
+constexpr int kMaxRoutePages = kInfoCap / kRouteSpans;
+constexpr int kMaxCgSmem = 256;       // CTAs per KV head the producer can index
+constexpr int kMaxRecPerPage = 8;     // small basis records packed into one page
 
-constexpr int kMaxRecPerPage = 8;   // small basis records packed into one page
-constexpr int kWrStride = 528;      // W_r rows in shared memory (512 B + 16 B pad)
-
-constexpr int kOffScratch = kPages * kPageStride;
-constexpr int kOffInfo = kOffScratch + kConsumerWarps * kScratchPerWarp;
-constexpr int kOffWr = kOffInfo + kInfoCap * 4;   // info cache: one float per span
-constexpr int kOffMisc = kOffWr + kRouteDim * kWrStride;
-constexpr int kMiscBytes = 4608;
+constexpr int kOffWr = kSlots * kSlotBytes;                     // W_r, 4 swizzled boxes (32 KB)
+constexpr int kOffScratch = kOffWr + kRouteDim * kHeadDim * 4;  // q (4 KB) + y (2 KB)
+constexpr int kOffInfo = kOffScratch + 6144;                    // summary bias per span (float)
+constexpr int kOffMisc = kOffInfo + kInfoCap * 4;
+constexpr int kMiscBytes = 6144;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
 enum PageType : int {
-  PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4, PG_EXP = 5, PG_END = 6, PG_EXPM = 7
+  PG_ROUTE = 1, PG_INFO = 2, PG_FULL = 3, PG_SUM = 4, PG_EXP = 5, PG_END = 6, PG_EXPM = 7,
+  PG_SYNC = 8  // no data: every routing page of the CTA comes before it
 };
 
 // One basis record inside a PG_EXPM page (several small records per page).
@@ -65,19 +68,19 @@ struct RecInfo {
 
 struct PageDesc {
   int type;
-  int n;       // rows / spans / body tokens in this page
+  int n;       // rows / spans / body tokens / records in this page
   int a;       // first row / first span ordinal / first body token
   int rk, rv;  // expanded span: ranks
-  int flag;    // ROUTE: last routing page
-  int off_a;   // EXP: byte offset of the key part (header..Vt_K) or -1
-  int off_uk;  // EXP: byte offset of U_K rows [a, a+n)
-  int off_uv;  // EXP: byte offset of U_V rows [a, a+n)
-  int off_b;   // EXP: byte offset of the value part (sigma_V..Vt_V) or -1
+  int flag;    // PG_ROUTE: routing page index within the CTA
+  int off_a;   // PG_EXP: byte offset of the key part (header..Vt_K) or -1
+  int off_uk;  // PG_EXP: byte offset of U_K rows [a, a+n)
+  int off_uv;  // PG_EXP: byte offset of U_V rows [a, a+n)
+  int off_b;   // PG_EXP: byte offset of the value part (sigma_V..Vt_V) or -1
   int pad0, pad1;
 };
 
 struct DecodeParams {
-  CUtensorMap tm_kfull, tm_vfull, tm_ksum, tm_vsum, tm_sroute;
+  CUtensorMap tm_kfull, tm_vfull, tm_ksum, tm_vsum, tm_sroute, tm_wr;
   const int32_t* n_spans;
   const int32_t* body_len;
   const int64_t* rec_off;
@@ -94,7 +97,9 @@ struct DecodeParams {
   GroupState* groups;
   int32_t* cta_n;
   int64_t* cta_bytes;
-  ExpEntry* entries;
+  ExpEntry* entries;     // fused: by span ordinal; list mode: compact, in list order
+  uint64_t* pmask;       // fused: [group][cta][routing page] expanded-span bit masks
+  int64_t* pbytes;       // fused: [group][cta][routing page] record bytes of those spans
   const uint16_t* info;  // list mode: per-span info written by the prep kernel
   Partial* partials;
   int B, Hq, Hkv, G, n_sink, n_recent, max_spans, cap_full, cg;
@@ -149,60 +154,38 @@ __host__ __device__ inline void fixed_range(int j, int cg, int n_full, int n_sp,
 }
 
 struct SmemMisc {
-  PageDesc desc[kPages];
-  RecInfo rec[kPages][kMaxRecPerPage];
-  uint64_t full[kPages];
-  uint64_t empty[kPages];
-  uint64_t wr_bar;   // W_r rows staged in shared memory (fused mode)
-  int n_local;
-  int wcnt[kConsumerWarps];
+  PageDesc desc[kSlots];
+  RecInfo rec[kSlots][kMaxRecPerPage];
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  uint64_t wr_bar;   // W_r boxes landed (fused mode)
+  unsigned long long rmask[kMaxRoutePages];  // expanded spans per routing page (bit i: span a+i)
+  long long rbytes[kMaxRoutePages];          // their record bytes
   int is_last;
-  int abort_flag;
-  int pad0;
-  long long bytes_local;
-  long long wbytes[kConsumerWarps];
   float theta[8];
-  int pre_n[kMaxCgSmem + 1];
-  long long pre_b[kMaxCgSmem + 1];
+  int pre_n[kMaxCgSmem + 1];                 // expanded spans before CTA jj (exclusive prefix)
+  long long pre_b[kMaxCgSmem + 1];           // their record bytes
+  long long bsrc[kMaxRecPerPage];            // producer: small records waiting for a page
+  RecInfo btab[kMaxRecPerPage];
 };
 static_assert(sizeof(SmemMisc) <= kMiscBytes, "misc smem");
 
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls (~1-2 s at most)
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded polls of global counters (~2-3 s)
 
-// ----------------------------------------------------------------------------
-// producer (one lane issues; the whole warp helps in the expanded phase)
-// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint8_t* slot_ptr(uint8_t* smem, int slot) {
+  return smem + slot * kSlotBytes;
+}
+
+// Per-warp ring position (slot index within the warp's two, phase bit).
 struct Ring {
-  int slot = 0;
+  int s = 0;
   uint32_t phase = 0;
 };
 
-__device__ __forceinline__ uint8_t* page_ptr(uint8_t* smem, int slot) {
-  return smem + slot * kPageStride;
-}
-
-// Wait for a free slot, publish the descriptor (and the record table of a
-// multi-record page) and only then arm the full barrier, so that the
-// consumers' acquire on the barrier covers both.
-__device__ __forceinline__ uint8_t* push_page(uint8_t* smem, SmemMisc* ms, Ring& r,
-                                              const PageDesc& d, uint32_t bytes,
-                                              int32_t* status, bool& ok,
-                                              const RecInfo* tab = nullptr, int ntab = 0) {
-  if (!mbar_wait(&ms->empty[r.slot], r.phase ^ 1u, kWaitLimit)) {
-    set_device_error(status, DEV_WAIT_TIMEOUT, 1);
-    ok = false;
-    return nullptr;
-  }
-  ms->desc[r.slot] = d;
-  for (int i = 0; i < ntab; ++i) ms->rec[r.slot][i] = tab[i];
-  mbar_arrive_expect_tx(&ms->full[r.slot], bytes);
-  return page_ptr(smem, r.slot);
-}
-
-__device__ __forceinline__ void advance(Ring& r) {
-  if (++r.slot == kPages) {
-    r.slot = 0;
+__device__ __forceinline__ void ring_advance(Ring& r) {
+  if (++r.s == kSlotsPerWarp) {
+    r.s = 0;
     r.phase ^= 1u;
   }
 }

@@ -1,102 +1,177 @@
-// Producer warp of the decode kernel: streams pages into the ring.
+// Producer warp of the decode kernel: streams pages into the consumer warps'
+// rings (lane 0 issues; the whole warp helps in the expanded phase).
+//
+// Every page after the routing barrier goes to whichever consumer warp has a
+// free slot first, so a warp busy with a heavy page never holds up the others.
 #pragma once
 
 #include "decode_attn.cuh"
 
 namespace sekv {
 
-// Issue the pages of one expanded span.  A record that fits a page goes in
-// one copy; a larger one as its key part, its U rows in tiles, its value part.
-__device__ __forceinline__ bool issue_expanded(uint8_t* smem, SmemMisc* ms, Ring& r,
-                                               const DecodeParams& P, const ExpEntry& e,
-                                               uint32_t* last_par, bool* filled) {
-  bool ok = true;
-  const int b = e.body, rK = e.rank & 0xFFFF, rV = (e.rank >> 16) & 0xFFFF;
-  const uint8_t* rec = P.store + e.off;
+// Issue state, passed by value (it stays in registers across the calls).
+struct ProdState {
+  uint32_t rs;        // per warp w: bit 2w = next slot (0/1), bit 2w+1 = its phase
+  uint32_t filled;    // per slot: a page was ever issued into it
+  uint32_t last_par;  // per slot: phase of the last page issued into it
+  int rr;             // warp tried first by the next pick
+  int ok;             // no wait has timed out
+};
+
+__device__ __forceinline__ int ring_slot(const ProdState& S, int w) {
+  return w * kSlotsPerWarp + int((S.rs >> (2 * w)) & 1u);
+}
+__device__ __forceinline__ uint32_t ring_phase(const ProdState& S, int w) {
+  return (S.rs >> (2 * w + 1)) & 1u;
+}
+
+// Bounded wait for any warp with a free slot.
+__device__ __forceinline__ int pick_warp(SmemMisc* ms, ProdState& S, int32_t* status) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) {
+      const int w = (S.rr + i) & (kConsumerWarps - 1);
+      if (mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u)) {
+        S.rr = (w + 1) & (kConsumerWarps - 1);
+        return w;
+      }
+    }
+    if (it > 16) __nanosleep(32);
+  }
+  set_device_error(status, DEV_WAIT_TIMEOUT, 6);
+  S.ok = 0;
+  return 0;
+}
+
+// Wait for warp w's next slot, publish the descriptor (and the record table
+// of a multi-record page), and only then arm the full barrier, so that the
+// consumer's acquire on the barrier covers both.  Returns the slot or -1.
+__device__ __forceinline__ int push_page(SmemMisc* ms, ProdState& S, int w, const PageDesc& d,
+                                         uint32_t bytes, int32_t* status, int ntab = 0) {
+  const int slot = ring_slot(S, w);
+  if (!mbar_wait(&ms->empty[slot], ring_phase(S, w) ^ 1u, kWaitLimit)) {
+    set_device_error(status, DEV_WAIT_TIMEOUT, 1);
+    S.ok = 0;
+    return -1;
+  }
+  ms->desc[slot] = d;
+  for (int i = 0; i < ntab; ++i) ms->rec[slot][i] = ms->btab[i];
+  mbar_arrive_expect_tx(&ms->full[slot], bytes);
+  return slot;
+}
+
+__device__ __forceinline__ void commit_page(ProdState& S, int w, int slot) {
+  S.filled |= 1u << slot;
+  S.last_par = (S.last_par & ~(1u << slot)) | (ring_phase(S, w) << slot);
+  // advance warp w's ring: the slot bit flips, the phase flips after slot 1
+  const uint32_t v = (S.rs >> (2 * w)) & 3u;
+  const uint32_t nv = (v ^ 1u) ^ ((v & 1u) << 1);
+  S.rs = (S.rs & ~(3u << (2 * w))) | (nv << (2 * w));
+}
+
+// The n small records staged in ms->bsrc / ms->btab (bytes in all) as one page.
+__device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
+                                              const DecodeParams& P, int n, int bytes) {
+  if (n == 0 || !S.ok) return S;
+  const uint64_t pol = policy_evict_first();
+  const int w = pick_warp(ms, S, P.status);
+  if (!S.ok) return S;
+  PageDesc d{};
+  d.type = PG_EXPM;
+  d.n = n;
+  const int slot = push_page(ms, S, w, d, uint32_t(bytes), P.status, n);
+  if (slot < 0) return S;
+  uint8_t* pg = slot_ptr(smem, slot);
+  for (int i = 0; i < n; ++i) {
+    const RecInfo ri = ms->btab[i];
+    bulk_g2s_hint(pg + ri.off, P.store + ms->bsrc[i], uint32_t(record_bytes(ri.b, ri.rk, ri.rv)),
+                  &ms->full[slot], pol);
+  }
+  commit_page(S, w, slot);
+  return S;
+}
+
+// A record larger than a page: its key part, its U rows in tiles, its value
+// part, all to one warp (the partial state of the span stays in its registers).
+__device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdState S,
+                                              const DecodeParams& P, int b, int rank,
+                                              long long off) {
+  const uint64_t pol = policy_evict_first();
+  const int w = pick_warp(ms, S, P.status);
+  if (!S.ok) return S;
+  const int rK = rank & 0xFFFF, rV = (rank >> 16) & 0xFFFF;
+  const uint8_t* rec = P.store + off;
   const RecordLayout L = record_layout(b, rK, rV);
   PageDesc d{};
   d.type = PG_EXP;
   d.rk = rK;
   d.rv = rV;
-  if (L.total <= kPageData) {
-    d.n = b; d.a = 0;
-    d.off_a = 0; d.off_uk = int(L.uk); d.off_uv = int(L.uv); d.off_b = int(L.vpart);
-    uint8_t* pg = push_page(smem, ms, r, d, uint32_t(L.total), P.status, ok);
-    if (!ok) return false;
-    bulk_g2s(pg, rec, uint32_t(L.total), &ms->full[r.slot]);
-    filled[r.slot] = true;
-    last_par[r.slot] = r.phase;
-    advance(r);
-    return true;
-  }
-  // key part
   d.n = 0; d.a = 0; d.off_a = 0; d.off_uk = 0; d.off_uv = 0; d.off_b = -1;
-  {
-    uint8_t* pg = push_page(smem, ms, r, d, uint32_t(L.uk), P.status, ok);
-    if (!ok) return false;
-    bulk_g2s(pg, rec, uint32_t(L.uk), &ms->full[r.slot]);
-    filled[r.slot] = true;
-    last_par[r.slot] = r.phase;
-    advance(r);
-  }
-  // U rows: [i0, i0 + n) of U_K at +0 and of U_V at +16384
-  const int rmax = r8(rK) > r8(rV) ? r8(rK) : r8(rV);
-  int rows = rmax > 0 ? (16384 / (2 * rmax)) & ~15 : 512;
+  int slot = push_page(ms, S, w, d, uint32_t(L.uk), P.status);
+  if (slot < 0) return S;
+  bulk_g2s_hint(slot_ptr(smem, slot), rec, uint32_t(L.uk), &ms->full[slot], pol);
+  commit_page(S, w, slot);
+  const int row_bytes = 2 * (r8(rK) + r8(rV));
+  int rows = row_bytes > 0 ? (kPageData / row_bytes) & ~15 : 512;
   if (rows > 512) rows = 512;
   for (int i0 = 0; i0 < b; i0 += rows) {
     const int n = (b - i0) < rows ? (b - i0) : rows;
     const uint32_t bk = uint32_t(2 * n * r8(rK)), bv = uint32_t(2 * n * r8(rV));
-    d.n = n; d.a = i0; d.off_a = -1; d.off_uk = 0; d.off_uv = 16384; d.off_b = -1;
-    uint8_t* pg = push_page(smem, ms, r, d, bk + bv, P.status, ok);
-    if (!ok) return false;
-    if (bk) bulk_g2s(pg, rec + L.uk + 2 * int64_t(i0) * r8(rK), bk, &ms->full[r.slot]);
-    if (bv) bulk_g2s(pg + 16384, rec + L.uv + 2 * int64_t(i0) * r8(rV), bv, &ms->full[r.slot]);
-    filled[r.slot] = true;
-    last_par[r.slot] = r.phase;
-    advance(r);
+    d.n = n; d.a = i0; d.off_a = -1; d.off_uk = 0; d.off_uv = int(bk); d.off_b = -1;
+    slot = push_page(ms, S, w, d, bk + bv, P.status);
+    if (slot < 0) return S;
+    uint8_t* pg = slot_ptr(smem, slot);
+    if (bk) bulk_g2s_hint(pg, rec + L.uk + 2 * int64_t(i0) * r8(rK), bk, &ms->full[slot], pol);
+    if (bv)
+      bulk_g2s_hint(pg + bk, rec + L.uv + 2 * int64_t(i0) * r8(rV), bv, &ms->full[slot], pol);
+    commit_page(S, w, slot);
   }
-  // value part
-  {
-    const uint32_t bytes = uint32_t(L.total - L.vpart);
-    d.n = 0; d.a = 0; d.off_a = -1; d.off_b = 0;
-    uint8_t* pg = push_page(smem, ms, r, d, bytes, P.status, ok);
-    if (!ok) return false;
-    if (bytes) bulk_g2s(pg, rec + L.vpart, bytes, &ms->full[r.slot]);
-    filled[r.slot] = true;
-    last_par[r.slot] = r.phase;
-    advance(r);
-  }
-  return true;
+  const uint32_t vb = uint32_t(L.total - L.vpart);
+  d.n = 0; d.a = 0; d.off_a = -1; d.off_b = 0;
+  slot = push_page(ms, S, w, d, vb, P.status);
+  if (slot < 0) return S;
+  if (vb) bulk_g2s_hint(slot_ptr(smem, slot), rec + L.vpart, vb, &ms->full[slot], pol);
+  commit_page(S, w, slot);
+  return S;
 }
 
-// Small records waiting to be packed into one page (producer lane 0).
-struct Batch {
-  int n = 0;
-  int64_t bytes = 0;
-  int64_t src[kMaxRecPerPage];
-  RecInfo tab[kMaxRecPerPage];
-};
-
-__device__ __forceinline__ bool flush_batch(uint8_t* smem, SmemMisc* ms, Ring& r,
-                                            const DecodeParams& P, Batch& bat,
-                                            uint32_t* last_par, bool* filled) {
-  if (bat.n == 0) return true;
-  bool ok = true;
+// Fixed page t of this CTA: full-resolution rows first, then summary rows,
+// 32 per page, to the first warp with a free slot.
+__device__ __noinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, ProdState S,
+                                              const DecodeParams& P, int t, int nfp, int f0,
+                                              int f1, int k0, int k1, int g) {
+  const int w = pick_warp(ms, S, P.status);
+  if (!S.ok) return S;
   PageDesc d{};
-  d.type = PG_EXPM;
-  d.n = bat.n;
-  uint8_t* pg = push_page(smem, ms, r, d, uint32_t(bat.bytes), P.status, ok, bat.tab, bat.n);
-  if (!ok) return false;
-  for (int i = 0; i < bat.n; ++i) {
-    const int64_t sz = record_bytes(bat.tab[i].b, bat.tab[i].rk, bat.tab[i].rv);
-    bulk_g2s(pg + bat.tab[i].off, P.store + bat.src[i], uint32_t(sz), &ms->full[r.slot]);
+  const bool full = t < nfp;
+  const int a = full ? f0 + kTileRows * t : k0 + kTileRows * (t - nfp);
+  const int e = full ? f1 : k1;
+  d.type = full ? PG_FULL : PG_SUM;
+  d.n = (e - a) < kTileRows ? (e - a) : kTileRows;
+  d.a = a;
+  const int slot = push_page(ms, S, w, d, 4 * kBoxBytes, P.status);
+  if (slot < 0) return S;
+  uint8_t* pg = slot_ptr(smem, slot);
+  const CUtensorMap* tk = full ? &P.tm_kfull : &P.tm_ksum;
+  const CUtensorMap* tv = full ? &P.tm_vfull : &P.tm_vsum;
+  const uint64_t pol = policy_evict_first();
+  tma_g2s_3d_hint(pg, tk, 0, a, g, &ms->full[slot], pol);
+  tma_g2s_3d_hint(pg + kBoxBytes, tk, 64, a, g, &ms->full[slot], pol);
+  tma_g2s_3d_hint(pg + 2 * kBoxBytes, tv, 0, a, g, &ms->full[slot], pol);
+  tma_g2s_3d_hint(pg + 3 * kBoxBytes, tv, 64, a, g, &ms->full[slot], pol);
+  commit_page(S, w, slot);
+  return S;
+}
+
+// Inclusive warp scan of a 64-bit value.
+__device__ __forceinline__ long long warp_incl_scan(long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
   }
-  filled[r.slot] = true;
-  last_par[r.slot] = r.phase;
-  advance(r);
-  bat.n = 0;
-  bat.bytes = 0;
-  return true;
+  return v;
 }
 
 __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P, int g, int j,
@@ -106,14 +181,11 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
   const int n_full = P.n_sink + n_sp + P.n_recent;
   int f0, f1, k0, k1;
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
-  Ring r;
-  uint32_t last_par[kPages];
-  bool filled[kPages];
-#pragma unroll
-  for (int s = 0; s < kPages; ++s) { filled[s] = false; last_par[s] = 0; }
-  bool ok = true;
+  const int nfp = (f1 - f0 + kTileRows - 1) / kTileRows;
+  const int nfixed = nfp + (k1 - k0 + kTileRows - 1) / kTileRows;
+  ProdState S{0u, 0u, 0u, 0, 1};
   const size_t gs = size_t(g) * P.max_spans;
-  Batch bat;
+  int t_fixed = 0;  // fixed pages issued so far
 
   // list mode reads what the preparation kernel wrote: wait for it first
   if (!P.fused) pdl_wait();
@@ -122,180 +194,230 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
     prefetch_tmap(&P.tm_vfull);
     prefetch_tmap(&P.tm_ksum);
     prefetch_tmap(&P.tm_vsum);
+    PageDesc d{};
     if (P.fused) {
       prefetch_tmap(&P.tm_sroute);
-      // routing weights of this KV head, rows padded to kWrStride bytes
+      // routing weights of this KV head: four 128B-swizzled boxes of 64 rows x 32 floats
       mbar_arrive_expect_tx(&ms->wr_bar, kRouteDim * kHeadDim * 4);
-      for (int row = 0; row < kRouteDim; ++row)
-        bulk_g2s(smem + kOffWr + row * kWrStride,
-                 P.W_r + (size_t(c) * kRouteDim + row) * kHeadDim, kHeadDim * 4, &ms->wr_bar);
-    }
-    PageDesc d{};
-    // 1. routing pages (fused) or the span-info page (list mode)
-    if (P.fused) {
-      int k = k0;
-      do {
+      for (int x = 0; x < 4; ++x)
+        tma_g2s_3d(smem + kOffWr + x * 8192, &P.tm_wr, 32 * x, 0, c, &ms->wr_bar);
+      // routing pages, 64 spans each
+      const uint64_t pol = policy_evict_first();
+      for (int k = k0, p = 0; S.ok && k < k1; k += kRouteSpans, ++p) {
         const int n = (k1 - k) < kRouteSpans ? (k1 - k) : kRouteSpans;
-        d.type = PG_ROUTE; d.n = n; d.a = k; d.flag = (k + n >= k1);
-        const int nb = (n + 63) / 64;  // row boxes of 64 spans
-        const uint32_t n4 = uint32_t((n + 3) & ~3);
-        const uint32_t n2 = uint32_t((n + 1) & ~1);
-        const uint32_t bytes = n > 0 ? nb * 2 * 8192 + n4 * 4 * 2 + n2 * 8 : 0;
-        uint8_t* pg = push_page(smem, ms, r, d, bytes, P.status, ok);
-        if (!ok) break;
-        if (n > 0) {
-          for (int rb = 0; rb < nb; ++rb)
-            for (int cb = 0; cb < 2; ++cb)
-              tma_g2s_3d(pg + (rb * 2 + cb) * 8192, &P.tm_sroute, cb * 32, k + rb * 64, g,
-                         &ms->full[r.slot]);
-          bulk_g2s(pg + kAuxBody, P.body_len + size_t(b) * P.max_spans + k, n4 * 4,
-                   &ms->full[r.slot]);
-          bulk_g2s(pg + kAuxRank, P.rec_rank + gs + k, n4 * 4, &ms->full[r.slot]);
-          bulk_g2s(pg + kAuxOff, P.rec_off + gs + k, n2 * 8, &ms->full[r.slot]);
-        }
-        filled[r.slot] = true; last_par[r.slot] = r.phase;
-        advance(r);
-        k += n;
-      } while (k < k1);
-    } else if (ok) {
+        const uint32_t n4 = uint32_t((n + 3) & ~3), n2 = uint32_t((n + 1) & ~1);
+        d.type = PG_ROUTE; d.n = n; d.a = k; d.flag = p;
+        const int w = pick_warp(ms, S, P.status);
+        if (!S.ok) break;
+        const int slot = push_page(ms, S, w, d, 2 * 8192 + n4 * 8 + n2 * 8, P.status);
+        if (slot < 0) break;
+        uint8_t* pg = slot_ptr(smem, slot);
+        tma_g2s_3d_hint(pg, &P.tm_sroute, 0, k, g, &ms->full[slot], pol);
+        tma_g2s_3d_hint(pg + 8192, &P.tm_sroute, 32, k, g, &ms->full[slot], pol);
+        bulk_g2s_hint(pg + kAuxBody, P.body_len + size_t(b) * P.max_spans + k, n4 * 4,
+                      &ms->full[slot], pol);
+        bulk_g2s_hint(pg + kAuxRank, P.rec_rank + gs + k, n4 * 4, &ms->full[slot], pol);
+        bulk_g2s_hint(pg + kAuxOff, P.rec_off + gs + k, n2 * 8, &ms->full[slot], pol);
+        commit_page(S, w, slot);
+      }
+    } else if (k1 > k0) {
       const int n = k1 - k0;
       const uint32_t bytes = uint32_t(pad16(2 * int64_t(n)));
       d.type = PG_INFO; d.n = n; d.a = k0;
-      uint8_t* pg = push_page(smem, ms, r, d, bytes, P.status, ok);
-      if (ok) {
-        if (bytes) bulk_g2s(pg, P.info + gs + k0, bytes, &ms->full[r.slot]);
-        filled[r.slot] = true; last_par[r.slot] = r.phase;
-        advance(r);
+      const int slot = push_page(ms, S, 0, d, bytes, P.status);
+      if (slot >= 0) {
+        bulk_g2s(slot_ptr(smem, slot), P.info + gs + k0, bytes, &ms->full[slot]);
+        commit_page(S, 0, slot);
       }
     }
-    // 2. full-resolution rows
-    for (int f = f0; ok && f < f1; f += kTileRows) {
-      const int n = (f1 - f) < kTileRows ? (f1 - f) : kTileRows;
-      d.type = PG_FULL; d.n = n; d.a = f;
-      uint8_t* pg = push_page(smem, ms, r, d, 4 * 8192, P.status, ok);
-      if (!ok) break;
-      tma_g2s_3d(pg, &P.tm_kfull, 0, f, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 8192, &P.tm_kfull, 64, f, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 16384, &P.tm_vfull, 0, f, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 24576, &P.tm_vfull, 64, f, g, &ms->full[r.slot]);
-      filled[r.slot] = true; last_par[r.slot] = r.phase;
-      advance(r);
-    }
-    // 3. summary rows of the span range
-    for (int k = k0; ok && k < k1; k += kTileRows) {
-      const int n = (k1 - k) < kTileRows ? (k1 - k) : kTileRows;
-      d.type = PG_SUM; d.n = n; d.a = k;
-      uint8_t* pg = push_page(smem, ms, r, d, 4 * 8192, P.status, ok);
-      if (!ok) break;
-      tma_g2s_3d(pg, &P.tm_ksum, 0, k, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 8192, &P.tm_ksum, 64, k, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 16384, &P.tm_vsum, 0, k, g, &ms->full[r.slot]);
-      tma_g2s_3d(pg + 24576, &P.tm_vsum, 64, k, g, &ms->full[r.slot]);
-      filled[r.slot] = true; last_par[r.slot] = r.phase;
-      advance(r);
+    // every warp passes the routing barrier at this page
+    for (int w = 0; S.ok && w < kConsumerWarps; ++w) {
+      d = PageDesc{};
+      d.type = PG_SYNC;
+      const int slot = push_page(ms, S, w, d, 0, P.status);
+      if (slot >= 0) commit_page(S, w, slot);
     }
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
 
-  // 4. expanded spans: wait until every CTA of this KV head has published,
-  // then take the entries whose byte offset falls in this CTA's share.
+  // Until every CTA of this KV head has published its expanded spans, keep
+  // the warps busy with fixed pages (at most three quarters of them: the
+  // rest balance the tail).
   pdl_wait();
-  if (ok) {
-    if (P.fused) {
-      int pub = 0;
-      if (lane == 0) {
-        uint32_t it = 0;
-        while ((pub = ld_acquire(&P.groups[g].published)) < P.cg && it < kSpinLimit) {
-          ++it;
-          __nanosleep(128);
-        }
-        if (pub < P.cg) set_device_error(P.status, DEV_WAIT_TIMEOUT, 2);
-      }
-      pub = __shfl_sync(0xffffffffu, pub, 0);
-      if (pub < P.cg) ok = false;
+  if (lane == 0 && S.ok) {
+    const int part = (3 * nfixed + 3) / 4;
+    while (S.ok && t_fixed < part) {
+      if (P.fused && ld_acquire(&P.groups[g].published) >= P.cg) break;
+      S = issue_fixed(smem, ms, S, P, t_fixed, nfp, f0, f1, k0, k1, g);
+      ++t_fixed;
     }
   }
-  if (ok) {
-    const int cg = P.cg;
-    // per-CTA entry counts and byte totals -> exclusive prefixes in smem
-    for (int jj = lane; jj < cg; jj += 32) {
-      ms->pre_n[jj + 1] = __ldcg(P.cta_n + size_t(g) * cg + jj);
-      ms->pre_b[jj + 1] = __ldcg(reinterpret_cast<const long long*>(P.cta_bytes) + size_t(g) * cg + jj);
-    }
-    __syncwarp();
+  S.ok = __shfl_sync(0xffffffffu, S.ok, 0);
+  t_fixed = __shfl_sync(0xffffffffu, t_fixed, 0);
+
+  // expanded spans: wait until every CTA of this KV head has published,
+  // then take the entries whose byte offset falls in this CTA's share.
+  if (S.ok && P.fused) {
+    int pub = 0;
     if (lane == 0) {
-      ms->pre_n[0] = 0;
-      ms->pre_b[0] = 0;
-      for (int jj = 1; jj <= cg; ++jj) {
-        ms->pre_n[jj] += ms->pre_n[jj - 1];
-        ms->pre_b[jj] += ms->pre_b[jj - 1];
+      uint32_t it = 0;
+      while ((pub = ld_acquire(&P.groups[g].published)) < P.cg && it < kSpinLimit) {
+        ++it;
+        __nanosleep(64);
       }
+      if (pub < P.cg) set_device_error(P.status, DEV_WAIT_TIMEOUT, 2);
     }
-    __syncwarp();
+    pub = __shfl_sync(0xffffffffu, pub, 0);
+    if (pub < P.cg) S.ok = 0;
+  }
+  int bn = 0, bbytes = 0;  // staged small records (lane 0)
+  if (S.ok) {
+    const int cg = P.cg;
+    // round trip 1: expanded-span counts and bytes of every CTA, prefixed
+    {
+      long long carry = 0;
+      int ncarry = 0;
+      for (int j0 = 0; j0 < cg; j0 += 32) {
+        const int jj = j0 + lane;
+        const long long v =
+            jj < cg ? __ldcg(reinterpret_cast<const long long*>(P.cta_bytes) + size_t(g) * cg + jj)
+                    : 0;
+        const int cn = jj < cg ? __ldcg(P.cta_n + size_t(g) * cg + jj) : 0;
+        const long long inc = warp_incl_scan(v);
+        const long long incn = warp_incl_scan(cn);
+        if (jj < cg) {
+          ms->pre_b[jj] = carry + inc - v;
+          ms->pre_n[jj] = ncarry + int(incn) - cn;
+        }
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+        ncarry += int(__shfl_sync(0xffffffffu, incn, 31));
+      }
+      if (lane == 0) {
+        ms->pre_b[cg] = carry;
+        ms->pre_n[cg] = ncarry;
+      }
+      __syncwarp();
+    }
     const long long Tb = ms->pre_b[cg];
     const long long lo = Tb * j / cg, hi = Tb * (j + 1) / cg;
-    // walk the sublists that can hold entries starting in [lo, hi)
-    for (int jj = 0; jj < cg && ok; ++jj) {
+    // lanes hold candidate entries in byte order; lane 0 takes those that
+    // start in [lo, hi): into the current batch, or as a split record
+    auto offer = [&](bool mine, const ExpEntry& en) {
+      uint32_t bal = __ballot_sync(0xffffffffu, mine);
+      while (bal && S.ok) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1;
+        const int body = __shfl_sync(0xffffffffu, en.body, src);
+        const int rank = __shfl_sync(0xffffffffu, en.rank, src);
+        const long long off = __shfl_sync(0xffffffffu, en.off, src);
+        if (lane == 0) {
+          const int xr = rank & 0xFFFF, xv = (rank >> 16) & 0xFFFF;
+          const int sz = int(record_bytes(body, xr, xv));
+          if (sz > kPageData) {
+            S = issue_split(smem, ms, S, P, body, rank, off);
+          } else {
+            if (bn == kMaxRecPerPage || bbytes + sz > kPageData) {
+              S = flush_batch(smem, ms, S, P, bn, bbytes);
+              bn = 0;
+              bbytes = 0;
+            }
+            ms->bsrc[bn] = off;
+            ms->btab[bn] = RecInfo{bbytes, body, xr, xv};
+            bbytes += sz;
+            ++bn;
+          }
+        }
+        S.ok = __shfl_sync(0xffffffffu, S.ok, 0);
+      }
+    };
+    for (int jj = 0; jj < cg && S.ok; ++jj) {
       const int cnt = ms->pre_n[jj + 1] - ms->pre_n[jj];
       if (cnt == 0 || ms->pre_b[jj + 1] <= lo) continue;
       if (ms->pre_b[jj] >= hi) break;
-      int sk0 = 0;
-      if (P.fused) {
-        int a0, a1, a2;
-        fixed_range(jj, cg, n_full, n_sp, 1, a0, a1, sk0, a2);
+      if (!P.fused) {
+        // list mode: one compact sublist with per-entry byte offsets
+        const ExpEntry* base = P.entries + gs;
+        for (int e0 = 0; e0 < cnt && S.ok; e0 += 32) {
+          ExpEntry en{};
+          bool mine = false;
+          if (e0 + lane < cnt) {
+            const int4* src = reinterpret_cast<const int4*>(base + e0 + lane);
+            const int4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+            en.k = v0.x; en.body = v0.y; en.rank = v0.z;
+            en.off = (long long)(uint32_t(v1.x)) | ((long long)v1.y << 32);
+            const long long cum = (long long)(uint32_t(v1.z)) | ((long long)v1.w << 32);
+            const long long st = ms->pre_b[jj] + cum;
+            mine = st >= lo && st < hi && en.body > 0;
+          }
+          offer(mine, en);
+        }
+        continue;
       }
-      const ExpEntry* base = P.entries + gs + sk0;
-      for (int e0 = 0; e0 < cnt && ok; e0 += 32) {
+      // fused mode, round trip 2: CTA jj's routing pages (one per lane)
+      int a0, a1, sk0, sk1;
+      fixed_range(jj, cg, n_full, n_sp, 1, a0, a1, sk0, sk1);
+      const int npj = (sk1 - sk0 + kRouteSpans - 1) / kRouteSpans;
+      const size_t pb = (size_t(g) * cg + jj) * kMaxRoutePages;
+      const long long pbytes =
+          lane < npj ? __ldcg(reinterpret_cast<const long long*>(P.pbytes) + pb + lane) : 0;
+      const unsigned long long pmask =
+          lane < npj ? __ldcg(reinterpret_cast<const unsigned long long*>(P.pmask) + pb + lane)
+                     : 0ull;
+      const long long pstart = ms->pre_b[jj] + warp_incl_scan(pbytes) - pbytes;
+      const bool hit = lane < npj && pbytes > 0 && pstart < hi && pstart + pbytes > lo;
+      const int cntp = hit ? __popcll(pmask) : 0;
+      const int cincl = int(warp_incl_scan(cntp));
+      const int cpre = cincl - cntp;
+      const int E = __shfl_sync(0xffffffffu, cincl, 31);
+      // round trip 3: the entries of the hit pages, flattened over the lanes
+      for (int f0 = 0; f0 < E && S.ok; f0 += 32) {
+        const int f = f0 + lane;
+        int pl = 0;  // last page whose entry prefix is <= f
+#pragma unroll
+        for (int step = 16; step; step >>= 1) {
+          const int v = __shfl_sync(0xffffffffu, cpre, (pl + step) & 31);
+          if (pl + step < 32 && v <= f) pl += step;
+        }
+        const int i = f - __shfl_sync(0xffffffffu, cpre, pl);
+        const long long pst = __shfl_sync(0xffffffffu, pstart, pl);
         ExpEntry en{};
         bool mine = false;
-        if (e0 + lane < cnt) {
-          const int4* src = reinterpret_cast<const int4*>(base + e0 + lane);
-          int4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+        if (f < E) {
+          const int4* src = reinterpret_cast<const int4*>(P.entries + gs + sk0 +
+                                                          kRouteSpans * pl + i);
+          const int4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
           en.k = v0.x; en.body = v0.y; en.rank = v0.z;
           en.off = (long long)(uint32_t(v1.x)) | ((long long)v1.y << 32);
           const long long cum = (long long)(uint32_t(v1.z)) | ((long long)v1.w << 32);
-          const long long st = ms->pre_b[jj] + cum;
-          mine = st >= lo && st < hi && en.body > 0;
+          const long long st = pst + cum;
+          mine = st >= lo && st < hi;
         }
-        uint32_t bal = __ballot_sync(0xffffffffu, mine);
-        while (bal && ok) {
-          const int src_lane = __ffs(bal) - 1;
-          bal &= bal - 1;
-          ExpEntry x;
-          x.k = __shfl_sync(0xffffffffu, en.k, src_lane);
-          x.body = __shfl_sync(0xffffffffu, en.body, src_lane);
-          x.rank = __shfl_sync(0xffffffffu, en.rank, src_lane);
-          x.off = __shfl_sync(0xffffffffu, en.off, src_lane);
-          if (lane == 0) {
-            const int xr = x.rank & 0xFFFF, xv = (x.rank >> 16) & 0xFFFF;
-            const int64_t sz = record_bytes(x.body, xr, xv);
-            if (sz > kPageData) {  // too big for a page: split path
-              ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
-              if (ok) ok = issue_expanded(smem, ms, r, P, x, last_par, filled);
-            } else {
-              if (bat.n == kMaxRecPerPage || bat.bytes + sz > kPageData)
-                ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
-              bat.src[bat.n] = x.off;
-              bat.tab[bat.n] = RecInfo{int(bat.bytes), x.body, xr, xv};
-              bat.bytes += sz;
-              ++bat.n;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
+        offer(mine, en);
       }
     }
   }
-  if (lane == 0 && ok) ok = flush_batch(smem, ms, r, P, bat, last_par, filled);
   if (lane == 0) {
-    PageDesc d{};
-    d.type = PG_END;
-    bool ok2 = true;
-    push_page(smem, ms, r, d, 0, P.status, ok2);
-    if (ok2) { filled[r.slot] = true; last_par[r.slot] = r.phase; advance(r); }
+    S = flush_batch(smem, ms, S, P, bn, bbytes);
+    // the remaining fixed pages, to whichever warp frees a slot first
+    while (S.ok && t_fixed < nfixed) {
+      S = issue_fixed(smem, ms, S, P, t_fixed, nfp, f0, f1, k0, k1, g);
+      ++t_fixed;
+    }
+    // every consumer warp ends with an END page
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      PageDesc d{};
+      d.type = PG_END;
+      ProdState S2 = S;
+      S2.ok = 1;
+      const int slot = push_page(ms, S2, w, d, 0, P.status);
+      if (slot >= 0) commit_page(S2, w, slot);
+      S.rs = S2.rs;
+      S.filled = S2.filled;
+      S.last_par = S2.last_par;
+    }
     // drain: every issued copy has landed before the CTA may exit
-    for (int s = 0; s < kPages; ++s)
-      if (filled[s] && !mbar_wait(&ms->full[s], last_par[s], kWaitLimit))
+    for (int s = 0; s < kSlots; ++s)
+      if (((S.filled >> s) & 1u) &&
+          !mbar_wait(&ms->full[s], (S.last_par >> s) & 1u, kWaitLimit))
         set_device_error(P.status, DEV_WAIT_TIMEOUT, 3);
   }
 }

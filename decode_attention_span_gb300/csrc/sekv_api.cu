@@ -79,7 +79,9 @@ WsLayout ws_layout(const sekv_config* cfg, int sms) {
   L.partials = off;   off += align256(ng * L.cg * sizeof(Partial));
   L.route_list = off; off += align256(ng * ms * 4);
   L.route_cnt = off;  off += align256(ng * L.route_chunks * 4);
-  // cta_bytes lives after route_cnt
+  L.pmask = off;      off += align256(ng * L.cg * kMaxRoutePages * 8);
+  L.pbytes = off;     off += align256(ng * L.cg * kMaxRoutePages * 8);
+  // cta_bytes lives after pbytes
   L.total = off + align256(ng * L.cg * 8);
   return L;
 }
@@ -205,12 +207,12 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   const int ng = L.ng;
   const uint64_t cap_full = uint64_t(cfg->n_sink) + cfg->max_spans + cfg->n_recent;
   bool ok = true;
-  ok &= encode_3d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, 64, 64);
-  ok &= encode_3d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, 64, 64);
-  ok &= encode_3d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, 64, 64);
-  ok &= encode_3d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, 64, 64);
+  ok &= encode_3d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, 64, kTileRows);
+  ok &= encode_3d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, 64, kTileRows);
+  ok &= encode_3d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, 64, kTileRows);
+  ok &= encode_3d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, 64, kTileRows);
   if (fused) {
-    ok &= encode_3d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, 32, 64);
+    ok &= encode_3d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, 32, kRouteSpans);
   } else {
     P.tm_sroute = P.tm_ksum;
   }
@@ -226,6 +228,8 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.cta_bytes = reinterpret_cast<int64_t*>(w + ws_cta_bytes(L));
   P.entries = reinterpret_cast<ExpEntry*>(w + L.entries);
   P.info = reinterpret_cast<const uint16_t*>(w + L.info);
+  P.pmask = reinterpret_cast<uint64_t*>(w + L.pmask);
+  P.pbytes = reinterpret_cast<int64_t*>(w + L.pbytes);
   P.partials = reinterpret_cast<Partial*>(w + L.partials);
   P.B = cfg->batch;
   P.Hq = cfg->n_q_heads;
@@ -238,6 +242,14 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.cg = L.cg;
   P.fused = fused ? 1 : 0;
   return SEKV_OK;
+}
+
+// W_r [Hkv][64][128] fp32 as a tensor of boxes of 64 rows x 32 floats (128B swizzle)
+sekv_status encode_wr(DecodeParams& P, const float* W_r, const sekv_config* cfg) {
+  return encode_3d(&P.tm_wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W_r, 128, kRouteDim,
+                   cfg->n_kv_heads, 4, 32, kRouteDim)
+             ? SEKV_OK
+             : SEKV_ERR_CUDA;
 }
 
 sekv_status launch_decode(const DecodeParams& P, const WsLayout& L, const sekv_config* cfg,
@@ -318,6 +330,8 @@ extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer
   P.store = static_cast<const uint8_t*>(cache->store);
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.W_r = W_r;
+  st = encode_wr(P, W_r, cfg);
+  if (st != SEKV_OK) return st;
   P.theta = theta;
   P.out = out;
   P.lse = lse;
