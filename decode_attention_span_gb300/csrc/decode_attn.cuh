@@ -105,6 +105,7 @@ struct DecodeParams {
   int B, Hq, Hkv, G, n_sink, n_recent, max_spans, cap_full, cg;
   float scale_log2;
   int fused;
+  int rank_lim;  // largest record rank the kernel instance handles (16 KS)
 };
 
 struct PrepParams {
@@ -124,33 +125,41 @@ struct PrepParams {
   int Hkv, max_spans, cg;
 };
 
+template <int KS>
 __global__ void decode_kernel(const __grid_constant__ DecodeParams P);
 __global__ void prep_list_kernel(const PrepParams P);
 
-// Fixed-part split: rows cost 2 units (512 B of K+V), spans 3 units in fused
-// mode (512 B of summary K+V plus 256 B of routing summary) or 2 in list mode.
-// Span boundaries are rounded up to multiples of 8 so that every per-span
-// array slice starts 16-byte aligned.
+// Host-side handles of the decode kernel instances (ranks up to 16 KS).
+const void* decode_kernel_fn_ks1();
+const void* decode_kernel_fn_ks2();
+const void* decode_kernel_fn_ks3();
+const void* decode_kernel_fn_ks4();
+
+// Fixed-part split: CTA j of cg takes an equal share of the full-resolution
+// rows and an equal share of the spans (routing summaries and summary rows),
+// so routing is spread over all CTAs of a KV head.  Span boundaries are
+// rounded up to multiples of 8 so that every per-span array slice starts
+// 16-byte aligned.  32-bit arithmetic: the host rejects shapes with
+// (2 (n_sink + n_recent) + 5 max_spans) * 256 >= 2^31.  (fused: unused, the
+// split is the same in both modes.)
 __host__ __device__ inline void fixed_range(int j, int cg, int n_full, int n_sp, int fused,
                                             int& f0, int& f1, int& k0, int& k1) {
-  const int64_t ws = fused ? 3 : 2;
-  const int64_t U = 2 * int64_t(n_full) + ws * int64_t(n_sp);
-  const int64_t x0 = U * j / cg, x1 = U * (j + 1) / cg;
-  auto fpos = [&](int64_t x) -> int {
-    int64_t v = (x + 1) / 2;
-    return int(v < n_full ? v : n_full);
+  (void)fused;
+  f0 = n_full * j / cg;
+  f1 = n_full * (j + 1) / cg;
+  auto kpos = [&](int jj) -> int {
+    const int v = ((n_sp * jj / cg) + 7) & ~7;
+    return v < n_sp ? v : n_sp;
   };
-  auto kpos = [&](int64_t x) -> int {
-    int64_t r = x - 2 * int64_t(n_full);
-    if (r <= 0) return 0;
-    int64_t v = (r + ws - 1) / ws;
-    v = (v + 7) & ~int64_t(7);
-    return int(v < n_sp ? v : n_sp);
-  };
-  f0 = fpos(x0);
-  f1 = fpos(x1);
-  k0 = kpos(x0);
-  k1 = kpos(x1);
+  k0 = kpos(j);
+  k1 = kpos(j + 1);
+}
+
+// Boundary j of cg equal shares of T bytes (monotone in j, 0 at j = 0, T at
+// j = cg); every CTA evaluates the same expression, so the shares tile [0, T).
+__host__ __device__ inline long long byte_split(long long T, int j, int cg) {
+  if (j >= cg) return T;
+  return (long long)((double)T * j / cg);
 }
 
 struct SmemMisc {

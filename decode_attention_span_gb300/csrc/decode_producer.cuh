@@ -25,35 +25,39 @@ __device__ __forceinline__ uint32_t ring_phase(const ProdState& S, int w) {
   return (S.rs >> (2 * w + 1)) & 1u;
 }
 
-// Bounded wait for any warp with a free slot.
+// First warp (from S.rr on) whose next slot is free; bounded.
 __device__ __forceinline__ int pick_warp(SmemMisc* ms, ProdState& S, int32_t* status) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-#pragma unroll
-    for (int i = 0; i < kConsumerWarps; ++i) {
-      const int w = (S.rr + i) & (kConsumerWarps - 1);
-      if (mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u)) {
-        S.rr = (w + 1) & (kConsumerWarps - 1);
-        return w;
-      }
+  int w = S.rr;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u)) break;
+    w = (w + 1) & (kConsumerWarps - 1);
+    if (it >= kWaitLimit) {
+      set_device_error(status, DEV_WAIT_TIMEOUT, 6);
+      S.ok = 0;
+      return 0;
     }
-    if (it > 16) __nanosleep(32);
+    if (it > 64) __nanosleep(32);
   }
-  set_device_error(status, DEV_WAIT_TIMEOUT, 6);
-  S.ok = 0;
-  return 0;
+  S.rr = (w + 1) & (kConsumerWarps - 1);
+  return w;
 }
 
-// Wait for warp w's next slot, publish the descriptor (and the record table
-// of a multi-record page), and only then arm the full barrier, so that the
-// consumer's acquire on the barrier covers both.  Returns the slot or -1.
-__device__ __forceinline__ int push_page(SmemMisc* ms, ProdState& S, int w, const PageDesc& d,
-                                         uint32_t bytes, int32_t* status, int ntab = 0) {
-  const int slot = ring_slot(S, w);
-  if (!mbar_wait(&ms->empty[slot], ring_phase(S, w) ^ 1u, kWaitLimit)) {
+// Bounded wait for warp w's next slot (pages that must go to that warp).
+__device__ __forceinline__ bool wait_warp(SmemMisc* ms, ProdState& S, int w, int32_t* status) {
+  if (!mbar_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u, kWaitLimit)) {
     set_device_error(status, DEV_WAIT_TIMEOUT, 1);
     S.ok = 0;
-    return -1;
+    return false;
   }
+  return true;
+}
+
+// Warp w's next slot, known free: publish the descriptor (and the record
+// table of a multi-record page), then arm the full barrier, so that the
+// consumer's acquire on the barrier covers both.
+__device__ __forceinline__ int arm_page(SmemMisc* ms, const ProdState& S, int w,
+                                        const PageDesc& d, uint32_t bytes, int ntab = 0) {
+  const int slot = ring_slot(S, w);
   ms->desc[slot] = d;
   for (int i = 0; i < ntab; ++i) ms->rec[slot][i] = ms->btab[i];
   mbar_arrive_expect_tx(&ms->full[slot], bytes);
@@ -70,7 +74,7 @@ __device__ __forceinline__ void commit_page(ProdState& S, int w, int slot) {
 }
 
 // The n small records staged in ms->bsrc / ms->btab (bytes in all) as one page.
-__device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
+static __device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
                                               const DecodeParams& P, int n, int bytes) {
   if (n == 0 || !S.ok) return S;
   const uint64_t pol = policy_evict_first();
@@ -79,8 +83,7 @@ __device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdS
   PageDesc d{};
   d.type = PG_EXPM;
   d.n = n;
-  const int slot = push_page(ms, S, w, d, uint32_t(bytes), P.status, n);
-  if (slot < 0) return S;
+  const int slot = arm_page(ms, S, w, d, uint32_t(bytes), n);
   uint8_t* pg = slot_ptr(smem, slot);
   for (int i = 0; i < n; ++i) {
     const RecInfo ri = ms->btab[i];
@@ -93,7 +96,7 @@ __device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdS
 
 // A record larger than a page: its key part, its U rows in tiles, its value
 // part, all to one warp (the partial state of the span stays in its registers).
-__device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdState S,
+static __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdState S,
                                               const DecodeParams& P, int b, int rank,
                                               long long off) {
   const uint64_t pol = policy_evict_first();
@@ -107,8 +110,7 @@ __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdS
   d.rk = rK;
   d.rv = rV;
   d.n = 0; d.a = 0; d.off_a = 0; d.off_uk = 0; d.off_uv = 0; d.off_b = -1;
-  int slot = push_page(ms, S, w, d, uint32_t(L.uk), P.status);
-  if (slot < 0) return S;
+  int slot = arm_page(ms, S, w, d, uint32_t(L.uk));
   bulk_g2s_hint(slot_ptr(smem, slot), rec, uint32_t(L.uk), &ms->full[slot], pol);
   commit_page(S, w, slot);
   const int row_bytes = 2 * (r8(rK) + r8(rV));
@@ -118,8 +120,8 @@ __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdS
     const int n = (b - i0) < rows ? (b - i0) : rows;
     const uint32_t bk = uint32_t(2 * n * r8(rK)), bv = uint32_t(2 * n * r8(rV));
     d.n = n; d.a = i0; d.off_a = -1; d.off_uk = 0; d.off_uv = int(bk); d.off_b = -1;
-    slot = push_page(ms, S, w, d, bk + bv, P.status);
-    if (slot < 0) return S;
+    if (!wait_warp(ms, S, w, P.status)) return S;
+    slot = arm_page(ms, S, w, d, bk + bv);
     uint8_t* pg = slot_ptr(smem, slot);
     if (bk) bulk_g2s_hint(pg, rec + L.uk + 2 * int64_t(i0) * r8(rK), bk, &ms->full[slot], pol);
     if (bv)
@@ -128,8 +130,8 @@ __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdS
   }
   const uint32_t vb = uint32_t(L.total - L.vpart);
   d.n = 0; d.a = 0; d.off_a = -1; d.off_b = 0;
-  slot = push_page(ms, S, w, d, vb, P.status);
-  if (slot < 0) return S;
+  if (!wait_warp(ms, S, w, P.status)) return S;
+  slot = arm_page(ms, S, w, d, vb);
   if (vb) bulk_g2s_hint(slot_ptr(smem, slot), rec + L.vpart, vb, &ms->full[slot], pol);
   commit_page(S, w, slot);
   return S;
@@ -137,7 +139,7 @@ __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdS
 
 // Fixed page t of this CTA: full-resolution rows first, then summary rows,
 // 32 per page, to the first warp with a free slot.
-__device__ __noinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, ProdState S,
+__device__ __forceinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, ProdState S,
                                               const DecodeParams& P, int t, int nfp, int f0,
                                               int f1, int k0, int k1, int g) {
   const int w = pick_warp(ms, S, P.status);
@@ -149,8 +151,7 @@ __device__ __noinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, ProdS
   d.type = full ? PG_FULL : PG_SUM;
   d.n = (e - a) < kTileRows ? (e - a) : kTileRows;
   d.a = a;
-  const int slot = push_page(ms, S, w, d, 4 * kBoxBytes, P.status);
-  if (slot < 0) return S;
+  const int slot = arm_page(ms, S, w, d, 4 * kBoxBytes);
   uint8_t* pg = slot_ptr(smem, slot);
   const CUtensorMap* tk = full ? &P.tm_kfull : &P.tm_ksum;
   const CUtensorMap* tv = full ? &P.tm_vfull : &P.tm_vsum;
@@ -174,7 +175,7 @@ __device__ __forceinline__ long long warp_incl_scan(long long v) {
   return v;
 }
 
-__device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P, int g, int j,
+static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P, int g, int j,
                               int b, int c) {
   const int lane = threadIdx.x & 31;
   const int n_sp = P.n_spans[b];
@@ -209,8 +210,7 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
         d.type = PG_ROUTE; d.n = n; d.a = k; d.flag = p;
         const int w = pick_warp(ms, S, P.status);
         if (!S.ok) break;
-        const int slot = push_page(ms, S, w, d, 2 * 8192 + n4 * 8 + n2 * 8, P.status);
-        if (slot < 0) break;
+        const int slot = arm_page(ms, S, w, d, 2 * 8192 + n4 * 8 + n2 * 8);
         uint8_t* pg = slot_ptr(smem, slot);
         tma_g2s_3d_hint(pg, &P.tm_sroute, 0, k, g, &ms->full[slot], pol);
         tma_g2s_3d_hint(pg + 8192, &P.tm_sroute, 32, k, g, &ms->full[slot], pol);
@@ -224,8 +224,8 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
       const int n = k1 - k0;
       const uint32_t bytes = uint32_t(pad16(2 * int64_t(n)));
       d.type = PG_INFO; d.n = n; d.a = k0;
-      const int slot = push_page(ms, S, 0, d, bytes, P.status);
-      if (slot >= 0) {
+      if (wait_warp(ms, S, 0, P.status)) {
+        const int slot = arm_page(ms, S, 0, d, bytes);
         bulk_g2s(slot_ptr(smem, slot), P.info + gs + k0, bytes, &ms->full[slot]);
         commit_page(S, 0, slot);
       }
@@ -234,8 +234,7 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
     for (int w = 0; S.ok && w < kConsumerWarps; ++w) {
       d = PageDesc{};
       d.type = PG_SYNC;
-      const int slot = push_page(ms, S, w, d, 0, P.status);
-      if (slot >= 0) commit_page(S, w, slot);
+      if (wait_warp(ms, S, w, P.status)) commit_page(S, w, arm_page(ms, S, w, d, 0));
     }
   }
 
@@ -298,7 +297,7 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
       __syncwarp();
     }
     const long long Tb = ms->pre_b[cg];
-    const long long lo = Tb * j / cg, hi = Tb * (j + 1) / cg;
+    const long long lo = byte_split(Tb, j, cg), hi = byte_split(Tb, j + 1, cg);
     // lanes hold candidate entries in byte order; lane 0 takes those that
     // start in [lo, hi): into the current batch, or as a split record
     auto offer = [&](bool mine, const ExpEntry& en) {
@@ -312,7 +311,9 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
         if (lane == 0) {
           const int xr = rank & 0xFFFF, xv = (rank >> 16) & 0xFFFF;
           const int sz = int(record_bytes(body, xr, xv));
-          if (sz > kPageData) {
+          if (xr > P.rank_lim || xv > P.rank_lim) {
+            set_device_error(P.status, DEV_BAD_RANK, xr > xv ? xr : xv);  // record skipped
+          } else if (sz > kPageData) {
             S = issue_split(smem, ms, S, P, body, rank, off);
           } else {
             if (bn == kMaxRecPerPage || bbytes + sz > kPageData) {
@@ -408,8 +409,7 @@ __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodeParams& P
       d.type = PG_END;
       ProdState S2 = S;
       S2.ok = 1;
-      const int slot = push_page(ms, S2, w, d, 0, P.status);
-      if (slot >= 0) commit_page(S2, w, slot);
+      if (wait_warp(ms, S2, w, P.status)) commit_page(S2, w, arm_page(ms, S2, w, d, 0));
       S.rs = S2.rs;
       S.filled = S2.filled;
       S.last_par = S2.last_par;

@@ -24,6 +24,12 @@ bool config_ok(const sekv_config* cfg, sekv_status* why) {
     *why = SEKV_ERR_INVALID;
     return false;
   }
+  // the kernels split rows and spans among CTAs in 32-bit arithmetic
+  if ((2 * int64_t(cfg->n_sink + cfg->n_recent) + 5 * int64_t(cfg->max_spans)) * 256 >=
+      (int64_t(1) << 31)) {
+    *why = SEKV_ERR_UNSUPPORTED;
+    return false;
+  }
   if (cfg->n_q_heads / cfg->n_kv_heads > SEKV_MAX_GROUP || cfg->rank_cap > SEKV_MAX_RANK) {
     *why = SEKV_ERR_UNSUPPORTED;
     return false;
@@ -57,8 +63,7 @@ int decode_cg(const sekv_config* cfg, int sms) {
   int cg = sms / ng;
   if (cg < 1) cg = 1;
   // every CTA's span slice must fit the shared-memory span-info cache
-  const int64_t units = 2 * int64_t(cfg->n_sink + cfg->n_recent) + 4 * int64_t(cfg->max_spans);
-  while (cg < kMaxCgSmem && units / (2 * int64_t(cg)) + 16 > kInfoCap) ++cg;
+  while (cg < kMaxCgSmem && cfg->max_spans / cg + 16 > kInfoCap) ++cg;
   return cg > kMaxCgSmem ? kMaxCgSmem : cg;
 }
 
@@ -252,15 +257,27 @@ sekv_status encode_wr(DecodeParams& P, const float* W_r, const sekv_config* cfg)
              : SEKV_ERR_CUDA;
 }
 
-sekv_status launch_decode(const DecodeParams& P, const WsLayout& L, const sekv_config* cfg,
+// Rank k-steps of 16 the kernel instance needs for this configuration.
+int decode_ks(const sekv_config* cfg) {
+  const int ks = (cfg->rank_cap + 15) / 16;
+  return ks < 1 ? 1 : (ks > 4 ? 4 : ks);
+}
+
+sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_config* cfg,
                           cudaStream_t stream, bool overlap) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmemAlloc);
+  static const void* const fns[4] = {decode_kernel_fn_ks1(), decode_kernel_fn_ks2(),
+                                     decode_kernel_fn_ks3(), decode_kernel_fn_ks4()};
+  static std::once_flag once[4];
+  static cudaError_t attr_err[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
+  const int ks = decode_ks(cfg);
+  const void* fn = fns[ks - 1];
+  std::call_once(once[ks - 1], [&] {
+    attr_err[ks - 1] =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   });
-  if (attr_err != cudaSuccess) return SEKV_ERR_CUDA;
+  if (attr_err[ks - 1] != cudaSuccess) return SEKV_ERR_CUDA;
+  DecodeParams P = P0;
+  P.rank_lim = 16 * ks;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(L.cg, cfg->n_kv_heads, cfg->batch);
   lc.blockDim = dim3(kThreads);
@@ -271,7 +288,8 @@ sekv_status launch_decode(const DecodeParams& P, const WsLayout& L, const sekv_c
   at[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = overlap ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, decode_kernel, P) != cudaSuccess) return SEKV_ERR_CUDA;
+  void* args[] = {&P};
+  if (cudaLaunchKernelExC(&lc, fn, args) != cudaSuccess) return SEKV_ERR_CUDA;
   count_launch(1);
   return SEKV_OK;
 }
