@@ -53,6 +53,8 @@ constexpr int kOffInfo = kOffScratch + 6144;                    // summary bias 
 constexpr int kOffMisc = kOffInfo + kInfoCap * 4;
 constexpr int kMiscBytes = 6144;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes;
+constexpr int kCombineChunk = 32;                       // partials per bulk copy (133 KB)
+constexpr int kCombineLOff = kOffWr - kMaxCgSmem * 8 * 4;  // [cg][8] floats below W_r
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
 enum PageType : int {
@@ -168,6 +170,7 @@ struct SmemMisc {
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
   uint64_t wr_bar;   // W_r boxes landed (fused mode)
+  uint64_t cmb_bar;  // last CTA of a KV head: a chunk of partials landed
   unsigned long long rmask[kMaxRoutePages];  // expanded spans per routing page (bit i: span a+i)
   long long rbytes[kMaxRoutePages];          // their record bytes
   int is_last;

@@ -108,7 +108,6 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
   const size_t gs = size_t(g) * P.max_spans;
   float* infoc = reinterpret_cast<float*>(smem + kOffInfo);  // summary bias per span
-  float* qs = reinterpret_cast<float*>(smem + kOffScratch);         // prologue only
   float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages
 
   pdl_wait();
@@ -137,30 +136,40 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   X.had = false;
 
   if (P.fused) {
-    for (int i = tid; i < 8 * kHeadDim; i += kConsumers)
-      qs[i] = (i / kHeadDim) < G ? __bfloat162float(qg[i]) : 0.f;
     if (tid < 8) ms->theta[tid] = tid < G ? P.theta[c * G + tid] : 0.f;
-    named_bar(1, kConsumers);
-    // y_h = W_r[c] q_h from the swizzled W_r boxes (box x: dims 32x..32x+31,
-    // 64 rows of 128 B), one routing coordinate per thread, heads hh, hh+2, ...
     if (!mbar_wait(&ms->wr_bar, 0, kWaitLimit) && tid == 0)
       set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
-    const int jr = tid & 63, hh = tid >> 6;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int d4 = 0; d4 < 32; ++d4) {
-      const float4 wv = *reinterpret_cast<const float4*>(
-          smem + kOffWr + (d4 >> 3) * 8192 + jr * 128 + (((d4 & 7) ^ (jr & 7)) << 4));
+    // y_h = W_r[c] q_h on the tensor cores: heads are the M rows, warp w takes
+    // routing coordinates 16w .. 16w+15 (two n-tiles); W_r (fp32, in four
+    // 128B-swizzled boxes of 64 rows x 32 floats) is split into bf16 hi + lo
+    const int gid = lane >> 2, tig = lane & 3;
+    float yh[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, yl[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (hh + 2 * i < G) {
-          const float4 qv = reinterpret_cast<const float4*>(qs + (hh + 2 * i) * kHeadDim)[d4];
-          acc[i] = fmaf(wv.x, qv.x, fmaf(wv.y, qv.y, fmaf(wv.z, qv.z, fmaf(wv.w, qv.w, acc[i]))));
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a0 = (ks & 1) ? qf[ks >> 1].z : qf[ks >> 1].x;
+      const uint32_t a2 = (ks & 1) ? qf[ks >> 1].w : qf[ks >> 1].y;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int r = 16 * w + 8 * nt + gid;
+        uint32_t bh[2], bl[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int d = 16 * ks + 8 * hf + 2 * tig;
+          const float2 v = *reinterpret_cast<const float2*>(
+              smem + kOffWr + (d >> 5) * 8192 + r * 128 + ((((d & 31) >> 2) ^ (r & 7)) << 4) +
+              (d & 3) * 4);
+          split_bf16(v.x, v.y, bh[hf], bl[hf]);
         }
+        mma_bf16_rows8(yh[nt][0], yh[nt][1], a0, a2, bh[0], bh[1]);
+        mma_bf16_rows8(yl[nt][0], yl[nt][1], a0, a2, bl[0], bl[1]);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ys[(hh + 2 * i) * kRouteDim + jr] = acc[i];
+    for (int nt = 0; nt < 2; ++nt) {
+      const int r = 16 * w + 8 * nt + 2 * tig;
+      ys[gid * kRouteDim + r] = yh[nt][0] + yl[nt][0];
+      ys[gid * kRouteDim + r + 1] = yh[nt][1] + yl[nt][1];
+    }
     named_bar(1, kConsumers);
   }
 
@@ -281,25 +290,27 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   if (!ms->is_last) return;
 
   // ---- last CTA of this KV head: merge the partials, write the output -----
+  // (the partials arrive by bulk copy, chunks of kCombineChunk CTAs, so the
+  // merge costs one global round trip per chunk)
   __threadfence();
   const int cg = P.cg;
   const Partial* parts = P.partials + size_t(g) * cg;
-  float* sm_m = reinterpret_cast<float*>(smem + 32768);   // [cg][8]
-  float* sm_s = sm_m + kMaxCgSmem * 8;                    // [cg][8] scales
-  float* sm_l = sm_s + kMaxCgSmem * 8;                    // [cg][8]
-  float* sm_ML = sm_l + kMaxCgSmem * 8;                   // M[8], L[8]
+  float* sm_s = reinterpret_cast<float*>(smem + kOffInfo);          // [cg][8] m, then scales
+  float* sm_l = reinterpret_cast<float*>(smem + kCombineLOff);      // [cg][8]
+  float* sm_ML = reinterpret_cast<float*>(smem + kOffScratch);      // M[8], L[8]
+  const Partial* cbuf = reinterpret_cast<const Partial*>(smem);     // chunk of partials
   for (int i = tid; i < cg * 8; i += kConsumers) {
     const int jj = i >> 3, h = i & 7;
-    sm_m[i] = h < G ? __ldcg(&parts[jj].m[h]) : kNegInf;
+    sm_s[i] = h < G ? __ldcg(&parts[jj].m[h]) : kNegInf;
     sm_l[i] = h < G ? __ldcg(&parts[jj].l[h]) : 0.f;
   }
   named_bar(1, kConsumers);
   if (tid < G) {
     float M = kNegInf;
-    for (int jj = 0; jj < cg; ++jj) M = fmaxf(M, sm_m[jj * 8 + tid]);
+    for (int jj = 0; jj < cg; ++jj) M = fmaxf(M, sm_s[jj * 8 + tid]);
     float L = 0.f;
     if (M != kNegInf)
-      for (int jj = 0; jj < cg; ++jj) L = fmaf(sm_l[jj * 8 + tid], exp2f(sm_m[jj * 8 + tid] - M), L);
+      for (int jj = 0; jj < cg; ++jj) L = fmaf(sm_l[jj * 8 + tid], exp2f(sm_s[jj * 8 + tid] - M), L);
     sm_ML[tid] = M;
     sm_ML[8 + tid] = L;
   }
@@ -307,31 +318,43 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   for (int i = tid; i < cg * 8; i += kConsumers) {
     const int h = i & 7;
     const float M = h < G ? sm_ML[h] : kNegInf;
-    sm_s[i] = (M == kNegInf) ? 0.f : exp2f(sm_m[i] - M);
+    sm_s[i] = (M == kNegInf) ? 0.f : exp2f(sm_s[i] - M);
+  }
+  float Oh[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) Oh[h] = 0.f;
+  for (int c0 = 0, ph = 0; c0 < cg; c0 += kCombineChunk, ph ^= 1) {
+    const int nc = (cg - c0) < kCombineChunk ? (cg - c0) : kCombineChunk;
+    named_bar(1, kConsumers);  // the previous chunk is consumed, the scales are written
+    if (tid == 0) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&ms->cmb_bar, uint32_t(nc * sizeof(Partial)));
+      bulk_g2s(smem, parts + c0, uint32_t(nc * sizeof(Partial)), &ms->cmb_bar);
+    }
+    // every thread takes every barrier of this loop, even after a timeout
+    const bool landed = mbar_wait(&ms->cmb_bar, uint32_t(ph), kWaitLimit);
+    if (!landed && tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 7);
+    for (int jj = 0; landed && jj < nc; ++jj) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < G) Oh[h] = fmaf(cbuf[jj].o[h][tid], sm_s[(c0 + jj) * 8 + h], Oh[h]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if (h < G) {
+      const float L = sm_ML[8 + h];
+      const size_t row = size_t(b) * P.Hq + size_t(c) * G + h;
+      P.out[row * kHeadDim + tid] = L > 0.f ? Oh[h] / L : 0.f;
+      if (tid == 0 && P.lse != nullptr)
+        P.lse[row] = L > 0.f ? (sm_ML[h] + log2f(L)) * kLn2 : kNegInf;
+    }
   }
   named_bar(1, kConsumers);
-  for (int h = 0; h < G; ++h) {
-    float Oa[4] = {0.f, 0.f, 0.f, 0.f};
-    int jj = 0;
-    for (; jj + 4 <= cg; jj += 4) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcg(&parts[jj + u].o[h][tid]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) Oa[u] = fmaf(v[u], sm_s[(jj + u) * 8 + h], Oa[u]);
-    }
-    for (; jj < cg; ++jj) Oa[0] = fmaf(__ldcg(&parts[jj].o[h][tid]), sm_s[jj * 8 + h], Oa[0]);
-    const float O = (Oa[0] + Oa[1]) + (Oa[2] + Oa[3]);
-    const float L = sm_ML[8 + h];
-    const size_t row = size_t(b) * P.Hq + size_t(c) * G + h;
-    P.out[row * kHeadDim + tid] = L > 0.f ? O / L : 0.f;
-    if (tid == 0 && P.lse != nullptr)
-      P.lse[row] = L > 0.f ? (sm_ML[h] + log2f(L)) * kLn2 : kNegInf;
-  }
   if (P.expanded_out != nullptr && P.fused) {
     // the CTAs' routing pages in order; page p of CTA jj covers spans
     // sk0 + 64p + (0..63), bit i of its mask marks span sk0 + 64p + i
-    int* pre = reinterpret_cast<int*>(sm_ML + 16);  // [kMaxRoutePages + 1]
+    int* pre = reinterpret_cast<int*>(sm_ML + 16);  // [kMaxRoutePages + 1] (scratch: 6 KB)
     int base = 0;
     for (int jj = 0; jj < cg; ++jj) {
       int a0, a1, sk0, sk1;
@@ -381,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms->empty[s], 1);  // each slot belongs to one consumer warp
     }
     mbar_init(&ms->wr_bar, 1);
+    mbar_init(&ms->cmb_bar, 1);
     ms->is_last = 0;
     fence_mbar_init();
   }

@@ -118,6 +118,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Orders this thread's view of global memory (including other CTAs' writes
+// it has acquired) before its later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // L2 policy for data read exactly once: evicted first, so that it does not
 // push out what is reused (code, routing weights, counters).
 __device__ __forceinline__ uint64_t policy_evict_first() {
