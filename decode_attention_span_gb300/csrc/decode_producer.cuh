@@ -25,14 +25,24 @@ __device__ __forceinline__ uint32_t ring_phase(const ProdState& S, int w) {
   return (S.rs >> (2 * w + 1)) & 1u;
 }
 
-// First warp (from S.rr on) whose next slot is free; bounded.
-__device__ __forceinline__ int pick_warp(SmemMisc* ms, ProdState& S, int32_t* status) {
+__device__ __forceinline__ bool slot_free(SmemMisc* ms, const ProdState& S, int w) {
+  return mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u);
+}
+
+__device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
+                                                     ProdState S, const DecodeParams& P);
+
+// First warp (from S.rr on, never the one holding a split record) whose next
+// slot is free; bounded.  While it polls it keeps the split record moving.
+__device__ __forceinline__ int pick_warp(uint8_t* smem, SmemMisc* ms, ProdState& S,
+                                         const DecodeParams& P) {
   int w = S.rr;
   for (uint32_t it = 0;; ++it) {
-    if (mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u)) break;
+    if (ms->sp_w >= 0 && slot_free(ms, S, ms->sp_w)) S = push_split_part(smem, ms, S, P);
+    if (w != ms->sp_w && slot_free(ms, S, w)) break;
     w = (w + 1) & (kConsumerWarps - 1);
-    if (it >= kWaitLimit) {
-      set_device_error(status, DEV_WAIT_TIMEOUT, 6);
+    if (it >= kWaitLimit || !S.ok) {
+      set_device_error(P.status, DEV_WAIT_TIMEOUT, 6);
       S.ok = 0;
       return 0;
     }
@@ -74,11 +84,11 @@ __device__ __forceinline__ void commit_page(ProdState& S, int w, int slot) {
 }
 
 // The n small records staged in ms->bsrc / ms->btab (bytes in all) as one page.
-static __device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
+__device__ __forceinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
                                               const DecodeParams& P, int n, int bytes) {
   if (n == 0 || !S.ok) return S;
   const uint64_t pol = policy_evict_first();
-  const int w = pick_warp(ms, S, P.status);
+  const int w = pick_warp(smem, ms, S, P);
   if (!S.ok) return S;
   PageDesc d{};
   d.type = PG_EXPM;
@@ -94,47 +104,86 @@ static __device__ __noinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms
   return S;
 }
 
-// A record larger than a page: its key part, its U rows in tiles, its value
-// part, all to one warp (the partial state of the span stays in its registers).
-static __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms, ProdState S,
-                                              const DecodeParams& P, int b, int rank,
-                                              long long off) {
+// A record larger than a page goes to one warp as several pages (its key
+// part, its U rows in tiles, its value part; the partial state of the span
+// stays in that warp's registers).  The parts are pushed one at a time as
+// that warp frees slots, so the other warps are never held up behind it.
+__device__ __forceinline__ int split_rows(int rK, int rV) {
+  const int row_bytes = 2 * (r8(rK) + r8(rV));
+  int rows = row_bytes > 0 ? (kPageData / row_bytes) & ~15 : 512;
+  return rows > 512 ? 512 : rows;
+}
+
+// Part ms->sp_part of the split record to warp ms->sp_w, whose next slot is free.
+__device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
+                                                         ProdState S, const DecodeParams& P) {
   const uint64_t pol = policy_evict_first();
-  const int w = pick_warp(ms, S, P.status);
-  if (!S.ok) return S;
-  const int rK = rank & 0xFFFF, rV = (rank >> 16) & 0xFFFF;
-  const uint8_t* rec = P.store + off;
+  const int w = ms->sp_w, part = ms->sp_part, b = ms->sp_b;
+  const int rK = ms->sp_rank & 0xFFFF, rV = (ms->sp_rank >> 16) & 0xFFFF;
+  const uint8_t* rec = P.store + ms->sp_off;
   const RecordLayout L = record_layout(b, rK, rV);
+  const int rows = split_rows(rK, rV);
   PageDesc d{};
   d.type = PG_EXP;
   d.rk = rK;
   d.rv = rV;
-  d.n = 0; d.a = 0; d.off_a = 0; d.off_uk = 0; d.off_uv = 0; d.off_b = -1;
-  int slot = arm_page(ms, S, w, d, uint32_t(L.uk));
-  bulk_g2s_hint(slot_ptr(smem, slot), rec, uint32_t(L.uk), &ms->full[slot], pol);
-  commit_page(S, w, slot);
-  const int row_bytes = 2 * (r8(rK) + r8(rV));
-  int rows = row_bytes > 0 ? (kPageData / row_bytes) & ~15 : 512;
-  if (rows > 512) rows = 512;
-  for (int i0 = 0; i0 < b; i0 += rows) {
-    const int n = (b - i0) < rows ? (b - i0) : rows;
-    const uint32_t bk = uint32_t(2 * n * r8(rK)), bv = uint32_t(2 * n * r8(rV));
-    d.n = n; d.a = i0; d.off_a = -1; d.off_uk = 0; d.off_uv = int(bk); d.off_b = -1;
-    if (!wait_warp(ms, S, w, P.status)) return S;
-    slot = arm_page(ms, S, w, d, bk + bv);
-    uint8_t* pg = slot_ptr(smem, slot);
-    if (bk) bulk_g2s_hint(pg, rec + L.uk + 2 * int64_t(i0) * r8(rK), bk, &ms->full[slot], pol);
-    if (bv)
-      bulk_g2s_hint(pg + bk, rec + L.uv + 2 * int64_t(i0) * r8(rV), bv, &ms->full[slot], pol);
-    commit_page(S, w, slot);
+  d.off_a = -1;
+  d.off_b = -1;
+  uint32_t bytes;
+  if (part == 0) {  // header, sigma_K, g_K, Vt_K
+    d.off_a = 0;
+    bytes = uint32_t(L.uk);
+  } else if (part < ms->sp_nparts - 1) {  // U_K and U_V rows of one tile
+    const int i0 = (part - 1) * rows;
+    d.n = (b - i0) < rows ? (b - i0) : rows;
+    d.a = i0;
+    d.off_uv = 2 * d.n * r8(rK);
+    bytes = uint32_t(d.off_uv + 2 * d.n * r8(rV));
+  } else {  // sigma_V, g_V, Vt_V
+    d.off_b = 0;
+    bytes = uint32_t(L.total - L.vpart);
   }
-  const uint32_t vb = uint32_t(L.total - L.vpart);
-  d.n = 0; d.a = 0; d.off_a = -1; d.off_b = 0;
-  if (!wait_warp(ms, S, w, P.status)) return S;
-  slot = arm_page(ms, S, w, d, vb);
-  if (vb) bulk_g2s_hint(slot_ptr(smem, slot), rec + L.vpart, vb, &ms->full[slot], pol);
+  const int slot = arm_page(ms, S, w, d, bytes);
+  uint8_t* pg = slot_ptr(smem, slot);
+  if (part == 0) {
+    bulk_g2s_hint(pg, rec, bytes, &ms->full[slot], pol);
+  } else if (part < ms->sp_nparts - 1) {
+    const uint32_t bk = uint32_t(d.off_uv), bv = bytes - bk;
+    if (bk) bulk_g2s_hint(pg, rec + L.uk + 2 * int64_t(d.a) * r8(rK), bk, &ms->full[slot], pol);
+    if (bv) bulk_g2s_hint(pg + bk, rec + L.uv + 2 * int64_t(d.a) * r8(rV), bv, &ms->full[slot], pol);
+  } else if (bytes) {
+    bulk_g2s_hint(pg, rec + L.vpart, bytes, &ms->full[slot], pol);
+  }
   commit_page(S, w, slot);
+  if (++ms->sp_part == ms->sp_nparts) ms->sp_w = -1;
   return S;
+}
+
+// Push every remaining part of the split record (waits on its warp).
+__device__ __forceinline__ ProdState finish_split(uint8_t* smem, SmemMisc* ms, ProdState S,
+                                                  const DecodeParams& P) {
+  while (ms->sp_w >= 0 && S.ok)
+    if (wait_warp(ms, S, ms->sp_w, P.status)) S = push_split_part(smem, ms, S, P);
+  return S;
+}
+
+// Start a split record on a free warp (the previous split, if any, first).
+__device__ __forceinline__ ProdState start_split(uint8_t* smem, SmemMisc* ms, ProdState S,
+                                                     const DecodeParams& P, int b, int rank,
+                                                     long long off) {
+  S = finish_split(smem, ms, S, P);
+  if (!S.ok) return S;
+  const int w = pick_warp(smem, ms, S, P);
+  if (!S.ok) return S;
+  const int rK = rank & 0xFFFF, rV = (rank >> 16) & 0xFFFF;
+  const int rows = split_rows(rK, rV);
+  ms->sp_part = 0;
+  ms->sp_nparts = 2 + (b + rows - 1) / rows;
+  ms->sp_b = b;
+  ms->sp_rank = rank;
+  ms->sp_off = off;
+  ms->sp_w = w;
+  return push_split_part(smem, ms, S, P);
 }
 
 // Fixed page t of this CTA: full-resolution rows first, then summary rows,
@@ -142,7 +191,7 @@ static __device__ __noinline__ ProdState issue_split(uint8_t* smem, SmemMisc* ms
 __device__ __forceinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, ProdState S,
                                               const DecodeParams& P, int t, int nfp, int f0,
                                               int f1, int k0, int k1, int g) {
-  const int w = pick_warp(ms, S, P.status);
+  const int w = pick_warp(smem, ms, S, P);
   if (!S.ok) return S;
   PageDesc d{};
   const bool full = t < nfp;
@@ -208,7 +257,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
         const int n = (k1 - k) < kRouteSpans ? (k1 - k) : kRouteSpans;
         const uint32_t n4 = uint32_t((n + 3) & ~3), n2 = uint32_t((n + 1) & ~1);
         d.type = PG_ROUTE; d.n = n; d.a = k; d.flag = p;
-        const int w = pick_warp(ms, S, P.status);
+        const int w = pick_warp(smem, ms, S, P);
         if (!S.ok) break;
         const int slot = arm_page(ms, S, w, d, 2 * 8192 + n4 * 8 + n2 * 8);
         uint8_t* pg = slot_ptr(smem, slot);
@@ -314,7 +363,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
           if (xr > P.rank_lim || xv > P.rank_lim) {
             set_device_error(P.status, DEV_BAD_RANK, xr > xv ? xr : xv);  // record skipped
           } else if (sz > kPageData) {
-            S = issue_split(smem, ms, S, P, body, rank, off);
+            S = start_split(smem, ms, S, P, body, rank, off);
           } else {
             if (bn == kMaxRecPerPage || bbytes + sz > kPageData) {
               S = flush_batch(smem, ms, S, P, bn, bbytes);
@@ -325,6 +374,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
             ms->btab[bn] = RecInfo{bbytes, body, xr, xv};
             bbytes += sz;
             ++bn;
+
           }
         }
         S.ok = __shfl_sync(0xffffffffu, S.ok, 0);
@@ -403,6 +453,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
       S = issue_fixed(smem, ms, S, P, t_fixed, nfp, f0, f1, k0, k1, g);
       ++t_fixed;
     }
+    S = finish_split(smem, ms, S, P);
     // every consumer warp ends with an END page
     for (int w = 0; w < kConsumerWarps; ++w) {
       PageDesc d{};
