@@ -65,6 +65,12 @@ def dist_setup(args):
     return ws, rank, local
 
 
+def whole_job_rate(steps: int, ms_max: float, world: int) -> float:
+    """Steps/s of the whole job: every rank runs `steps` steps of its own
+    replica; the slowest rank's time counts."""
+    return steps * world / (ms_max / 1000.0)
+
+
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -463,7 +469,7 @@ def main():
     ms_total, ck = run_resident(sk, cfg, ws, layers, args.steps, args.warmup, ws_n, clocks)
     ms_total = max_over_ranks(ms_total, ws_n)
     ms_step = ms_total / args.steps
-    value = ws_n * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(args.steps, ms_total, ws_n)
     bytes_step = sum(L["bytes"] for L in layers)
     per_launch = bytes_step / len(layers)
     launch_s = ms_total / 1e3 / (args.steps * len(layers))

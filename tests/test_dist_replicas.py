@@ -1,0 +1,63 @@
+"""Multi-process (gloo, world size 2) checks of the replica logic of bench.py:
+the path has no exchange step, so N GPUs run N replicas, the timed region is
+bracketed by a barrier on every rank and the slowest rank's time counts."""
+
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+
+    class A:
+        pass
+
+    ws, r, local = bench.dist_setup(A())
+    assert (ws, r, local) == (world, rank, rank)
+    bench.barrier(ws)
+    # each rank "measured" a different time; every rank must see the maximum
+    ms = 10.0 + 5.0 * rank
+    mx = bench.max_over_ranks(ms, ws)
+    out[rank] = mx
+    bench.barrier(ws)
+    dist.destroy_process_group()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="gloo replica test runs on CPU hosts")
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == 15.0
+
+
+def test_whole_job_rate_counts_every_replica():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # 2 ranks x 100 steps in 50 ms (slowest rank) -> 4000 steps/s for the job
+    assert bench.whole_job_rate(100, 50.0, 2) == pytest.approx(4000.0)
+    assert bench.whole_job_rate(100, 50.0, 1) == pytest.approx(2000.0)
