@@ -194,8 +194,9 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
     const uint8_t* page = slot_ptr(smem, slot);
     const uint32_t pu = smem_u32(page);
     if (!routed && (d.type == PG_SYNC || d.type == PG_END)) {
-      // all routing pages of the CTA are done past this barrier
-      if (P.fused) __threadfence();
+      // all routing pages of the CTA are done past this barrier; warp 0's
+      // gpu-scope fence after it (in publish_routes) is cumulative, so it
+      // also orders the other warps' entry writes before the publication
       named_bar(2, kConsumers);
       routed = true;
       if (P.fused && w == 0 && d.type == PG_SYNC) publish_routes(P, ms, g, j, np);
