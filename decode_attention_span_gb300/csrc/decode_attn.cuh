@@ -174,6 +174,7 @@ struct SmemMisc {
   unsigned long long rmask[kMaxRoutePages];  // expanded spans per routing page (bit i: span a+i)
   long long rbytes[kMaxRoutePages];          // their record bytes
   int is_last;
+  uint32_t warm[kConsumerWarps];  // sink of the instruction-cache warm-up pass
   float theta[8];
   int pre_n[kMaxCgSmem + 1];                 // expanded spans before CTA jj (exclusive prefix)
   long long pre_b[kMaxCgSmem + 1];           // their record bytes

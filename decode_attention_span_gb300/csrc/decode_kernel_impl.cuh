@@ -110,6 +110,13 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   float* infoc = reinterpret_cast<float*>(smem + kOffInfo);  // summary bias per span
   float* ys = reinterpret_cast<float*>(smem + kOffScratch + 4096);  // routing pages
 
+  if (P.fused) {
+    // Run the routing routine once on whatever the W_r area holds (the
+    // result is discarded): its code is fetched into the instruction cache
+    // while the routing weights and the first routing pages are in flight.
+    const unsigned long long warm = route_hits(smem + kOffWr, ys, ms->theta, G);
+    if (lane == 0) ms->warm[w] = uint32_t(warm);
+  }
   pdl_wait();
   WarpAcc A;
   const __nv_bfloat16* qg = P.q + (size_t(b) * P.Hq + size_t(c) * G) * kHeadDim;
