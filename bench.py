@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--path", default="decode", choices=["decode", "build"],
+                    help="decode: the headline decode step; build: the prefill cache build")
     return ap.parse_args()
 
 
@@ -450,9 +452,103 @@ def run_reference(args, w, ws_n, rank):
 # main
 # ----------------------------------------------------------------------------
 
+def build_bytes(w, inp, out) -> int:
+    """HBM bytes the prefill build of one layer must move: read K, V (bf16),
+    the surprisal, W_r and the gates; write the full-resolution rows, the
+    routing summaries, the summary keys/values, the per-span metadata and the
+    basis records actually packed."""
+    B, Hkv, T = w.batch, w.n_kv_heads, w.ctx
+    ms = inp["max_spans"]
+    n_sp = out["n_spans"].long()
+    rd = 2 * B * Hkv * T * 128 * 2 + 4 * B * T + inp["W_r"].numel() * 4 + inp["gates"].size * 4
+    n_full = (w.n_sink + n_sp + w.n_recent).sum().item()
+    wr = Hkv * (512 * n_full + (256 + 512 + 8 + 4) * n_sp.sum().item()) + 4 * B * (1 + ms)
+    rec = out["rec_rank"].long()
+    body = out["body_len"].long()[:, None, :].expand_as(rec)
+    valid = torch.arange(ms, device=rec.device)[None, None, :] < n_sp[:, None, None]
+    recb = (gen.record_size(body, rec & 0xFFFF, (rec >> 16) & 0xFFFF) * (valid & (body > 0))).sum()
+    return int(rd + wr + recb.item())
+
+
+def run_build_bench(args, ws_n, rank, local):
+    """Prefill cache build at 128K (Mistral-7B shape): segmentation, summaries
+    and the batched gated span SVD of every span, one layer per call.  Two
+    layers of distinct inputs (1 GB of K/V) alternate, so every call streams
+    from HBM."""
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (build) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.get_config("mistral_7b_build_128k")
+    inps = [gen.build_inputs(w, l, device="cpu") for l in range(2)]
+    ms = max(i["max_spans"] for i in inps)
+    cfg = sk.Config(w.batch, w.n_q_heads, w.n_kv_heads, w.n_sink, w.n_recent, ms, w.rank_cap,
+                    w.len_min, w.len_max, w.tau)
+    ws = sk.Workspace(cfg, which=sk.sekv.SEKV_CALL_BUILD, ctx_len=w.ctx)
+    layers = []
+    for inp in inps:
+        gates = np.zeros((w.batch, w.n_kv_heads, 2, ms, w.rank_cap), np.float32)
+        gates[:, :, :, :inp["gates"].shape[3]] = inp["gates"]
+        layers.append(dict(K=inp["K"].to(dev), V=inp["V"].to(dev),
+                           H=torch.from_numpy(inp["H"]).to(dev), W=inp["W_r"].to(dev),
+                           g=torch.from_numpy(gates).to(dev), inp=inp,
+                           out=sk.alloc_cache(cfg, 1 << 30, dev)))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            L = layers[i % 2]
+            sk.build_spans(cfg, L["K"], L["V"], L["H"], L["W"], L["g"], L["out"], ws, stream=stream)
+    torch.cuda.synchronize()
+    ws.raise_on_error()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            L = layers[i % 2]
+            sk.build_spans(cfg, L["K"], L["V"], L["H"], L["W"], L["g"], L["out"], ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    barrier(ws_n)
+    ws.raise_on_error()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), ws_n)
+    per_call = ms_total / 1e3 / args.steps
+    tokens = w.batch * w.ctx
+    nbytes = sum(build_bytes(w, L["inp"], L["out"]) for L in layers) / 2
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / per_call / 1e9
+    if rank != 0:
+        return
+    line = {"metric": "prefill cache build tokens/s at 128K ctx (one layer per call)",
+            "value": whole_job_rate(args.steps, ms_total, ws_n) * tokens, "unit": "tokens/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, fp32 compute", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx,
+                       "kv_heads": w.n_kv_heads, "rank_cap": w.rank_cap,
+                       "spans_per_head": int(np.mean([int(L["out"]["n_spans"][0]) for L in layers])),
+                       "l2": "two layers of distinct inputs alternate (1 GB of K/V)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "bytes_per_call": nbytes,
+                         "note": "the batched Jacobi SVD is ALU-bound; this is the HBM fraction"},
+            "clocks": ck, "gpu_launches": None}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws_n, rank, local = dist_setup(args)
+    if args.path == "build":
+        run_build_bench(args, ws_n, rank, local)
+        return
     w = synth.get_config(args.config)
     if args.layers:
         w = synth.get_config(args.config, layers=args.layers)
