@@ -12,7 +12,7 @@ namespace sekv {
 
 
 
-// grid (chunks, Hkv, B).  Each CTA scores spans [chunk*1024, +1024) of one
+// grid (chunks, Hkv, B).  Each CTA scores spans [chunk*256, +256) of one
 // (sequence, KV head); the last CTA of the pair concatenates the slices.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams P) {
   __shared__ float qs[8][kHeadDim];
@@ -97,12 +97,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  int pre = 0;
-  for (int ch = 0; ch < P.chunks; ++ch) {
-    const int cnt = __ldcg(P.cnt_scratch + size_t(g) * P.chunks + ch);
-    for (int i = tid; i < cnt; i += kRouteThreads)
-      P.expanded[gs + pre + i] = __ldcg(P.list_scratch + gs + size_t(ch) * kRouteChunk + i);
-    pre += cnt;
+  // concatenate the chunks' slices: all counts in one round trip, prefix in
+  // shared memory, then every entry copied in one flattened pass
+  __shared__ int s_pre[kRouteMaxChunks + 1];
+  for (int ch = tid; ch < P.chunks; ch += kRouteThreads)
+    s_pre[ch + 1] = __ldcg(P.cnt_scratch + size_t(g) * P.chunks + ch);
+  __syncthreads();
+  if (tid == 0) {
+    s_pre[0] = 0;
+    for (int ch = 0; ch < P.chunks; ++ch) s_pre[ch + 1] += s_pre[ch];
+  }
+  __syncthreads();
+  const int pre = s_pre[P.chunks];
+  for (int e = tid; e < pre; e += kRouteThreads) {
+    int lo = 0, hi = P.chunks;  // last chunk whose prefix is <= e
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= e) lo = mid; else hi = mid;
+    }
+    P.expanded[gs + e] = __ldcg(P.list_scratch + gs + size_t(lo) * kRouteChunk + (e - s_pre[lo]));
   }
   if (tid == 0) {
     P.n_expanded[g] = pre;
@@ -160,7 +173,22 @@ __global__ void __launch_bounds__(256) fetch_kernel(const FetchParams P) {
           const long long st = carry + incl[t] - sz;
           const int4* src = reinterpret_cast<const int4*>(P.store + P.rec_off[gs + ks[t]]);
           int4* dst = reinterpret_cast<int4*>(P.staging + int64_t(g) * P.per_group + st);
-          for (long long i = tid; i < sz / 16; i += 256) dst[i] = src[i];
+          // eight 16-byte loads in flight per thread: the host link's latency
+          // is hidden by concurrency, not by one load at a time
+          const long long n16 = sz / 16;
+          for (long long i0 = 0; i0 < n16; i0 += 256 * kFetchUnroll) {
+            int4 v[kFetchUnroll];
+#pragma unroll
+            for (int u = 0; u < kFetchUnroll; ++u) {
+              const long long i = i0 + tid + 256 * u;
+              if (i < n16) v[u] = __ldcs(src + i);
+            }
+#pragma unroll
+            for (int u = 0; u < kFetchUnroll; ++u) {
+              const long long i = i0 + tid + 256 * u;
+              if (i < n16) dst[i] = v[u];
+            }
+          }
         }
       }
       __syncthreads();

@@ -5,8 +5,9 @@
 
 namespace sekv {
 
-constexpr int kRouteChunk = 1024;  // spans per routing CTA
+constexpr int kRouteChunk = 256;   // spans per routing CTA (one per thread)
 constexpr int kRouteThreads = 256;
+constexpr int kRouteMaxChunks = 1024;  // max_spans <= 262144
 
 struct RouteParams {
   const int32_t* n_spans;
@@ -25,7 +26,8 @@ struct RouteParams {
   int B, Hq, Hkv, G, max_spans, chunks;
 };
 
-constexpr int kFetchParts = 16;
+constexpr int kFetchParts = 48;
+constexpr int kFetchUnroll = 8;  // 16-byte loads in flight per thread
 
 struct FetchParams {
   const int32_t* n_spans;

@@ -24,6 +24,11 @@ bool config_ok(const sekv_config* cfg, sekv_status* why) {
     *why = SEKV_ERR_INVALID;
     return false;
   }
+  // the routing kernel concatenates at most kRouteMaxChunks slices
+  if (cfg->max_spans > kRouteChunk * kRouteMaxChunks) {
+    *why = SEKV_ERR_UNSUPPORTED;
+    return false;
+  }
   // the kernels split rows and spans among CTAs in 32-bit arithmetic
   if ((2 * int64_t(cfg->n_sink + cfg->n_recent) + 5 * int64_t(cfg->max_spans)) * 256 >=
       (int64_t(1) << 31)) {
@@ -67,7 +72,7 @@ int decode_cg(const sekv_config* cfg, int sms) {
   return cg > kMaxCgSmem ? kMaxCgSmem : cg;
 }
 
-int route_chunks(const sekv_config* cfg) { return (cfg->max_spans + 1023) / 1024; }
+int route_chunks(const sekv_config* cfg) { return (cfg->max_spans + kRouteChunk - 1) / kRouteChunk; }
 
 WsLayout ws_layout(const sekv_config* cfg, int sms) {
   WsLayout L{};
