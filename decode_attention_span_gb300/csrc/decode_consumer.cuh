@@ -57,6 +57,40 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
   lo = pack_bf16(x0 - hf.x, x1 - hf.y);
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Lazy online-softmax re-basing: the running max m only moves when a new
+// logit exceeds it by more than kRebase (log2 units), so exponentials stay
+// below 2^kRebase and most tiles skip the shuffles and the rescale.  The
+// output is normalised by the sum taken against the same m, so the choice of
+// m changes only rounding.
+constexpr float kRebase = 8.f;
+
+// Re-base the warp's state to cover the row maxima mx (rows lane/4) if
+// some lane's exceeds the running max by more than kRebase; returns alpha
+// (1 when nothing moved).
+__device__ __forceinline__ float rebase_if_needed(WarpAcc& A, float mx) {
+  float alpha = 1.f;
+  if (__any_sync(0xffffffffu, mx > A.m_row + kRebase)) {
+    mx = quad_max(mx);
+    const float m_new = fmaxf(A.m_row, mx);
+    float msub;
+    softmax_rescale(A.m_row, m_new, alpha, msub);
+    A.m_row = m_new;
+    A.l_part *= alpha;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      A.o[t][0] *= alpha;
+      A.o[t][1] *= alpha;
+    }
+  }
+  return alpha;
+}
+
 // One full-resolution or summary page: up to 32 rows whose 32-row boxes are
 // 128B-swizzled (keys for dims 0-63 at kb, 64-127 at kb + kBoxBytes; values
 // likewise at vb), folded into the warp's softmax state with one rescale.
@@ -104,10 +138,8 @@ __device__ __forceinline__ void consume_kv_page(WarpAcc& A, uint32_t kb, uint32_
         s[hh][nt][e] = valid ? fmaf(s[hh][nt][e], scale_log2, bias) : kNegInf;
         mx = fmaxf(mx, s[hh][nt][e]);
       }
-  mx = quad_max(mx);
-  const float m_new = fmaxf(A.m_row, mx);
-  float alpha, msub;
-  softmax_rescale(A.m_row, m_new, alpha, msub);
+  rebase_if_needed(A, mx);
+  const float msub = A.m_row == kNegInf ? 0.f : A.m_row;
   float ps = 0.f;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh)
@@ -115,18 +147,10 @@ __device__ __forceinline__ void consume_kv_page(WarpAcc& A, uint32_t kb, uint32_
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        s[hh][nt][e] = exp2f(s[hh][nt][e] - msub);
+        s[hh][nt][e] = ex2_approx(s[hh][nt][e] - msub);
         ps += s[hh][nt][e];
       }
-  A.l_part = fmaf(A.l_part, alpha, ps);
-  A.m_row = m_new;
-  if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      A.o[t][0] *= alpha;
-      A.o[t][1] *= alpha;
-    }
-  }
+  A.l_part += ps;
   const int mi = lane >> 3;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -288,11 +312,6 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
   X.had = false;
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Scores (log2 domain, scale folded into c) of the 16 body tokens
 // [rbase, rbase + 16) for the query heads, C layout: s[nt][e] is head
@@ -322,11 +341,10 @@ __device__ __forceinline__ void token_scores(const ExpAcc<KS>& X, uint32_t uku, 
 }
 
 // Body tokens [0, n) of this page; U_K rows at uk, U_V rows at uv (row
-// strides r8(rK), r8(rV) bf16).  Softmax at page granularity: pass 1 takes
-// the page's max logit per head, the state is rescaled once, pass 2
-// recomputes the scores and accumulates exp and w; the 16-token tiles of
-// either pass are independent of one another.  Rows or ranks past the valid
-// ones read neighbouring shared memory and are masked, never multiplied.
+// strides r8(rK), r8(rV) bf16), one pass of 16-token tiles with lazy
+// re-basing (the tiles are independent unless a re-base is needed).  Rows
+// or ranks past the valid ones read neighbouring shared memory and are
+// masked, never multiplied.
 template <int KS>
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* uk,
                                            const uint8_t* uv, int n, int rK, int rV) {
@@ -335,39 +353,22 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
   const int sk = 2 * r8(rK), sv = 2 * r8(rV);  // row strides in bytes
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
   const int mi = lane >> 3;
-  // pass 1: max logit of the page
-  float mx = kNegInf;
-#pragma unroll 2
-  for (int rb = 0; rb < n; rb += 16) {
-    float s[2][2];
-    token_scores<KS>(X, uku, sk, rb, n, rK, s);
-    mx = fmaxf(mx, fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
-  }
-  mx = quad_max(mx);
-  const float m_new = fmaxf(A.m_row, mx);
-  float alpha, msub;
-  softmax_rescale(A.m_row, m_new, alpha, msub);
-  A.m_row = m_new;
-  A.l_part *= alpha;
-  if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      A.o[t][0] *= alpha;
-      A.o[t][1] *= alpha;
-    }
-#pragma unroll
-    for (int t = 0; t < 2 * KS; ++t) {
-      X.wacc[t][0] *= alpha;
-      X.wacc[t][1] *= alpha;
-    }
-  }
   X.had = true;
-  // pass 2: p = 2^(s - m), row sums, w += p U_V
   float ps = 0.f;
 #pragma unroll 2
   for (int rb = 0; rb < n; rb += 16) {
     float s[2][2];
     token_scores<KS>(X, uku, sk, rb, n, rK, s);
+    const float alpha =
+        rebase_if_needed(A, fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
+    if (alpha != 1.f) {
+#pragma unroll
+      for (int t = 0; t < 2 * KS; ++t) {
+        X.wacc[t][0] *= alpha;
+        X.wacc[t][1] *= alpha;
+      }
+    }
+    const float msub = A.m_row == kNegInf ? 0.f : A.m_row;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
