@@ -384,7 +384,7 @@ cudaError_t launch_svd(const BuildParams& P, int cls, int sms, cudaStream_t stre
 cudaError_t launch_svd_all(const BuildParams& P, int sms, cudaStream_t stream) {
   cudaError_t e = launch_svd<32, 64, false>(P, 0, sms, stream);
   if (e == cudaSuccess) e = launch_svd<64, 128, false>(P, 1, sms, stream);
-  if (e == cudaSuccess) e = launch_svd<128, 512, false>(P, 2, sms, stream);
+  if (e == cudaSuccess) e = launch_svd<128, 1024, false>(P, 2, sms, stream);
   if (e == cudaSuccess) e = launch_svd<128, 512, true>(P, 3, sms, stream);
   return e;
 }
