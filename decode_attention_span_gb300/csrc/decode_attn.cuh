@@ -34,11 +34,8 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kSlotsPerWarp = 2;
 constexpr int kSlots = kConsumerWarps * kSlotsPerWarp;
-constexpr int kSlotBytes = 19456;     // 18 KB data + 1 KB routing aux, 1024-aligned
+constexpr int kSlotBytes = 19456;     // 18 KB of data, 1024-aligned (19 KB)
 constexpr int kPageData = 18432;      // bytes of data a page may hold
-constexpr int kAuxBody = 18432;       // routing page: body lengths (64 x int32)
-constexpr int kAuxRank = 18688;       //               ranks (64 x int32)
-constexpr int kAuxOff = 18944;        //               record offsets (64 x int64)
 constexpr int kTileRows = 32;         // rows per full / summary page
 constexpr int kBoxBytes = kTileRows * 128;  // one 128B-swizzled box: 32 rows x 64 bf16
 constexpr int kRouteSpans = 64;       // spans per routing page

@@ -15,21 +15,28 @@ namespace sekv {
 // ordinal on; the page keeps a bit mask of them and their record bytes.
 __device__ __forceinline__ void consume_route(const uint8_t* page, const PageDesc& d, int k0,
                                               const DecodeParams& P, SmemMisc* ms, float* infoc,
-                                              const float* ys, size_t gs) {
+                                              const float* ys, size_t gs, size_t bs) {
   const int lane = threadIdx.x & 31;
+  // the spans' metadata comes straight from global memory (issued before the
+  // logits, so its latency overlaps them)
+  int body[2], rank[2], size[2];
+  long long off[2];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int kk = lane + 32 * half;
+    const bool valid = kk < d.n;
+    body[half] = valid ? __ldg(P.body_len + bs + d.a + kk) : 0;
+    rank[half] = valid ? __ldg(P.rec_rank + gs + d.a + kk) : 0;
+    off[half] = valid ? __ldg(P.rec_off + gs + d.a + kk) : 0;
+  }
   const unsigned long long hits = route_hits(page, ys, ms->theta, P.G);
   // expanded spans of this page: entries compacted at [d.a, d.a + count), in
   // span order, each with the record bytes of the ones before it (cum)
-  int body[2], rank[2], size[2];
-  long long off[2];
   bool ex[2];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int kk = lane + 32 * half;
     const bool valid = kk < d.n;
-    body[half] = valid ? reinterpret_cast<const int*>(page + kAuxBody)[kk] : 0;
-    rank[half] = valid ? reinterpret_cast<const int*>(page + kAuxRank)[kk] : 0;
-    off[half] = valid ? reinterpret_cast<const long long*>(page + kAuxOff)[kk] : 0;
     ex[half] = valid && body[half] > 0 && ((hits >> kk) & 1ull);
     if (valid) infoc[d.a - k0 + kk] = (body[half] > 0 && !ex[half]) ? log2f(float(body[half])) : kNegInf;
     size[half] = ex[half] ? int(record_bytes(body[half], rank[half] & 0xffff, (rank[half] >> 16) & 0xffff)) : 0;
@@ -210,7 +217,7 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
     }
     // one call site per page routine keeps the kernel's code small
     if (d.type == PG_ROUTE) {
-      consume_route(page, d, k0, P, ms, infoc, ys, gs);
+      consume_route(page, d, k0, P, ms, infoc, ys, gs, size_t(b) * P.max_spans);
     } else if (d.type == PG_INFO) {
       const uint16_t* src = reinterpret_cast<const uint16_t*>(page);
       for (int i = lane; i < d.n; i += 32) {

@@ -205,10 +205,8 @@ __device__ __forceinline__ ProdState issue_fixed(uint8_t* smem, SmemMisc* ms, Pr
   const CUtensorMap* tk = full ? &P.tm_kfull : &P.tm_ksum;
   const CUtensorMap* tv = full ? &P.tm_vfull : &P.tm_vsum;
   const uint64_t pol = policy_evict_first();
-  tma_g2s_3d_hint(pg, tk, 0, a, g, &ms->full[slot], pol);
-  tma_g2s_3d_hint(pg + kBoxBytes, tk, 64, a, g, &ms->full[slot], pol);
-  tma_g2s_3d_hint(pg + 2 * kBoxBytes, tv, 0, a, g, &ms->full[slot], pol);
-  tma_g2s_3d_hint(pg + 3 * kBoxBytes, tv, 64, a, g, &ms->full[slot], pol);
+  tma_g2s_4d_hint(pg, tk, 0, a, 0, g, &ms->full[slot], pol);                  // both halves of K
+  tma_g2s_4d_hint(pg + 2 * kBoxBytes, tv, 0, a, 0, g, &ms->full[slot], pol);  // both halves of V
   commit_page(S, w, slot);
   return S;
 }
@@ -255,18 +253,13 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
       const uint64_t pol = policy_evict_first();
       for (int k = k0, p = 0; S.ok && k < k1; k += kRouteSpans, ++p) {
         const int n = (k1 - k) < kRouteSpans ? (k1 - k) : kRouteSpans;
-        const uint32_t n4 = uint32_t((n + 3) & ~3), n2 = uint32_t((n + 1) & ~1);
         d.type = PG_ROUTE; d.n = n; d.a = k; d.flag = p;
         const int w = pick_warp(smem, ms, S, P);
         if (!S.ok) break;
-        const int slot = arm_page(ms, S, w, d, 2 * 8192 + n4 * 8 + n2 * 8);
-        uint8_t* pg = slot_ptr(smem, slot);
-        tma_g2s_3d_hint(pg, &P.tm_sroute, 0, k, g, &ms->full[slot], pol);
-        tma_g2s_3d_hint(pg + 8192, &P.tm_sroute, 32, k, g, &ms->full[slot], pol);
-        bulk_g2s_hint(pg + kAuxBody, P.body_len + size_t(b) * P.max_spans + k, n4 * 4,
-                      &ms->full[slot], pol);
-        bulk_g2s_hint(pg + kAuxRank, P.rec_rank + gs + k, n4 * 4, &ms->full[slot], pol);
-        bulk_g2s_hint(pg + kAuxOff, P.rec_off + gs + k, n2 * 8, &ms->full[slot], pol);
+        // the routing summaries of 64 spans, both halves of each row (the
+        // consumer reads the spans' metadata from global memory itself)
+        const int slot = arm_page(ms, S, w, d, 2 * 8192);
+        tma_g2s_4d_hint(slot_ptr(smem, slot), &P.tm_sroute, 0, k, 0, g, &ms->full[slot], pol);
         commit_page(S, w, slot);
       }
     } else if (k1 > k0) {

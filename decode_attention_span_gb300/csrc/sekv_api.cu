@@ -140,6 +140,27 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of `row_elems` elements as a 4-D tensor (half-row, row, half, group)
+// so that one box of `box_rows` rows brings both 128-byte halves of each
+// row: in shared memory the first halves of the box's rows come first, then
+// the second halves, each 128B-swizzled by the row index.
+bool encode_rows4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                   uint64_t row_elems, uint64_t rows, uint64_t groups, int elem_bytes,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base) return false;
+  const uint64_t half = row_elems / 2;
+  const cuuint64_t dims[4] = {half, rows, 2, groups};
+  const cuuint64_t strides[3] = {row_elems * elem_bytes, half * elem_bytes,
+                                 rows * row_elems * elem_bytes};
+  const cuuint32_t box[4] = {uint32_t(half), box_rows, 2, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(map, dtype, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace sekv
 
 extern "C" {
@@ -217,12 +238,12 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   const int ng = L.ng;
   const uint64_t cap_full = uint64_t(cfg->n_sink) + cfg->max_spans + cfg->n_recent;
   bool ok = true;
-  ok &= encode_3d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, 64, kTileRows);
-  ok &= encode_3d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, 64, kTileRows);
-  ok &= encode_3d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, 64, kTileRows);
-  ok &= encode_3d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, 64, kTileRows);
+  ok &= encode_rows4d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, kTileRows);
+  ok &= encode_rows4d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, kTileRows);
+  ok &= encode_rows4d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, kTileRows);
+  ok &= encode_rows4d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, kTileRows);
   if (fused) {
-    ok &= encode_3d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, 32, kRouteSpans);
+    ok &= encode_rows4d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, kRouteSpans);
   } else {
     P.tm_sroute = P.tm_ksum;
   }

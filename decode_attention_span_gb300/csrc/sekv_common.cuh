@@ -161,6 +161,17 @@ __device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, in
       : "memory");
 }
 
+// 4-D tiled tensor copy global -> shared with an L2 cache hint.
+__device__ __forceinline__ void tma_g2s_4d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                int z, int w, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+      "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
