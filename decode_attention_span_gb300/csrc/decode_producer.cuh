@@ -245,10 +245,10 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
     PageDesc d{};
     if (P.fused) {
       prefetch_tmap(&P.tm_sroute);
-      // routing weights of this KV head: four 128B-swizzled boxes of 64 rows x 32 floats
+      // routing weights of this KV head in one copy (four 128B-swizzled blocks
+      // of 64 rows x 32 floats); every CTA of the head reads them: kept in L2
       mbar_arrive_expect_tx(&ms->wr_bar, kRouteDim * kHeadDim * 4);
-      for (int x = 0; x < 4; ++x)
-        tma_g2s_3d(smem + kOffWr + x * 8192, &P.tm_wr, 32 * x, 0, c, &ms->wr_bar);
+      tma_g2s_4d_hint(smem + kOffWr, &P.tm_wr, 0, 0, 0, c, &ms->wr_bar, policy_evict_last());
       // routing pages, 64 spans each
       const uint64_t pol = policy_evict_first();
       for (int k = k0, p = 0; S.ok && k < k1; k += kRouteSpans, ++p) {

@@ -277,8 +277,18 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
 
 // W_r [Hkv][64][128] fp32 as a tensor of boxes of 64 rows x 32 floats (128B swizzle)
 sekv_status encode_wr(DecodeParams& P, const float* W_r, const sekv_config* cfg) {
-  return encode_3d(&P.tm_wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W_r, 128, kRouteDim,
-                   cfg->n_kv_heads, 4, 32, kRouteDim)
+  // W_r [Hkv][64][128] fp32 as (32 floats, row, quarter, head): one box of
+  // 64 rows x 4 quarters brings a head's 32 KB in one copy, laid out in
+  // shared memory as four 128B-swizzled blocks of 64 rows x 32 floats
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !W_r) return SEKV_ERR_CUDA;
+  const cuuint64_t dims[4] = {32, uint64_t(kRouteDim), 4, uint64_t(cfg->n_kv_heads)};
+  const cuuint64_t strides[3] = {kHeadDim * 4, 32 * 4, uint64_t(kRouteDim) * kHeadDim * 4};
+  const cuuint32_t box[4] = {32, uint32_t(kRouteDim), 4, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(&P.tm_wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(W_r), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
              ? SEKV_OK
              : SEKV_ERR_CUDA;
 }

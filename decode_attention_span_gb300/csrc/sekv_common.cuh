@@ -132,6 +132,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// L2 policy for data many CTAs read (the routing weights of a KV head).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
                                               uint64_t* bar, uint64_t pol) {
   asm volatile(
