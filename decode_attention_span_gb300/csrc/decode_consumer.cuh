@@ -354,7 +354,6 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
   const int mi = lane >> 3;
   X.had = true;
-  float ps = 0.f;
 #pragma unroll 2
   for (int rb = 0; rb < n; rb += 16) {
     float s[2][2];
@@ -373,7 +372,8 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) s[nt][e] = ex2_approx(s[nt][e] - msub);
-    ps += (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
+    // into the running sum right away: a later re-base rescales it
+    A.l_part += (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
     const uint32_t a0 = pack_bf16(s[0][0], s[0][1]);
     const uint32_t a2 = pack_bf16(s[1][0], s[1][1]);
     const int tk = rb + 2 * (lane & 3);  // tokens held by b0/b2 (+8 in b1/b3)
@@ -389,7 +389,6 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
       mma_bf16_rows8(X.wacc[2 * jp + 1][0], X.wacc[2 * jp + 1][1], a0, a2, b2, b3);
     }
   }
-  A.l_part += ps;
 }
 
 template <int KS>

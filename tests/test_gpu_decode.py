@@ -74,6 +74,26 @@ def test_decode_step_matches_oracle(sk, name, over, mode):
         assert np.allclose(lse.cpu().numpy(), case.lse, atol=1e-3)
 
 
+@pytest.mark.parametrize("name,over", [("llama3_8b_32k", dict(ctx=8192)),
+                                       ("qwen2_7b_stress", dict(ctx=8192, batch=1))])
+def test_decode_step_sharp_softmax(sk, name, over):
+    """A 6x softmax scale spreads the logits over tens of log2 units, so the
+    online softmax re-bases its running max often, also between the 16-token
+    tiles of one expanded span: every partial sum must follow the re-base."""
+    case = decode_case(name, mode="all", run_oracle=False, **over)
+    sharp = 6.0 * SCALE
+    o_ref, lse_ref = oracle.decode_attention(case.q.float().numpy(), case.cache, case.E, sharp)
+    cfg = sk_config(sk, case)
+    cache = sk.LayerCache(to_dev(case))
+    ws = sk.Workspace(cfg)
+    out, lse, _, _ = sk.decode_step(cfg, cache, case.q.cuda(), case.W.cuda(),
+                                    torch.from_numpy(case.theta).cuda(), sharp, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    compare_out(out.cpu().numpy(), o_ref, f"{name} sharp softmax")
+    assert np.allclose(lse.cpu().numpy(), lse_ref, atol=1e-3)
+
+
 @pytest.mark.parametrize("name,over,mode", CASES[:3])
 def test_route_matches_oracle(sk, name, over, mode):
     case = decode_case(name, mode=mode, run_oracle=False, **over)
