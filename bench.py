@@ -93,6 +93,42 @@ def max_over_ranks(x: float, ws: int) -> float:
 # peaks and clocks
 # ----------------------------------------------------------------------------
 
+DECODE_SOURCES = ("decode_attn.cuh", "decode_consumer.cuh", "decode_producer.cuh",
+                  "decode_kernel_impl.cuh", "decode_ks1.cu", "decode_ks2.cu", "decode_ks3.cu",
+                  "decode_ks4.cu", "sekv_common.cuh")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_kernel_llama3_8b_128k.md")
+
+
+def decode_source_hash() -> str:
+    """sha256 over the decode kernel's sources (the kernel the profile covers)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "decode_attention_span_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, or None
+    when the kernel sources changed since it was taken."""
+    try:
+        text = open(DECODE_PROFILE, encoding="utf-8").read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        for key in ("source-sha256:", "traffic-bytes-per-launch:"):
+            if line.strip().startswith(key):
+                vals[key] = line.split(":", 1)[1].strip().strip("`")
+    if vals.get("source-sha256:") != decode_source_hash():
+        return None
+    try:
+        return int(vals["traffic-bytes-per-launch:"])
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -585,7 +621,7 @@ def main():
                        "parallelism": f"replicas x{ws_n}",
                        "graph": "one CUDA graph per step, programmatic dependent launch"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": profiled_traffic(),
                          "peak_kind": peak_kind, "kernel": "sekv::decode_kernel",
                          "bytes_per_launch": per_launch,
                          "avg_launch_us": launch_s * 1e6},
