@@ -175,11 +175,9 @@ struct SmemMisc {
   float theta[8];
   int pre_n[kMaxCgSmem + 1];                 // expanded spans before CTA jj (exclusive prefix)
   long long pre_b[kMaxCgSmem + 1];           // their record bytes
-  long long bsrc[kMaxRecPerPage];            // producer: small records waiting for a page
-  RecInfo btab[kMaxRecPerPage];
-  // producer: a record larger than a page being pushed part by part to warp
-  // sp_w (-1: none): its key part, U tiles, value part
-  int sp_w, sp_part, sp_nparts, sp_b, sp_rank;
+  // producer: a record larger than a page being pushed part by part to one
+  // warp: its key part, U tiles, value part
+  int sp_part, sp_nparts, sp_b, sp_rank;
   long long sp_off;
 };
 static_assert(sizeof(SmemMisc) <= kMiscBytes, "misc smem");

@@ -174,74 +174,47 @@ __device__ __forceinline__ void consume_kv_page(WarpAcc& A, uint32_t kb, uint32_
   }
 }
 
-// Bit 4i of x (i = 0..7) set iff nibble i of v has a set bit; returns those
-// eight bits packed into bits 0..7.
-__device__ __forceinline__ uint32_t nibble_any(uint32_t v) {
-  uint32_t m = (v | (v >> 1) | (v >> 2) | (v >> 3)) & 0x11111111u;
-  m = (m | (m >> 3)) & 0x03030303u;
-  m = (m | (m >> 6)) & 0x000F000Fu;
-  return (m | (m >> 12)) & 0xFFu;
-}
 
 // Routing logits z[span][head] = s_span . y_head of a routing page (two
-// 128B-swizzled boxes of 64 rows x 32 floats) on the tensor cores: spans are
-// the M rows (four tiles of 16), heads the N columns, routing dims K; s and y
-// both split into bf16 hi + lo parts, the products hi*hi, hi*lo and lo*hi
-// summed in fp32 (error about 2^-16 of sum |s_d y_d|).  The twelve
-// (tile, product) accumulators are independent chains; the k loop is rolled
-// (this runs about once per warp and launch, so its code is fetched cold).  Rows past the page's
-// spans are computed and ignored by the caller.  Returns the 64-bit mask of
-// spans with z > theta for some head of the group.
+// 128B-swizzled boxes of 64 rows x 32 floats) in fp32 FMAs: lane l takes the
+// spans l and l + 32, four heads per pass (y rows past the group are zero and
+// ignored).  Each 16-byte chunk of a row sits at chunk ^ (row & 7), so the
+// eight lanes of a quarter-warp read eight different bank groups; the y
+// chunks are broadcasts.  Rows past the page's spans are computed and ignored
+// by the caller.  Returns the 64-bit mask of spans with z > theta for some
+// head of the group.
 __device__ __forceinline__ unsigned long long route_hits(const uint8_t* page, const float* ys,
                                                         const float* theta, int G) {
-  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  float acc[4][3][4];
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-    for (int pr = 0; pr < 3; ++pr) acc[mt][pr][0] = acc[mt][pr][1] = acc[mt][pr][2] = acc[mt][pr][3] = 0.f;
+  const int lane = threadIdx.x & 31, sw = lane & 7;
+  bool hit0 = false, hit1 = false;
 #pragma unroll 1
-  for (int ks = 0; ks < 4; ++ks) {
-    uint32_t bh[2], bl[2];
+  for (int h0 = 0; h0 < G; h0 += 4) {
+    float z[2][4];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const float2 v = *reinterpret_cast<const float2*>(ys + gid * kRouteDim + 16 * ks + 8 * hf +
-                                                        2 * tig);
-      split_bf16(v.x, v.y, bh[hf], bl[hf]);
-    }
+    for (int hh = 0; hh < 4; ++hh) z[0][hh] = z[1][hh] = 0.f;
+#pragma unroll 2
+    for (int c = 0; c < 16; ++c) {  // routing dims 4c .. 4c + 3
+      const uint8_t* rowc = page + (c >> 3) * 8192 + lane * 128 + (((c & 7) ^ sw) << 4);
+      const float4 s0 = *reinterpret_cast<const float4*>(rowc);
+      const float4 s1 = *reinterpret_cast<const float4*>(rowc + 32 * 128);
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      uint32_t ah[4], al[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = 16 * mt + gid + 8 * (q & 1);
-        const int dim = 16 * ks + 2 * tig + 8 * (q >> 1);
-        const float2 v = *reinterpret_cast<const float2*>(
-            page + (dim >> 5) * 8192 + row * 128 + ((((dim & 31) >> 2) ^ (row & 7)) << 4) +
-            (dim & 3) * 4);
-        split_bf16(v.x, v.y, ah[q], al[q]);
+      for (int hh = 0; hh < 4; ++hh) {
+        const float4 y = *reinterpret_cast<const float4*>(ys + (h0 + hh) * kRouteDim + 4 * c);
+        z[0][hh] = fmaf(s0.w, y.w, fmaf(s0.z, y.z, fmaf(s0.y, y.y, fmaf(s0.x, y.x, z[0][hh]))));
+        z[1][hh] = fmaf(s1.w, y.w, fmaf(s1.z, y.z, fmaf(s1.y, y.y, fmaf(s1.x, y.x, z[1][hh]))));
       }
-      mma_bf16_16816(acc[mt][0], ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
-      mma_bf16_16816(acc[mt][1], ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-      mma_bf16_16816(acc[mt][2], al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      if (h0 + hh < G) {
+        const float th = theta[h0 + hh];
+        hit0 |= z[0][hh] > th;
+        hit1 |= z[1][hh] > th;
+      }
     }
   }
-  const bool ok0 = 2 * tig < G, ok1 = 2 * tig + 1 < G;
-  const float th0 = theta[2 * tig], th1 = theta[2 * tig + 1];
-  unsigned long long hits = 0;
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
-    float z[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) z[e] = (acc[mt][0][e] + acc[mt][1][e]) + acc[mt][2][e];
-    // rows gid, gid + 8; heads 2 tig, 2 tig + 1; any head of the quad
-    const bool hA = (ok0 && z[0] > th0) || (ok1 && z[1] > th1);
-    const bool hB = (ok0 && z[2] > th0) || (ok1 && z[3] > th1);
-    const uint32_t m16 = nibble_any(__ballot_sync(0xffffffffu, hA)) |
-                         (nibble_any(__ballot_sync(0xffffffffu, hB)) << 8);
-    hits |= (unsigned long long)m16 << (16 * mt);
-  }
-  return hits;
+  return (unsigned long long)__ballot_sync(0xffffffffu, hit0) |
+         ((unsigned long long)__ballot_sync(0xffffffffu, hit1) << 32);
 }
 
 // ---------------------------------------------------------------------------

@@ -420,7 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ms->wr_bar, 1);
     mbar_init(&ms->cmb_bar, 1);
-    ms->sp_w = -1;
     ms->is_last = 0;
     fence_mbar_init();
   }

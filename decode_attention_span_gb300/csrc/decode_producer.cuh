@@ -16,6 +16,7 @@ struct ProdState {
   uint32_t last_par;  // per slot: phase of the last page issued into it
   int rr;             // warp tried first by the next pick
   int ok;             // no wait has timed out
+  int spw;            // warp holding the split record being pushed (-1: none)
 };
 
 __device__ __forceinline__ int ring_slot(const ProdState& S, int w) {
@@ -29,6 +30,14 @@ __device__ __forceinline__ bool slot_free(SmemMisc* ms, const ProdState& S, int 
   return mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u);
 }
 
+// Bit w set iff warp w's next slot is free (the four tests overlap).
+__device__ __forceinline__ uint32_t free_warps(SmemMisc* ms, const ProdState& S) {
+  const uint32_t e0 = smem_u32(&ms->empty[0]);
+  return mbar_test4(e0 + 8u * ring_slot(S, 0), e0 + 8u * ring_slot(S, 1),
+                    e0 + 8u * ring_slot(S, 2), e0 + 8u * ring_slot(S, 3), ring_phase(S, 0) ^ 1u,
+                    ring_phase(S, 1) ^ 1u, ring_phase(S, 2) ^ 1u, ring_phase(S, 3) ^ 1u);
+}
+
 __device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
                                                      ProdState S, const DecodeParams& P);
 
@@ -36,11 +45,21 @@ __device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms
 // slot is free; bounded.  While it polls it keeps the split record moving.
 __device__ __forceinline__ int pick_warp(uint8_t* smem, SmemMisc* ms, ProdState& S,
                                          const DecodeParams& P) {
-  int w = S.rr;
+  static_assert(kConsumerWarps == 4, "four consumer warps");
+  int w = 0;
   for (uint32_t it = 0;; ++it) {
-    if (ms->sp_w >= 0 && slot_free(ms, S, ms->sp_w)) S = push_split_part(smem, ms, S, P);
-    if (w != ms->sp_w && slot_free(ms, S, w)) break;
-    w = (w + 1) & (kConsumerWarps - 1);
+    uint32_t fm = free_warps(ms, S);
+    if (S.spw >= 0) {
+      const uint32_t sb = 1u << S.spw;
+      if (fm & sb) S = push_split_part(smem, ms, S, P);
+      fm &= ~sb;  // its free slot was just filled, or it holds the split record
+    }
+    if (fm) {
+      // the first free warp from S.rr on
+      const uint32_t rot = ((fm | (fm << 4)) >> S.rr) & 0xFu;
+      w = (S.rr + __ffs(rot) - 1) & 3;
+      break;
+    }
     if (it >= kWaitLimit || !S.ok) {
       set_device_error(P.status, DEV_WAIT_TIMEOUT, 6);
       S.ok = 0;
@@ -62,14 +81,12 @@ __device__ __forceinline__ bool wait_warp(SmemMisc* ms, ProdState& S, int w, int
   return true;
 }
 
-// Warp w's next slot, known free: publish the descriptor (and the record
-// table of a multi-record page), then arm the full barrier, so that the
-// consumer's acquire on the barrier covers both.
+// Warp w's next slot, known free: publish the descriptor, then arm the full
+// barrier, so that the consumer's acquire on the barrier covers it.
 __device__ __forceinline__ int arm_page(SmemMisc* ms, const ProdState& S, int w,
-                                        const PageDesc& d, uint32_t bytes, int ntab = 0) {
+                                        const PageDesc& d, uint32_t bytes) {
   const int slot = ring_slot(S, w);
   ms->desc[slot] = d;
-  for (int i = 0; i < ntab; ++i) ms->rec[slot][i] = ms->btab[i];
   mbar_arrive_expect_tx(&ms->full[slot], bytes);
   return slot;
 }
@@ -83,25 +100,48 @@ __device__ __forceinline__ void commit_page(ProdState& S, int w, int slot) {
   S.rs = (S.rs & ~(3u << (2 * w))) | (nv << (2 * w));
 }
 
-// The n small records staged in ms->bsrc / ms->btab (bytes in all) as one page.
-__device__ __forceinline__ ProdState flush_batch(uint8_t* smem, SmemMisc* ms, ProdState S,
-                                              const DecodeParams& P, int n, int bytes) {
-  if (n == 0 || !S.ok) return S;
-  const uint64_t pol = policy_evict_first();
-  const int w = pick_warp(smem, ms, S, P);
-  if (!S.ok) return S;
-  PageDesc d{};
-  d.type = PG_EXPM;
-  d.n = n;
-  const int slot = arm_page(ms, S, w, d, uint32_t(bytes), n);
-  uint8_t* pg = slot_ptr(smem, slot);
-  for (int i = 0; i < n; ++i) {
-    const RecInfo ri = ms->btab[i];
-    bulk_g2s_hint(pg + ri.off, P.store + ms->bsrc[i], uint32_t(record_bytes(ri.b, ri.rk, ri.rv)),
-                  &ms->full[slot], pol);
+// Small records staged for the next multi-record page: lane i holds record
+// i (its source offset and table entry); n and bytes are the same in every lane.
+struct Batch {
+  int n, bytes;
+  long long src;
+  RecInfo ri;
+};
+
+// The staged records as one page.  Called by the whole warp: lane 0 picks
+// the warp and arms the barrier, every staged lane writes its table entry
+// and issues its own copy.
+__device__ __forceinline__ void flush_batch(uint8_t* smem, SmemMisc* ms, ProdState& S,
+                                            const DecodeParams& P, Batch& B) {
+  const int lane = threadIdx.x & 31;
+  if (B.n == 0 || !S.ok) return;
+  int slot = 0;
+  if (lane == 0) {
+    const int w = pick_warp(smem, ms, S, P);
+    if (S.ok) {
+      slot = ring_slot(S, w);
+      PageDesc d{};
+      d.type = PG_EXPM;
+      d.n = B.n;
+      ms->desc[slot] = d;
+      commit_page(S, w, slot);  // ring state only: the barrier is armed below
+    }
   }
-  commit_page(S, w, slot);
-  return S;
+  S.ok = __shfl_sync(0xffffffffu, S.ok, 0);
+  slot = __shfl_sync(0xffffffffu, slot, 0);
+  if (S.ok) {
+    if (lane < B.n) ms->rec[slot][lane] = B.ri;
+    __syncwarp();
+    // the descriptor and the table are published by this arrive (release)
+    if (lane == 0) mbar_arrive_expect_tx(&ms->full[slot], uint32_t(B.bytes));
+    __syncwarp();
+    if (lane < B.n)
+      bulk_g2s_hint(slot_ptr(smem, slot) + B.ri.off, P.store + B.src,
+                    uint32_t(record_bytes(B.ri.b, B.ri.rk, B.ri.rv)), &ms->full[slot],
+                    policy_evict_first());
+  }
+  B.n = 0;
+  B.bytes = 0;
 }
 
 // A record larger than a page goes to one warp as several pages (its key
@@ -114,11 +154,11 @@ __device__ __forceinline__ int split_rows(int rK, int rV) {
   return rows > 512 ? 512 : rows;
 }
 
-// Part ms->sp_part of the split record to warp ms->sp_w, whose next slot is free.
+// Part ms->sp_part of the split record to warp S.spw, whose next slot is free.
 __device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
                                                          ProdState S, const DecodeParams& P) {
   const uint64_t pol = policy_evict_first();
-  const int w = ms->sp_w, part = ms->sp_part, b = ms->sp_b;
+  const int w = S.spw, part = ms->sp_part, b = ms->sp_b;
   const int rK = ms->sp_rank & 0xFFFF, rV = (ms->sp_rank >> 16) & 0xFFFF;
   const uint8_t* rec = P.store + ms->sp_off;
   const RecordLayout L = record_layout(b, rK, rV);
@@ -155,15 +195,15 @@ __device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms
     bulk_g2s_hint(pg, rec + L.vpart, bytes, &ms->full[slot], pol);
   }
   commit_page(S, w, slot);
-  if (++ms->sp_part == ms->sp_nparts) ms->sp_w = -1;
+  if (++ms->sp_part == ms->sp_nparts) S.spw = -1;
   return S;
 }
 
 // Push every remaining part of the split record (waits on its warp).
 __device__ __forceinline__ ProdState finish_split(uint8_t* smem, SmemMisc* ms, ProdState S,
                                                   const DecodeParams& P) {
-  while (ms->sp_w >= 0 && S.ok)
-    if (wait_warp(ms, S, ms->sp_w, P.status)) S = push_split_part(smem, ms, S, P);
+  while (S.spw >= 0 && S.ok)
+    if (wait_warp(ms, S, S.spw, P.status)) S = push_split_part(smem, ms, S, P);
   return S;
 }
 
@@ -182,7 +222,7 @@ __device__ __forceinline__ ProdState start_split(uint8_t* smem, SmemMisc* ms, Pr
   ms->sp_b = b;
   ms->sp_rank = rank;
   ms->sp_off = off;
-  ms->sp_w = w;
+  S.spw = w;
   return push_split_part(smem, ms, S, P);
 }
 
@@ -231,7 +271,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
   const int nfp = (f1 - f0 + kTileRows - 1) / kTileRows;
   const int nfixed = nfp + (k1 - k0 + kTileRows - 1) / kTileRows;
-  ProdState S{0u, 0u, 0u, 0, 1};
+  ProdState S{0u, 0u, 0u, 0, 1, -1};
   const size_t gs = size_t(g) * P.max_spans;
   int t_fixed = 0;  // fixed pages issued so far
 
@@ -310,7 +350,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
     pub = __shfl_sync(0xffffffffu, pub, 0);
     if (pub < P.cg) S.ok = 0;
   }
-  int bn = 0, bbytes = 0;  // staged small records (lane 0)
+  Batch B{0, 0, 0, RecInfo{}};  // staged small records
   if (S.ok) {
     const int cg = P.cg;
     // round trip 1: expanded-span counts and bytes of every CTA, prefixed
@@ -340,8 +380,9 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
     }
     const long long Tb = ms->pre_b[cg];
     const long long lo = byte_split(Tb, j, cg), hi = byte_split(Tb, j + 1, cg);
-    // lanes hold candidate entries in byte order; lane 0 takes those that
-    // start in [lo, hi): into the current batch, or as a split record
+    // lanes hold candidate entries in byte order; those that start in
+    // [lo, hi) go into the current batch, or out as split records (every
+    // lane follows the batch; lane 0 alone issues)
     auto offer = [&](bool mine, const ExpEntry& en) {
       uint32_t bal = __ballot_sync(0xffffffffu, mine);
       while (bal && S.ok) {
@@ -350,25 +391,20 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
         const int body = __shfl_sync(0xffffffffu, en.body, src);
         const int rank = __shfl_sync(0xffffffffu, en.rank, src);
         const long long off = __shfl_sync(0xffffffffu, en.off, src);
-        if (lane == 0) {
-          const int xr = rank & 0xFFFF, xv = (rank >> 16) & 0xFFFF;
-          const int sz = int(record_bytes(body, xr, xv));
-          if (xr > P.rank_lim || xv > P.rank_lim) {
-            set_device_error(P.status, DEV_BAD_RANK, xr > xv ? xr : xv);  // record skipped
-          } else if (sz > kPageData) {
-            S = start_split(smem, ms, S, P, body, rank, off);
-          } else {
-            if (bn == kMaxRecPerPage || bbytes + sz > kPageData) {
-              S = flush_batch(smem, ms, S, P, bn, bbytes);
-              bn = 0;
-              bbytes = 0;
-            }
-            ms->bsrc[bn] = off;
-            ms->btab[bn] = RecInfo{bbytes, body, xr, xv};
-            bbytes += sz;
-            ++bn;
-
+        const int xr = rank & 0xFFFF, xv = (rank >> 16) & 0xFFFF;
+        const int sz = int(record_bytes(body, xr, xv));
+        if (xr > P.rank_lim || xv > P.rank_lim) {
+          if (lane == 0) set_device_error(P.status, DEV_BAD_RANK, xr > xv ? xr : xv);  // skipped
+        } else if (sz > kPageData) {
+          if (lane == 0) S = start_split(smem, ms, S, P, body, rank, off);
+        } else {
+          if (B.n == kMaxRecPerPage || B.bytes + sz > kPageData) flush_batch(smem, ms, S, P, B);
+          if (lane == B.n) {
+            B.src = off;
+            B.ri = RecInfo{B.bytes, body, xr, xv};
           }
+          B.bytes += sz;
+          ++B.n;
         }
         S.ok = __shfl_sync(0xffffffffu, S.ok, 0);
       }
@@ -439,8 +475,8 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
       }
     }
   }
+  flush_batch(smem, ms, S, P, B);
   if (lane == 0) {
-    S = flush_batch(smem, ms, S, P, bn, bbytes);
     // the remaining fixed pages, to whichever warp frees a slot first
     while (S.ok && t_fixed < nfixed) {
       S = issue_fixed(smem, ms, S, P, t_fixed, nfp, f0, f1, k0, k1, g);

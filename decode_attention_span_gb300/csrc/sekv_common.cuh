@@ -99,6 +99,27 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Four independent phase tests in one go (their latencies overlap); bit i of
+// the result is set iff barrier i has completed the phase of parity q_i.
+__device__ __forceinline__ uint32_t mbar_test4(uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t q0, uint32_t q1, uint32_t q2,
+                                               uint32_t q3) {
+  uint32_t m;
+  asm volatile(
+      "{\n .reg .pred p0, p1, p2, p3;\n .reg .b32 t0, t1, t2, t3;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p0, [%1], %5;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p1, [%2], %6;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p2, [%3], %7;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p3, [%4], %8;\n"
+      " selp.b32 t0, 1, 0, p0;\n selp.b32 t1, 2, 0, p1;\n"
+      " selp.b32 t2, 4, 0, p2;\n selp.b32 t3, 8, 0, p3;\n"
+      " or.b32 t0, t0, t1;\n or.b32 t2, t2, t3;\n or.b32 %0, t0, t2;\n}\n"
+      : "=r"(m)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(q0), "r"(q1), "r"(q2), "r"(q3)
+      : "memory");
+  return m;
+}
+
 // Bounded wait: returns false after `limit` polls (the caller flags an error).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i) {
