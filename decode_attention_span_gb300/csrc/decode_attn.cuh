@@ -75,7 +75,9 @@ struct PageDesc {
   int off_uk;  // PG_EXP: byte offset of U_K rows [a, a+n)
   int off_uv;  // PG_EXP: byte offset of U_V rows [a, a+n)
   int off_b;   // PG_EXP: byte offset of the value part (sigma_V..Vt_V) or -1
-  int pad0, pad1;
+  int part;    // PG_EXP: part index of the record
+  int b;       // PG_EXP: body tokens of the record
+  long long src;  // PG_EXP: the record's byte offset from the store base
 };
 
 struct DecodeParams {
@@ -175,10 +177,9 @@ struct SmemMisc {
   float theta[8];
   int pre_n[kMaxCgSmem + 1];                 // expanded spans before CTA jj (exclusive prefix)
   long long pre_b[kMaxCgSmem + 1];           // their record bytes
-  // producer: a record larger than a page being pushed part by part to one
-  // warp: its key part, U tiles, value part
-  int sp_part, sp_nparts, sp_b, sp_rank;
-  long long sp_off;
+  // warp w is loading and consuming a record larger than a page: set by the
+  // producer when it hands the record over, cleared by warp w after its last part
+  alignas(16) int sp_busy[kConsumerWarps];
 };
 static_assert(sizeof(SmemMisc) <= kMiscBytes, "misc smem");
 
@@ -200,6 +201,75 @@ __device__ __forceinline__ void ring_advance(Ring& r) {
     r.s = 0;
     r.phase ^= 1u;
   }
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// U rows per middle part of a record larger than a page (multiple of 16).
+__device__ __forceinline__ int split_rows(int rK, int rV) {
+  const int row_bytes = 2 * (r8(rK) + r8(rV));
+  int rows = row_bytes > 0 ? (kPageData / row_bytes) & ~15 : 512;
+  return rows > 512 ? 512 : rows;
+}
+
+// Parts of such a record: the key part, ceil(b / rows) U tiles, the value part.
+__device__ __forceinline__ int split_nparts(int b, int rK, int rV) {
+  const int rows = split_rows(rK, rV);
+  return 2 + (b + rows - 1) / rows;
+}
+
+// Part `part` of the record at store offset src (b body tokens, ranks rK,
+// rV) into `slot`, whose previous page has been consumed: its descriptor, the
+// full barrier armed with its bytes, then its one or two copies.  Issued by
+// one thread (the producer for part 0, the consuming warp for the others).
+__device__ __forceinline__ void issue_split_part(uint8_t* smem, SmemMisc* ms,
+                                                 const DecodeParams& P, int slot, int part, int b,
+                                                 int rK, int rV, long long src) {
+  const RecordLayout L = record_layout(b, rK, rV);
+  const int np = split_nparts(b, rK, rV);
+  PageDesc d{};
+  d.type = PG_EXP;
+  d.rk = rK;
+  d.rv = rV;
+  d.off_a = -1;
+  d.off_b = -1;
+  d.part = part;
+  d.b = b;
+  d.src = src;
+  int64_t s0 = 0, s1 = 0;
+  uint32_t n0 = 0, n1 = 0;
+  if (part == 0) {  // header, sigma_K, g_K, Vt_K
+    d.off_a = 0;
+    n0 = uint32_t(L.uk);
+  } else if (part < np - 1) {  // U_K and U_V rows of one tile
+    const int rows = split_rows(rK, rV);
+    const int i0 = (part - 1) * rows;
+    d.n = (b - i0) < rows ? (b - i0) : rows;
+    d.a = i0;
+    d.off_uv = 2 * d.n * r8(rK);
+    s0 = L.uk + 2 * int64_t(i0) * r8(rK);
+    n0 = uint32_t(d.off_uv);
+    s1 = L.uv + 2 * int64_t(i0) * r8(rV);
+    n1 = uint32_t(2 * d.n * r8(rV));
+  } else {  // sigma_V, g_V, Vt_V
+    d.off_b = 0;
+    s0 = L.vpart;
+    n0 = uint32_t(L.total - L.vpart);
+  }
+  ms->desc[slot] = d;
+  mbar_arrive_expect_tx(&ms->full[slot], n0 + n1);
+  uint8_t* pg = slot_ptr(smem, slot);
+  const uint8_t* rec = P.store + src;
+  const uint64_t pol = policy_evict_first();
+  if (n0) bulk_g2s_hint(pg, rec + s0, n0, &ms->full[slot], pol);
+  if (n1) bulk_g2s_hint(pg + n0, rec + s1, n1, &ms->full[slot], pol);
 }
 
 }  // namespace sekv

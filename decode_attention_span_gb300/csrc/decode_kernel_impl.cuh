@@ -8,8 +8,8 @@
 
 namespace sekv {
 
-// Routing page (64 spans), processed by one warp: z_h = y_h . s_S on the
-// tensor cores, then two spans per lane for the bookkeeping.  A span expands
+// Routing page (64 spans), processed by one warp: z_h = y_h . s_S in fp32
+// FMAs, then two spans per lane for the bookkeeping.  A span expands
 // iff its body is non-empty and some head of the group has z_h > theta_h.
 // The page's expanded spans get compact entries from the page's first span
 // ordinal on; the page keeps a bit mask of them and their record bytes.
@@ -228,7 +228,12 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
       consume_kv_page(A, pu, pu + 2 * kBoxBytes, d.n,
                       d.type == PG_SUM ? infoc + (d.a - k0) : nullptr, P.scale_log2);
     } else if (d.type == PG_EXP || d.type == PG_EXPM) {
-      // PG_EXP: one part of a record split over pages; PG_EXPM: whole records
+      // PG_EXP: one part of a record split over pages; PG_EXPM: whole records.
+      // The next part of a split record goes into this warp's other slot
+      // (its previous page is consumed) before this part is processed.
+      if (d.type == PG_EXP && lane == 0 && d.part + 1 < split_nparts(d.b, d.rk, d.rv))
+        issue_split_part(smem, ms, P, w * kSlotsPerWarp + (R.s ^ 1), d.part + 1, d.b, d.rk, d.rv,
+                         d.src);
       const int nrec = d.type == PG_EXPM ? d.n : 1;
       for (int i = 0; i < nrec; ++i) {
         int off_a = d.off_a, off_uk = d.off_uk, off_uv = d.off_uv, off_b = d.off_b;
@@ -251,6 +256,9 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->empty[slot]);
+    // the last part of a split record consumed: the ring is the producer's again
+    if (d.type == PG_EXP && lane == 0 && d.part + 1 == split_nparts(d.b, d.rk, d.rv))
+      st_release_cta(&ms->sp_busy[w], 0);
     if (d.type == PG_END) break;
     ring_advance(R);
   }
@@ -421,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms->wr_bar, 1);
     mbar_init(&ms->cmb_bar, 1);
     ms->is_last = 0;
+    for (int x = 0; x < kConsumerWarps; ++x) ms->sp_busy[x] = 0;
     fence_mbar_init();
   }
   __syncthreads();

@@ -16,7 +16,7 @@ struct ProdState {
   uint32_t last_par;  // per slot: phase of the last page issued into it
   int rr;             // warp tried first by the next pick
   int ok;             // no wait has timed out
-  int spw;            // warp holding the split record being pushed (-1: none)
+  uint32_t spm;       // bit w: warp w is consuming a record larger than a page
 };
 
 __device__ __forceinline__ int ring_slot(const ProdState& S, int w) {
@@ -38,22 +38,25 @@ __device__ __forceinline__ uint32_t free_warps(SmemMisc* ms, const ProdState& S)
                     ring_phase(S, 1) ^ 1u, ring_phase(S, 2) ^ 1u, ring_phase(S, 3) ^ 1u);
 }
 
-__device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
-                                                     ProdState S, const DecodeParams& P);
+// Warps whose record larger than a page is still in progress (acquire: a
+// cleared flag comes after that warp's last release of its ring slots).
+__device__ __forceinline__ uint32_t busy_warps(SmemMisc* ms) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int x = 0; x < kConsumerWarps; ++x) m |= ld_acquire_cta(&ms->sp_busy[x]) ? (1u << x) : 0u;
+  return m;
+}
 
-// First warp (from S.rr on, never the one holding a split record) whose next
-// slot is free; bounded.  While it polls it keeps the split record moving.
+// First warp (from S.rr on, never one still consuming a record larger than a
+// page) whose next slot is free; bounded.
 __device__ __forceinline__ int pick_warp(uint8_t* smem, SmemMisc* ms, ProdState& S,
                                          const DecodeParams& P) {
   static_assert(kConsumerWarps == 4, "four consumer warps");
   int w = 0;
   for (uint32_t it = 0;; ++it) {
-    uint32_t fm = free_warps(ms, S);
-    if (S.spw >= 0) {
-      const uint32_t sb = 1u << S.spw;
-      if (fm & sb) S = push_split_part(smem, ms, S, P);
-      fm &= ~sb;  // its free slot was just filled, or it holds the split record
-    }
+    if (S.spm) S.spm &= busy_warps(ms);
+    // a warp consuming a large record has its ring slots ahead in use
+    const uint32_t fm = free_warps(ms, S) & ~S.spm;
     if (fm) {
       // the first free warp from S.rr on
       const uint32_t rot = ((fm | (fm << 4)) >> S.rr) & 0xFu;
@@ -144,86 +147,42 @@ __device__ __forceinline__ void flush_batch(uint8_t* smem, SmemMisc* ms, ProdSta
   B.bytes = 0;
 }
 
-// A record larger than a page goes to one warp as several pages (its key
-// part, its U rows in tiles, its value part; the partial state of the span
-// stays in that warp's registers).  The parts are pushed one at a time as
-// that warp frees slots, so the other warps are never held up behind it.
-__device__ __forceinline__ int split_rows(int rK, int rV) {
-  const int row_bytes = 2 * (r8(rK) + r8(rV));
-  int rows = row_bytes > 0 ? (kPageData / row_bytes) & ~15 : 512;
-  return rows > 512 ? 512 : rows;
-}
-
-// Part ms->sp_part of the split record to warp S.spw, whose next slot is free.
-__device__ __forceinline__ ProdState push_split_part(uint8_t* smem, SmemMisc* ms,
-                                                         ProdState S, const DecodeParams& P) {
-  const uint64_t pol = policy_evict_first();
-  const int w = S.spw, part = ms->sp_part, b = ms->sp_b;
-  const int rK = ms->sp_rank & 0xFFFF, rV = (ms->sp_rank >> 16) & 0xFFFF;
-  const uint8_t* rec = P.store + ms->sp_off;
-  const RecordLayout L = record_layout(b, rK, rV);
-  const int rows = split_rows(rK, rV);
-  PageDesc d{};
-  d.type = PG_EXP;
-  d.rk = rK;
-  d.rv = rV;
-  d.off_a = -1;
-  d.off_b = -1;
-  uint32_t bytes;
-  if (part == 0) {  // header, sigma_K, g_K, Vt_K
-    d.off_a = 0;
-    bytes = uint32_t(L.uk);
-  } else if (part < ms->sp_nparts - 1) {  // U_K and U_V rows of one tile
-    const int i0 = (part - 1) * rows;
-    d.n = (b - i0) < rows ? (b - i0) : rows;
-    d.a = i0;
-    d.off_uv = 2 * d.n * r8(rK);
-    bytes = uint32_t(d.off_uv + 2 * d.n * r8(rV));
-  } else {  // sigma_V, g_V, Vt_V
-    d.off_b = 0;
-    bytes = uint32_t(L.total - L.vpart);
-  }
-  const int slot = arm_page(ms, S, w, d, bytes);
-  uint8_t* pg = slot_ptr(smem, slot);
-  if (part == 0) {
-    bulk_g2s_hint(pg, rec, bytes, &ms->full[slot], pol);
-  } else if (part < ms->sp_nparts - 1) {
-    const uint32_t bk = uint32_t(d.off_uv), bv = bytes - bk;
-    if (bk) bulk_g2s_hint(pg, rec + L.uk + 2 * int64_t(d.a) * r8(rK), bk, &ms->full[slot], pol);
-    if (bv) bulk_g2s_hint(pg + bk, rec + L.uv + 2 * int64_t(d.a) * r8(rV), bv, &ms->full[slot], pol);
-  } else if (bytes) {
-    bulk_g2s_hint(pg, rec + L.vpart, bytes, &ms->full[slot], pol);
-  }
-  commit_page(S, w, slot);
-  if (++ms->sp_part == ms->sp_nparts) S.spw = -1;
-  return S;
-}
-
-// Push every remaining part of the split record (waits on its warp).
-__device__ __forceinline__ ProdState finish_split(uint8_t* smem, SmemMisc* ms, ProdState S,
-                                                  const DecodeParams& P) {
-  while (S.spw >= 0 && S.ok)
-    if (wait_warp(ms, S, S.spw, P.status)) S = push_split_part(smem, ms, S, P);
-  return S;
-}
-
-// Start a split record on a free warp (the previous split, if any, first).
+// A record larger than a page goes to one warp as several pages: its key
+// part, its U rows in tiles, its value part (the partial state of the span
+// stays in that warp's registers).  The producer hands over part 0 and
+// counts all the parts into that warp's ring; the warp loads each further
+// part into its other slot itself as it starts on the one before, so the
+// parts follow each other at the warp's own pace.
 __device__ __forceinline__ ProdState start_split(uint8_t* smem, SmemMisc* ms, ProdState S,
-                                                     const DecodeParams& P, int b, int rank,
-                                                     long long off) {
-  S = finish_split(smem, ms, S, P);
-  if (!S.ok) return S;
+                                                 const DecodeParams& P, int b, int rank,
+                                                 long long off) {
   const int w = pick_warp(smem, ms, S, P);
   if (!S.ok) return S;
   const int rK = rank & 0xFFFF, rV = (rank >> 16) & 0xFFFF;
-  const int rows = split_rows(rK, rV);
-  ms->sp_part = 0;
-  ms->sp_nparts = 2 + (b + rows - 1) / rows;
-  ms->sp_b = b;
-  ms->sp_rank = rank;
-  ms->sp_off = off;
-  S.spw = w;
-  return push_split_part(smem, ms, S, P);
+  // Until the warp clears its flag the producer's view of its ring runs
+  // ahead of the barriers (all parts counted in), and a one-bit parity test
+  // would take a phase two back for the awaited one: its slots go untested.
+  ms->sp_busy[w] = 1;
+  const int slot = ring_slot(S, w);
+  issue_split_part(smem, ms, P, slot, 0, b, rK, rV, off);
+  const int np = split_nparts(b, rK, rV);
+  for (int k = 0; k < np; ++k) commit_page(S, w, ring_slot(S, w));
+  S.spm |= 1u << w;
+  return S;
+}
+
+// Every large record handed over has been consumed (bounded wait).
+__device__ __forceinline__ ProdState finish_splits(SmemMisc* ms, ProdState S,
+                                                   const DecodeParams& P) {
+  for (uint32_t it = 0; S.spm && S.ok; ++it) {
+    S.spm &= busy_warps(ms);
+    if (it >= kWaitLimit) {
+      set_device_error(P.status, DEV_WAIT_TIMEOUT, 8);
+      S.ok = 0;
+    }
+    if (it > 64) __nanosleep(32);
+  }
+  return S;
 }
 
 // Fixed page t of this CTA: full-resolution rows first, then summary rows,
@@ -271,7 +230,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
   fixed_range(j, P.cg, n_full, n_sp, P.fused, f0, f1, k0, k1);
   const int nfp = (f1 - f0 + kTileRows - 1) / kTileRows;
   const int nfixed = nfp + (k1 - k0 + kTileRows - 1) / kTileRows;
-  ProdState S{0u, 0u, 0u, 0, 1, -1};
+  ProdState S{0u, 0u, 0u, 0, 1, 0u};
   const size_t gs = size_t(g) * P.max_spans;
   int t_fixed = 0;  // fixed pages issued so far
 
@@ -482,7 +441,7 @@ static __device__ void producer_warp(uint8_t* smem, SmemMisc* ms, const DecodePa
       S = issue_fixed(smem, ms, S, P, t_fixed, nfp, f0, f1, k0, k1, g);
       ++t_fixed;
     }
-    S = finish_split(smem, ms, S, P);
+    S = finish_splits(ms, S, P);
     // every consumer warp ends with an END page
     for (int w = 0; w < kConsumerWarps; ++w) {
       PageDesc d{};
