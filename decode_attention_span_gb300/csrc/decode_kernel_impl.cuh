@@ -199,7 +199,7 @@ __device__ void consumer_warps(uint8_t* smem, SmemMisc* ms, const DecodeParams& 
   const int np = (k1 - k0 + kRouteSpans - 1) / kRouteSpans;
   for (;;) {
     const int slot = w * kSlotsPerWarp + R.s;
-    if (!mbar_wait(&ms->full[slot], R.phase, kWaitLimit)) {
+    if (!mbar_wait_parked(&ms->full[slot], R.phase)) {
       if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
       if (!routed) named_bar(2, kConsumers);
       break;

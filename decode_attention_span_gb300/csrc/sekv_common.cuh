@@ -120,6 +120,38 @@ __device__ __forceinline__ uint32_t mbar_test4(uint32_t a0, uint32_t a1, uint32_
   return m;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One phase test that may suspend the warp until the phase completes or
+// about hint_ns nanoseconds pass, whichever is first.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait in which the hardware parks the warp instead of a polling loop
+// (no shared-memory traffic while it waits); returns false after about two
+// seconds (the caller flags an error).
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if ((i & 15u) == 15u && globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
 // Bounded wait: returns false after `limit` polls (the caller flags an error).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i) {
