@@ -161,7 +161,23 @@ sekv_status sekv_workspace_init(void* workspace, size_t bytes, cudaStream_t stre
 
 /* Synchronise `stream`, copy the workspace's device status into *code and
  * *detail (either may be NULL) and clear it.  Returns SEKV_OK when the GPU
- * flagged nothing, SEKV_ERR_DEVICE or SEKV_ERR_TIMEOUT when it did. */
+ * flagged nothing, SEKV_ERR_DEVICE or SEKV_ERR_TIMEOUT when it did.  The
+ * first error of a call wins:
+ *   code 1  bad input: an expansion list not ascending, out of range or
+ *           naming an empty body (detail: the list position, or the
+ *           (sequence, KV head) whose count is out of range), or a build
+ *           that found more spans than max_spans (detail: the sequence);
+ *   code 2  a bounded wait ran out (SEKV_ERR_TIMEOUT; detail: which wait --
+ *           1 producer waiting for a consumer slot, 2 publication of the other
+ *           CTAs' routing, 3 copies landing before exit, 4 consumer waiting for
+ *           a page, 5 routing weights landing, 6 producer looking for a free
+ *           consumer slot, 7 partials landing in the merge, 8 a warp finishing
+ *           a record handed over to it);
+ *   code 3  the records do not fit: a fetch group's records exceed its
+ *           staging share (detail: the group), or a build's records exceed
+ *           the store (detail: the bytes needed, in MiB);
+ *   code 4  a record rank above what the kernel handles (detail: the rank; the
+ *           record is skipped). */
 sekv_status sekv_workspace_status(void* workspace, cudaStream_t stream,
                                   int32_t* code, int32_t* detail);
 
