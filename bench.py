@@ -49,8 +49,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--path", default="decode", choices=["decode", "build"],
-                    help="decode: the headline decode step; build: the prefill cache build")
+    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv"],
+                    help="decode: the headline decode step; build: the prefill cache build; "
+                         "fullkv: the same decode step over a full-KV cache (comparator)")
     return ap.parse_args()
 
 
@@ -579,11 +580,72 @@ def run_build_bench(args, ws_n, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_fullkv_bench(args, ws_n, rank, local):
+    """Full-KV comparator at the headline shape: the same decode step over a
+    cache with no spans, every one of the 128K context tokens a full-resolution
+    row (n_sink = 0, n_recent = T), so one step is plain softmax attention over
+    all tokens in every layer.  Layers hold distinct caches (16 GB), so every
+    step streams from HBM."""
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (fullkv) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.get_config(args.config)
+    if args.layers:
+        w = synth.get_config(args.config, layers=args.layers)
+    T = w.ctx
+    layers = []
+    for l in range(w.layers):
+        d = gen.full_kv_cache(w, l, T, device=dev)
+        g = gen._gen(w.seed * 7919 + 101 * l + 1, dev)
+        q = gen.query(g, w.batch, w.n_q_heads, dev)
+        layers.append(dict(cache=sk.LayerCache({k: v for k, v in d.items()
+                                                 if isinstance(v, torch.Tensor)}),
+                           t=d, q=q, W=gen.routing_weights(g, w.n_kv_heads, dev).contiguous(),
+                           theta=torch.zeros(w.n_q_heads, device=dev),
+                           out=torch.empty(w.batch, w.n_q_heads, 128, device=dev),
+                           lse=torch.empty(w.batch, w.n_q_heads, device=dev)))
+    cfg = sk.Config(w.batch, w.n_q_heads, w.n_kv_heads, 0, T, layers[0]["t"]["max_spans"],
+                    w.rank_cap, w.len_min, w.len_max, w.tau,
+                    flags=sk.sekv.FLAG_OVERLAP_PREVIOUS)
+    ws = sk.Workspace(cfg, dev)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    ms_total, ck = run_resident(sk, cfg, ws, layers, args.steps, args.warmup, ws_n, clocks)
+    ms_total = max_over_ranks(ms_total, ws_n)
+    launch_s = ms_total / 1e3 / args.steps / w.layers
+    per_launch = float(w.batch * w.n_kv_heads * T * 2 * 128 * 2)  # K and V rows, bf16
+    peak, peak_kind = measured_peaks()
+    achieved = per_launch / launch_s / 1e9
+    if rank != 0:
+        return
+    line = {"metric": "full-KV decode steps/s at 128K ctx (comparator: every token a "
+                      "full-resolution row)",
+            "value": whole_job_rate(args.steps, ms_total, ws_n), "unit": "steps/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name + "_fullkv", "layers": w.layers, "batch": w.batch,
+                       "ctx": T, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                       "l2": "inputs larger than L2 (distinct caches per layer)",
+                       "graph": "one CUDA graph per step, programmatic dependent launch"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "sekv::decode_kernel", "bytes_per_launch": per_launch,
+                         "avg_launch_us": launch_s * 1e6},
+            "clocks": ck, "gpu_launches": args.steps * w.layers}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws_n, rank, local = dist_setup(args)
     if args.path == "build":
         run_build_bench(args, ws_n, rank, local)
+        return
+    if args.path == "fullkv":
+        run_fullkv_bench(args, ws_n, rank, local)
         return
     w = synth.get_config(args.config)
     if args.layers:

@@ -420,6 +420,37 @@ def decode_cache(cfg: WorkloadConfig, layer: int, device="cpu",
                 max_spans=max_spans, lens=lens)
 
 
+def full_kv_cache(cfg: WorkloadConfig, layer: int, T: int, device="cpu",
+                  max_spans: int = 64) -> Dict[str, torch.Tensor]:
+    """One layer of a full-KV cache in the C-ABI layout: no spans, every one of
+    the T context tokens a full-resolution row.
+
+    The decode step over such a cache (configured with n_sink = 0 and
+    n_recent = T) is plain softmax attention over all T tokens, the full-KV
+    decode that SeKV is compared with.  Rows ~ N(0,1) in bf16, like the
+    full-resolution rows of ``decode_cache``; the span arrays are zero and the
+    basis store is a zero stub.
+    """
+    B, Hkv = cfg.batch, cfg.n_kv_heads
+    cap = max_spans + T
+    gen = _gen(cfg.seed * 15485863 + layer * 101 + 17, device)
+    k_full = torch.zeros(B, Hkv, cap, HEAD_DIM, dtype=torch.bfloat16, device=device)
+    v_full = torch.zeros_like(k_full)
+    for b in range(B):
+        k_full[b, :, :T] = torch.randn(Hkv, T, HEAD_DIM, generator=gen, device=device).to(torch.bfloat16)
+        v_full[b, :, :T] = torch.randn(Hkv, T, HEAD_DIM, generator=gen, device=device).to(torch.bfloat16)
+    z = dict(device=device)
+    return dict(n_spans=torch.zeros(B, dtype=torch.int32, **z),
+                body_len=torch.zeros(B, max_spans, dtype=torch.int32, **z),
+                k_full=k_full, v_full=v_full,
+                s_route=torch.zeros(B, Hkv, max_spans, ROUTE_DIM, dtype=torch.float32, **z),
+                k_sum=torch.zeros(B, Hkv, max_spans, HEAD_DIM, dtype=torch.bfloat16, **z),
+                v_sum=torch.zeros(B, Hkv, max_spans, HEAD_DIM, dtype=torch.bfloat16, **z),
+                rec_off=torch.zeros(B, Hkv, max_spans, dtype=torch.int64, **z),
+                rec_rank=torch.zeros(B, Hkv, max_spans, dtype=torch.int32, **z),
+                store=torch.zeros(256, dtype=torch.uint8, **z), max_spans=max_spans)
+
+
 def abi_to_numpy(d: Dict[str, object]) -> Dict[str, np.ndarray]:
     """numpy copies of ABI tensors (bfloat16 as uint16 bit patterns)."""
     out = {}
