@@ -18,8 +18,9 @@ size_t ws_cta_bytes(const WsLayout& L);
 void count_launch(int n);
 void reset_launches();
 
-// 3-D tiled tensor map over [d2][d1][d0] elements of `elem_bytes` each,
-// dense rows, box {box0, box1, 1}, 128-byte swizzle, zero fill out of range.
+// Rows of row_elems elements ([groups][rows][row_elems], dense) seen as
+// (x: half a row, row, half, group): a box of box_rows rows brings both
+// 128-byte halves of each row in one copy, 128-byte swizzle.
 bool encode_rows4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                    uint64_t row_elems, uint64_t rows, uint64_t groups, int elem_bytes,
                    uint32_t box_rows);
