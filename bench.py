@@ -641,6 +641,11 @@ def run_fullkv_bench(args, ws_n, rank, local):
 def main():
     args = parse()
     ws_n, rank, local = dist_setup(args)
+    if args.impl == "reference" and args.path != "decode":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm (the oracle) "
+                              "is timed on the decode path only"}), flush=True)
+        return
     if args.path == "build":
         run_build_bench(args, ws_n, rank, local)
         return

@@ -61,3 +61,16 @@ def test_whole_job_rate_counts_every_replica():
     # 2 ranks x 100 steps in 50 ms (slowest rank) -> 4000 steps/s for the job
     assert bench.whole_job_rate(100, 50.0, 2) == pytest.approx(4000.0)
     assert bench.whole_job_rate(100, 50.0, 1) == pytest.approx(2000.0)
+
+
+def test_reference_arm_is_decode_only():
+    """The reference arm times the oracle on the decode path; other paths say
+    so on one JSON line instead of timing this library's kernels."""
+    import json
+    import subprocess
+    for path in ("build", "fullkv"):
+        r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--path", path],
+                           capture_output=True, text=True, timeout=300, cwd=ROOT)
+        assert r.returncode == 0, r.stderr
+        line = json.loads(r.stdout.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and "unavailable" in line
