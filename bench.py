@@ -110,19 +110,20 @@ def decode_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic():
+def profiled_traffic(workload: str):
     """DRAM bytes per decode launch from the committed ncu summary, or None
-    when the kernel sources changed since it was taken."""
+    when the kernel sources changed since it was taken or the summary covers
+    another workload."""
     try:
         text = open(DECODE_PROFILE, encoding="utf-8").read()
     except OSError:
         return None
     vals = {}
     for line in text.splitlines():
-        for key in ("source-sha256:", "traffic-bytes-per-launch:"):
+        for key in ("source-sha256:", "traffic-bytes-per-launch:", "Workload:"):
             if line.strip().startswith(key):
-                vals[key] = line.split(":", 1)[1].strip().strip("`")
-    if vals.get("source-sha256:") != decode_source_hash():
+                vals[key] = line.split(":", 1)[1].strip(" `:")
+    if vals.get("Workload:") != workload or vals.get("source-sha256:") != decode_source_hash():
         return None
     try:
         return int(vals["traffic-bytes-per-launch:"])
@@ -688,7 +689,7 @@ def main():
                        "parallelism": f"replicas x{ws_n}",
                        "graph": "one CUDA graph per step, programmatic dependent launch"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                          "peak_kind": peak_kind, "kernel": "sekv::decode_kernel",
                          "bytes_per_launch": per_launch,
                          "avg_launch_us": launch_s * 1e6},

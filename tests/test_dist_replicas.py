@@ -74,3 +74,13 @@ def test_reference_arm_is_decode_only():
         assert r.returncode == 0, r.stderr
         line = json.loads(r.stdout.strip().splitlines()[-1])
         assert line["impl"] == "reference" and "unavailable" in line
+
+
+def test_profiled_traffic_covers_its_own_workload_only():
+    """The committed ncu summary's DRAM bytes are reported only for the
+    workload it was taken on (and only while the kernel sources match)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.profiled_traffic("qwen2_7b_stress") is None
+    t = bench.profiled_traffic("llama3_8b_128k")
+    assert t is None or (isinstance(t, int) and t > 0)
