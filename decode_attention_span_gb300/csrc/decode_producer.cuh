@@ -26,10 +26,6 @@ __device__ __forceinline__ uint32_t ring_phase(const ProdState& S, int w) {
   return (S.rs >> (2 * w + 1)) & 1u;
 }
 
-__device__ __forceinline__ bool slot_free(SmemMisc* ms, const ProdState& S, int w) {
-  return mbar_test_wait(&ms->empty[ring_slot(S, w)], ring_phase(S, w) ^ 1u);
-}
-
 // Bit w set iff warp w's next slot is free (the four tests overlap).
 __device__ __forceinline__ uint32_t free_warps(SmemMisc* ms, const ProdState& S) {
   const uint32_t e0 = smem_u32(&ms->empty[0]);

@@ -201,26 +201,6 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       : "memory");
 }
 
-__device__ __forceinline__ void tma_g2s_3d_hint(void* dst, const CUtensorMap* map, int x, int y,
-                                                int z, uint64_t* bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
-      "l"(pol)
-      : "memory");
-}
-
-// 3-D tiled tensor copy global -> shared (box given by the tensor map)
-__device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, int x, int y,
-                                           int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 4-D tiled tensor copy global -> shared with an L2 cache hint.
 __device__ __forceinline__ void tma_g2s_4d_hint(void* dst, const CUtensorMap* map, int x, int y,
                                                 int z, int w, uint64_t* bar, uint64_t pol) {
@@ -261,17 +241,6 @@ __device__ __forceinline__ void mma_bf16_rows8(float& d0, float& d1, uint32_t a0
       " {%8,%9}, {%0,%1,%10,%11};"
       : "+f"(d0), "+f"(d1), "=f"(z2), "=f"(z3)
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f));
-}
-
-// Full m16n8k16 bf16 mma, fp32 accumulate in place.
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
-      " {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
