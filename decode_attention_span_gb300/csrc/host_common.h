@@ -24,10 +24,6 @@ void reset_launches();
 bool encode_rows4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                    uint64_t row_elems, uint64_t rows, uint64_t groups, int elem_bytes,
                    uint32_t box_rows);
-// 3-D tiled tensor map over [d2][d1][d0] elements of `elem_bytes` each,
-// dense rows, box {box0, box1, 1}, 128-byte swizzle, zero fill out of range.
-bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
-               uint64_t d1, uint64_t d2, int elem_bytes, uint32_t box0, uint32_t box1);
 
 size_t build_workspace_size(const sekv_config* cfg, int64_t ctx_len);
 

@@ -126,20 +126,6 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
-bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
-               uint64_t d1, uint64_t d2, int elem_bytes, uint32_t box0, uint32_t box1) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || !base) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
-  const cuuint32_t box[3] = {box0, box1, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Rows of `row_elems` elements as a 4-D tensor (half-row, row, half, group)
 // so that one box of `box_rows` rows brings both 128-byte halves of each
 // row: in shared memory the first halves of the box's rows come first, then
