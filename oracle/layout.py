@@ -166,9 +166,11 @@ def pack_layer(cache: LayerCache, max_spans: int) -> Dict[str, np.ndarray]:
 
 
 def unpack_layer(arrs: Dict[str, np.ndarray], n_sink: int, n_recent: int,
-                 groups=None) -> LayerCache:
+                 groups=None, records: bool = True) -> LayerCache:
     """Logical cache from ABI arrays.  ``groups``: optional set of (b, c) to
-    decode fully; the others get empty per-head lists (for sampled checks)."""
+    decode fully; the others get empty per-head lists (for sampled checks).
+    ``records=False`` leaves every span's factors as None (routing needs no
+    basis records; it saves unpacking them)."""
     n_spans = np.asarray(arrs["n_spans"])
     B = n_spans.shape[0]
     Hkv = arrs["k_full"].shape[1]
@@ -193,7 +195,7 @@ def unpack_layer(arrs: Dict[str, np.ndarray], n_sink: int, n_recent: int,
             vs.append(bits_bf16(arrs["v_sum"][b, c, :ns]))
             row: List[Optional[SpanFactors]] = []
             for k in range(ns):
-                if body[k] <= 0:
+                if body[k] <= 0 or not records:
                     row.append(None)
                     continue
                 F = unpack_record(store, int(arrs["rec_off"][b, c, k]), int(body[k]))
