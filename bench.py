@@ -94,9 +94,9 @@ def max_over_ranks(x: float, ws: int) -> float:
 # peaks and clocks
 # ----------------------------------------------------------------------------
 
-DECODE_SOURCES = ("decode_attn.cuh", "decode_consumer.cuh", "decode_producer.cuh",
-                  "decode_kernel_impl.cuh", "decode_ks1.cu", "decode_ks2.cu", "decode_ks3.cu",
-                  "decode_ks4.cu", "sekv_common.cuh")
+DECODE_SOURCES = ("decode_attn.cuh", "decode_consumer.cuh", "decode_kernel_impl.cuh",
+                  "decode_ks1.cu", "decode_ks2.cu", "decode_ks3.cu", "decode_ks4.cu",
+                  "sekv_common.cuh")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_kernel_llama3_8b_128k.md")
 
 

@@ -91,130 +91,100 @@ __device__ __forceinline__ float rebase_if_needed(WarpAcc& A, float mx) {
   return alpha;
 }
 
-// One full-resolution or summary page: up to 32 rows whose 32-row boxes are
-// 128B-swizzled (keys for dims 0-63 at kb, 64-127 at kb + kBoxBytes; values
-// likewise at vb), folded into the warp's softmax state with one rescale.
-// bias_row: for summary pages the logit bias of the page's spans (log2|S|, or
-// -inf for a span that does not enter as a summary); nullptr for full rows.
-// Rows >= n are masked.
-__device__ __forceinline__ void consume_kv_page(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
-                                                const float* bias_row, float scale_log2) {
+// One full-resolution or summary page: up to kRows (16) rows whose two
+// 128-byte halves are 128B-swizzled boxes (keys: dims 0-63 at kb, 64-127 at
+// kb + kRowHalf; values likewise at vb), folded into the warp's softmax state
+// with at most one rescale.  bias_row: for summary pages the logit bias of
+// the page's spans (log2|S|, or -inf for a span that does not enter as a
+// summary); nullptr for full rows.  Rows >= n are masked.
+__device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
+                                               const float* bias_row, float scale_log2) {
   const int lane = threadIdx.x & 31;
-  float s[2][2][2];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) s[hh][nt][0] = s[hh][nt][1] = 0.f;
+  float s[2][2];
+  s[0][0] = s[0][1] = s[1][0] = s[1][1] = 0.f;
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {  // 32 head dims per step
     const uint4 q = lds128(A.qfrag + (i * 32 + lane) * 16);
-    const uint32_t box = kb + (i >> 1) * kBoxBytes;
+    const uint32_t box = kb + (i >> 1) * kRowHalf;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz128(box, 16 * hh + 8 * nt + (lane & 7), (i & 1) * 4 + (lane >> 3)), b0, b1,
-                b2, b3);
-        mma_bf16_rows8(s[hh][nt][0], s[hh][nt][1], q.x, q.y, b0, b1);
-        mma_bf16_rows8(s[hh][nt][0], s[hh][nt][1], q.z, q.w, b2, b3);
-      }
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(swz128(box, 8 * nt + (lane & 7), (i & 1) * 4 + (lane >> 3)), b0, b1, b2, b3);
+      mma_bf16_rows8(s[nt][0], s[nt][1], q.x, q.y, b0, b1);
+      mma_bf16_rows8(s[nt][0], s[nt][1], q.z, q.w, b2, b3);
     }
   }
   float mx = kNegInf;
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = 16 * hh + 8 * nt + 2 * (lane & 3) + e;
-        bool valid = key < n;
-        float bias = 0.f;
-        if (bias_row != nullptr && valid) {
-          bias = bias_row[key];
-          valid = bias != kNegInf;
-        }
-        s[hh][nt][e] = valid ? fmaf(s[hh][nt][e], scale_log2, bias) : kNegInf;
-        mx = fmaxf(mx, s[hh][nt][e]);
+    for (int e = 0; e < 2; ++e) {
+      const int key = 8 * nt + 2 * (lane & 3) + e;
+      bool valid = key < n;
+      float bias = 0.f;
+      if (bias_row != nullptr && valid) {
+        bias = bias_row[key];
+        valid = bias != kNegInf;
       }
+      s[nt][e] = valid ? fmaf(s[nt][e], scale_log2, bias) : kNegInf;
+      mx = fmaxf(mx, s[nt][e]);
+    }
   rebase_if_needed(A, mx);
   const float msub = A.m_row == kNegInf ? 0.f : A.m_row;
-  float ps = 0.f;
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s[hh][nt][e] = ex2_approx(s[hh][nt][e] - msub);
-        ps += s[hh][nt][e];
-      }
-  A.l_part += ps;
+    for (int e = 0; e < 2; ++e) s[nt][e] = ex2_approx(s[nt][e] - msub);
+  A.l_part += (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
   const int mi = lane >> 3;
+  const uint32_t a0 = pack_bf16(s[0][0], s[0][1]);
+  const uint32_t a2 = pack_bf16(s[1][0], s[1][1]);
+  // value rows past n (zero fill or unrelated rows) must not reach o
+  const int kt = 2 * (lane & 3);
+  const uint32_t t0 = (kt < n ? 0xffffu : 0u) | (kt + 1 < n ? 0xffff0000u : 0u);
+  const uint32_t t1 = (kt + 8 < n ? 0xffffu : 0u) | (kt + 9 < n ? 0xffff0000u : 0u);
+  const int key = 8 * (mi & 1) + (lane & 7);
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint32_t a0 = pack_bf16(s[hh][0][0], s[hh][0][1]);
-    const uint32_t a2 = pack_bf16(s[hh][1][0], s[hh][1][1]);
-    // value rows past n (zero fill or unrelated rows) must not reach o
-    const int kt = 16 * hh + 2 * (lane & 3);
-    const uint32_t t0 = (kt < n ? 0xffffu : 0u) | (kt + 1 < n ? 0xffff0000u : 0u);
-    const uint32_t t1 = (kt + 8 < n ? 0xffffu : 0u) | (kt + 9 < n ? 0xffff0000u : 0u);
-    const int key = 16 * hh + 8 * (mi & 1) + (lane & 7);
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      const int d0 = 16 * dp;
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(swz128(vb + (d0 >> 6) * kBoxBytes, key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1,
-                b2, b3);
-      b0 &= t0; b2 &= t0; b1 &= t1; b3 &= t1;
-      mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], a0, a2, b0, b1);
-      mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], a0, a2, b2, b3);
-    }
+  for (int dp = 0; dp < 8; ++dp) {
+    const int d0 = 16 * dp;
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(swz128(vb + (d0 >> 6) * kRowHalf, key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1, b2,
+              b3);
+    b0 &= t0; b2 &= t0; b1 &= t1; b3 &= t1;
+    mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], a0, a2, b0, b1);
+    mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], a0, a2, b2, b3);
   }
 }
 
-
 // Routing logits z[span][head] = s_span . y_head of a routing page (two
-// 128B-swizzled boxes of 64 rows x 32 floats) in fp32 FMAs: lane l takes the
-// spans l and l + 32, four heads per pass (y rows past the group are zero and
-// ignored).  Each 16-byte chunk of a row sits at chunk ^ (row & 7), so the
-// eight lanes of a quarter-warp read eight different bank groups; the y
-// chunks are broadcasts.  Rows past the page's spans are computed and ignored
-// by the caller.  Returns the 64-bit mask of spans with z > theta for some
-// head of the group.
-__device__ __forceinline__ unsigned long long route_hits(const uint8_t* page, const float* ys,
-                                                        const float* theta, int G) {
+// 128B-swizzled boxes of 32 rows x 32 floats: routing dims 0-31, then 32-63)
+// in fp32 FMAs, lane l taking span l, four heads per pass (y rows past the
+// group are zero and ignored).  Chunk c of a row sits at c ^ (row & 7), so
+// eight lanes read eight different bank groups; the y reads are broadcasts.
+// Returns whether some head h of the group has z > theta_h for this lane's
+// span (rows past the page's spans are computed and ignored by the caller).
+__device__ __forceinline__ bool route32(const uint8_t* page, const float* ys, const float* theta,
+                                        int G) {
   const int lane = threadIdx.x & 31, sw = lane & 7;
-  bool hit0 = false, hit1 = false;
+  bool hit = false;
 #pragma unroll 1
   for (int h0 = 0; h0 < G; h0 += 4) {
-    float z[2][4];
-#pragma unroll
-    for (int hh = 0; hh < 4; ++hh) z[0][hh] = z[1][hh] = 0.f;
-#pragma unroll 2
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int c = 0; c < 16; ++c) {  // routing dims 4c .. 4c + 3
-      const uint8_t* rowc = page + (c >> 3) * 8192 + lane * 128 + (((c & 7) ^ sw) << 4);
-      const float4 s0 = *reinterpret_cast<const float4*>(rowc);
-      const float4 s1 = *reinterpret_cast<const float4*>(rowc + 32 * 128);
+      const float4 s = *reinterpret_cast<const float4*>(page + (c >> 3) * 4096 + lane * 128 +
+                                                        (((c & 7) ^ sw) << 4));
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
         const float4 y = *reinterpret_cast<const float4*>(ys + (h0 + hh) * kRouteDim + 4 * c);
-        z[0][hh] = fmaf(s0.w, y.w, fmaf(s0.z, y.z, fmaf(s0.y, y.y, fmaf(s0.x, y.x, z[0][hh]))));
-        z[1][hh] = fmaf(s1.w, y.w, fmaf(s1.z, y.z, fmaf(s1.y, y.y, fmaf(s1.x, y.x, z[1][hh]))));
+        z[hh] = fmaf(s.w, y.w, fmaf(s.z, y.z, fmaf(s.y, y.y, fmaf(s.x, y.x, z[hh]))));
       }
     }
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-      if (h0 + hh < G) {
-        const float th = theta[h0 + hh];
-        hit0 |= z[0][hh] > th;
-        hit1 |= z[1][hh] > th;
-      }
-    }
+    for (int hh = 0; hh < 4; ++hh)
+      if (h0 + hh < G) hit |= z[hh] > theta[h0 + hh];
   }
-  return (unsigned long long)__ballot_sync(0xffffffffu, hit0) |
-         ((unsigned long long)__ballot_sync(0xffffffffu, hit1) << 32);
+  return hit;
 }
 
 // ---------------------------------------------------------------------------

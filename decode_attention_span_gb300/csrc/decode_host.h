@@ -11,7 +11,6 @@ bool aligned16(const void* p);
 sekv_status check_cache(const sekv_config* cfg, const sekv_layer_cache* c, bool need_store);
 sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* cache,
                                const WsLayout& L, void* ws, DecodeParams& P, bool fused);
-sekv_status encode_wr(DecodeParams& P, const float* W_r, const sekv_config* cfg);
 sekv_status launch_decode(const DecodeParams& P, const WsLayout& L, const sekv_config* cfg,
                           cudaStream_t stream, bool overlap);
 

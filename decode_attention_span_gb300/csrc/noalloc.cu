@@ -74,8 +74,6 @@ extern "C" sekv_status sekv_decode_step_noalloc(const sekv_config* cfg,
   P.store = static_cast<const uint8_t*>(cache->store);
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.W_r = W_r;
-  st = encode_wr(P, W_r, cfg);
-  if (st != SEKV_OK) return st;
   P.theta = theta;
   P.out = out;
   P.lse = lse;

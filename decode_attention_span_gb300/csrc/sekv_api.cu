@@ -62,14 +62,28 @@ int device_sm_count() {
   return cached[dev];
 }
 
-// CTAs per (sequence, KV head) of the decode kernel.
+// CTAs per (sequence, KV head) group of the decode kernel.  CTAs never wait
+// for one another, so the grid may take several waves; cg is picked so that
+// the last wave is as full as possible (1 to 4 waves of one CTA per SM, the
+// fewest waves among the best fills), and large enough that every CTA's span
+// share fits its shared-memory caches.
 int decode_cg(const sekv_config* cfg, int sms) {
   const int ng = cfg->batch * cfg->n_kv_heads;
-  int cg = sms / ng;
-  if (cg < 1) cg = 1;
-  // every CTA's span slice must fit the shared-memory span-info cache
-  while (cg < kMaxCgSmem && cfg->max_spans / cg + 16 > kInfoCap) ++cg;
-  return cg > kMaxCgSmem ? kMaxCgSmem : cg;
+  int best = 1;
+  double best_fill = -1.0;
+  for (int waves = 1; waves <= 4; ++waves) {
+    int cg = waves * sms / ng;
+    if (cg < 1) cg = 1;
+    const long long ctas = (long long)ng * cg;
+    const long long slots = (ctas + sms - 1) / sms * sms;
+    const double fill = double(ctas) / double(slots);
+    if (fill > best_fill + 0.02) {
+      best_fill = fill;
+      best = cg;
+    }
+  }
+  while (best < kMaxCg && cfg->max_spans / best + 8 > kSpanCap) ++best;
+  return best > kMaxCg ? kMaxCg : best;
 }
 
 int route_chunks(const sekv_config* cfg) { return (cfg->max_spans + kRouteChunk - 1) / kRouteChunk; }
@@ -84,19 +98,13 @@ WsLayout ws_layout(const sekv_config* cfg, int sms) {
   L.status = off;     off += align256(64);
   L.groups = off;     off += align256(ng * sizeof(GroupState));
   L.cta_n = off;      off += align256(ng * L.cg * 4);
-  L.entries = off;    off += align256(ng * ms * sizeof(ExpEntry));
-  L.info = off;       off += align256(ng * ms * 2);
+  L.cta_list = off;   off += align256(ng * ms * 4);
   L.partials = off;   off += align256(ng * L.cg * sizeof(Partial));
   L.route_list = off; off += align256(ng * ms * 4);
   L.route_cnt = off;  off += align256(ng * L.route_chunks * 4);
-  L.pmask = off;      off += align256(ng * L.cg * kMaxRoutePages * 8);
-  L.pbytes = off;     off += align256(ng * L.cg * kMaxRoutePages * 8);
-  // cta_bytes lives after pbytes
-  L.total = off + align256(ng * L.cg * 8);
+  L.total = off;
   return L;
 }
-
-size_t ws_cta_bytes(const WsLayout& L) { return L.total - align256(size_t(L.ng) * L.cg * 8); }
 
 void count_launch(int n) { g_launches += n; }
 void reset_launches() { g_launches = 0; }
@@ -224,10 +232,10 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   const int ng = L.ng;
   const uint64_t cap_full = uint64_t(cfg->n_sink) + cfg->max_spans + cfg->n_recent;
   bool ok = true;
-  ok &= encode_rows4d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, kTileRows);
-  ok &= encode_rows4d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, kTileRows);
-  ok &= encode_rows4d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, kTileRows);
-  ok &= encode_rows4d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, kTileRows);
+  ok &= encode_rows4d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, kRows);
+  ok &= encode_rows4d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, kRows);
+  ok &= encode_rows4d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, kRows);
+  ok &= encode_rows4d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, kRows);
   if (fused) {
     ok &= encode_rows4d(&P.tm_sroute, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cache->s_route, 64, cfg->max_spans, ng, 4, kRouteSpans);
   } else {
@@ -242,11 +250,7 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.status = reinterpret_cast<int32_t*>(w + L.status);
   P.groups = reinterpret_cast<GroupState*>(w + L.groups);
   P.cta_n = reinterpret_cast<int32_t*>(w + L.cta_n);
-  P.cta_bytes = reinterpret_cast<int64_t*>(w + ws_cta_bytes(L));
-  P.entries = reinterpret_cast<ExpEntry*>(w + L.entries);
-  P.info = reinterpret_cast<const uint16_t*>(w + L.info);
-  P.pmask = reinterpret_cast<uint64_t*>(w + L.pmask);
-  P.pbytes = reinterpret_cast<int64_t*>(w + L.pbytes);
+  P.cta_list = reinterpret_cast<int32_t*>(w + L.cta_list);
   P.partials = reinterpret_cast<Partial*>(w + L.partials);
   P.B = cfg->batch;
   P.Hq = cfg->n_q_heads;
@@ -255,28 +259,9 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.n_sink = cfg->n_sink;
   P.n_recent = cfg->n_recent;
   P.max_spans = cfg->max_spans;
-  P.cap_full = int(cap_full);
   P.cg = L.cg;
   P.fused = fused ? 1 : 0;
   return SEKV_OK;
-}
-
-// W_r [Hkv][64][128] fp32 as a tensor of boxes of 64 rows x 32 floats (128B swizzle)
-sekv_status encode_wr(DecodeParams& P, const float* W_r, const sekv_config* cfg) {
-  // W_r [Hkv][64][128] fp32 as (32 floats, row, quarter, head): one box of
-  // 64 rows x 4 quarters brings a head's 32 KB in one copy, laid out in
-  // shared memory as four 128B-swizzled blocks of 64 rows x 32 floats
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || !W_r) return SEKV_ERR_CUDA;
-  const cuuint64_t dims[4] = {32, uint64_t(kRouteDim), 4, uint64_t(cfg->n_kv_heads)};
-  const cuuint64_t strides[3] = {kHeadDim * 4, 32 * 4, uint64_t(kRouteDim) * kHeadDim * 4};
-  const cuuint32_t box[4] = {32, uint32_t(kRouteDim), 4, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(&P.tm_wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(W_r), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-             ? SEKV_OK
-             : SEKV_ERR_CUDA;
 }
 
 // Rank k-steps of 16 the kernel instance needs for this configuration.
@@ -316,34 +301,6 @@ sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_
   return SEKV_OK;
 }
 
-sekv_status launch_prep(const sekv_config* cfg, const sekv_layer_cache* cache,
-                        const int32_t* expanded, const int32_t* n_expanded,
-                        const int64_t* staged_off, const WsLayout& L, void* ws,
-                        cudaStream_t stream) {
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  PrepParams pp;
-  pp.n_spans = cache->n_spans;
-  pp.body_len = cache->body_len;
-  pp.rec_off = cache->rec_off;
-  pp.rec_rank = cache->rec_rank;
-  pp.expanded = expanded;
-  pp.n_expanded = n_expanded;
-  pp.staged_off = staged_off;
-  pp.status = reinterpret_cast<int32_t*>(w + L.status);
-  pp.groups = reinterpret_cast<GroupState*>(w + L.groups);
-  pp.cta_n = reinterpret_cast<int32_t*>(w + L.cta_n);
-  pp.cta_bytes = reinterpret_cast<int64_t*>(w + ws_cta_bytes(L));
-  pp.entries = reinterpret_cast<ExpEntry*>(w + L.entries);
-  pp.info = reinterpret_cast<uint16_t*>(w + L.info);
-  pp.Hkv = cfg->n_kv_heads;
-  pp.max_spans = cfg->max_spans;
-  pp.cg = L.cg;
-  prep_list_kernel<<<L.ng, 256, 0, stream>>>(pp);
-  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
-  count_launch(1);
-  return SEKV_OK;
-}
-
 }  // namespace sekv
 
 extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
@@ -370,8 +327,6 @@ extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer
   P.store = static_cast<const uint8_t*>(cache->store);
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.W_r = W_r;
-  st = encode_wr(P, W_r, cfg);
-  if (st != SEKV_OK) return st;
   P.theta = theta;
   P.out = out;
   P.lse = lse;
@@ -410,10 +365,10 @@ extern "C" sekv_status sekv_decode_attention(const sekv_config* cfg,
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.out = out;
   P.lse = lse;
+  P.list = expanded;
+  P.list_n = n_expanded;
+  P.staged_off = staged_off;
   P.scale_log2 = scale * kLog2e;
-  // prepare span info and entries from the list
-  st = launch_prep(cfg, cache, expanded, n_expanded, staged_off, L, workspace, stream);
-  if (st != SEKV_OK) return st;
   return launch_decode(P, L, cfg, stream, false);
 }
 

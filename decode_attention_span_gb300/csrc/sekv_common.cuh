@@ -30,19 +30,9 @@ enum DeviceError : int32_t {
 // workspace layout (bytes, all offsets 256-aligned)
 // ----------------------------------------------------------------------------
 struct GroupState {        // one per (sequence, KV head); zero between calls
-  int32_t published;       // CTAs that have published their expansion entries
-  int32_t done;            // CTAs that have written their partial
+  int32_t done;            // decode: CTAs that have written their partial
   int32_t route_done;      // route kernel: chunks finished
-  int32_t pad;
-};
-
-struct ExpEntry {          // one expanded span, 32 bytes
-  int32_t k;               // span ordinal
-  int32_t body;            // |S|
-  int32_t rank;            // rK | rV << 16
-  int32_t pad;
-  int64_t off;             // byte offset of its record (store or staging)
-  int64_t pad2;
+  int32_t pad[2];
 };
 
 struct Partial {           // one CTA's softmax state for up to 8 heads
@@ -52,8 +42,7 @@ struct Partial {           // one CTA's softmax state for up to 8 heads
 };
 
 struct WsLayout {
-  size_t status, groups, cta_n, entries, info, partials, route_list, route_cnt, pmask, pbytes,
-      total;
+  size_t status, groups, cta_n, cta_list, partials, route_list, route_cnt, total;
   int ng, cg, route_chunks;
 };
 
