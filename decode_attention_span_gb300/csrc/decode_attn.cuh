@@ -10,18 +10,21 @@
 // w = U_V^T p and o += Vt_V^T diag(sigma g) w; khat/vhat are never formed.
 //
 // Structure.  Grid (cg, Hkv, B): CTA j of a (sequence, KV head) group owns
-// an equal share of its full-resolution rows and of its spans.  Everything a
-// CTA needs besides the query is local to that share: it routes its own
-// spans, attends their summaries, and rebuilds the expanded ones among them,
-// so CTAs never wait for one another (the last CTA of a group to finish
-// merges the group's partial softmax states).
+// an equal share of the group's spans.  It routes them, attends their
+// summaries and rebuilds the expanded ones among them, so no CTA waits for
+// another's routing.  Full-resolution rows (sinks, anchors, recent) need no
+// routing: each CTA takes kStaticPages pages of them as its own, and the
+// rest form a pool of the group from which CTAs take pages while they have
+// nothing else to do, which evens out the CTAs' unequal record loads (the
+// last CTA of a group to finish merges the group's partial softmax states).
 //
 // Eight warps per CTA, each its own producer and consumer: a warp owns a
-// 24 KB arena of shared memory, claims work items from the CTA's two queues
-// (expanded records first, then fixed pages: full-resolution rows, then
-// summary rows), lands them in its arena with TMA (tensor copies with 128B
-// swizzle for row and routing pages, 1-D bulk copies for basis records), and
-// consumes them in issue order, keeping up to kMaxItems in flight.  Each
+// 24 KB arena of shared memory, claims work items (expanded records first,
+// then the CTA's own pages: full-resolution rows, then summary rows, then
+// pages from the group's pool), lands them in its arena with TMA (tensor
+// copies with 128B swizzle for row and routing pages, 1-D bulk copies for
+// basis records), and consumes them in issue order, keeping up to kMaxItems
+// in flight.  Each
 // warp keeps its own online-softmax state (query heads of the GQA group as
 // the M rows of mma.sync; keys, tokens or ranks as N); the eight states and
 // then the CTAs' states are merged at the end.
@@ -47,6 +50,10 @@ constexpr int kMaxRoutePages = kSpanCap / kRouteSpans;
 constexpr int kWholeMax = 16384;              // records up to this size land whole
 constexpr int kTileMax = 12288;               // U-row tiles of larger records
 constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) group
+constexpr int kStaticPages = 2;               // full-resolution pages each CTA owns
+constexpr int kPoolClaim = 2;                 // pages per claim from the group's pool
+constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
+constexpr int kPrologueItems = 2;             // items per warp issued before the query
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffArena = 0;
@@ -66,7 +73,7 @@ static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 enum ItemType : int {
   IT_ROUTE = 1,  // routing summaries of kRouteSpans spans (consumed before the barrier)
-  IT_FULL = 2,   // kRows full-resolution rows (K and V)
+  IT_FULL = 2,   // kRows full-resolution rows (K and V), the CTA's own or from the pool
   IT_SUM = 3,    // kRows summary rows (K and V) of unexpanded spans
   IT_REC = 4,    // one whole basis record
   IT_KEY = 5,    // key part of a split record (header, sigma_K, g_K, Vt_K)
@@ -111,7 +118,7 @@ struct DecodeParams {
   GroupState* groups;
   int32_t* cta_n;                // [g][cg] expanded spans per CTA (fused, list output)
   int32_t* cta_list;             // [g][max_spans] them, ascending within each CTA's share
-  Partial* partials;             // [g][cg]
+  float* partials;               // [g][cg] of 16 + G*128 floats (m[8], l[8], o[G][128])
   int B, Hq, Hkv, G, n_sink, n_recent, max_spans, cg;
   float scale_log2;
   int fused;
@@ -127,14 +134,11 @@ const void* decode_kernel_fn_ks2();
 const void* decode_kernel_fn_ks3();
 const void* decode_kernel_fn_ks4();
 
-// Share of CTA j of cg: full-resolution rows [f0, f1) and spans [k0, k1).
-// Span boundaries are rounded up to multiples of 8 so that every per-span
-// array slice starts 16-byte aligned.  32-bit arithmetic: the host rejects
-// shapes with (2 (n_sink + n_recent) + 5 max_spans) * 256 >= 2^31.
-__host__ __device__ inline void fixed_range(int j, int cg, int n_full, int n_sp, int& f0,
-                                            int& f1, int& k0, int& k1) {
-  f0 = n_full * j / cg;
-  f1 = n_full * (j + 1) / cg;
+// Span share [k0, k1) of CTA j of cg.  Boundaries are rounded up to
+// multiples of 8 so that every per-span array slice starts 16-byte aligned.
+// 32-bit arithmetic: the host rejects shapes with
+// (2 (n_sink + n_recent) + 5 max_spans) * 256 >= 2^31.
+__host__ __device__ inline void span_range(int j, int cg, int n_sp, int& k0, int& k1) {
   auto kpos = [&](int jj) -> int {
     const int v = ((n_sp * jj / cg) + 7) & ~7;
     return v < n_sp ? v : n_sp;
@@ -143,9 +147,43 @@ __host__ __device__ inline void fixed_range(int j, int cg, int n_full, int n_sp,
   k1 = kpos(j + 1);
 }
 
+// Everything a CTA derives from its block index (computed once, kept in
+// shared memory).
+struct Ctx {
+  int g, j, b, c;
+  int n_sp;     // spans of the sequence
+  int k0, k1;   // the CTA's spans
+  int n_full;   // full-resolution rows of the group
+  int n_fp;     // their pages
+  int own0;     // first of the CTA's own full-resolution pages
+  int n_own;    // how many it owns (kStaticPages, fewer at the end)
+  int pool0;    // first page of the group's pool (the pages no CTA owns)
+  int n_fixed;  // the CTA's own full-resolution pages + its summary pages
+  int n_rp;     // routing pages (fused mode)
+  long long gs; // g * max_spans
+  long long bs; // b * max_spans
+};
+
+// Issue state of one warp, in shared memory (lane 0 issues; every lane reads
+// ni / nd / ok after a __syncwarp).
+struct WarpQ {
+  int head, tail;   // arena granule counters (monotone)
+  int ni, nd;       // items issued / consumed
+  int pk;           // pending claim: 0 none, 1 own page, 2 record, 3 pool pages
+  int pidx;         // its index (own page, record entry, first pool page)
+  int ppart, pnp;   // record: next part, parts; pool: next page, pages
+  int fixed_out;    // own pages exhausted
+  int rec_out;      // record queue exhausted
+  int pool_out;     // the group's pool exhausted
+  int ok;           // no wait has run out
+};
+
 struct SmemMisc {
+  Ctx ctx;
+  WarpQ wq[kWarps];
   Item desc[kWarps][kMaxItems];
   uint64_t bar[kWarps][kMaxItems];
+  uint64_t cmb_bar;        // last CTA of a group: a chunk of partials landed
   unsigned int pmask[kMaxRoutePages];  // fused: expanded spans per routing page
   float theta[8];
   int n_rec;               // expanded records of this CTA

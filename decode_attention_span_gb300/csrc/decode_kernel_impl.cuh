@@ -7,7 +7,9 @@
 // warp issues and consumes its items itself, in order, so no handover
 // between warps is needed; the only CTA-wide synchronisation is the routing
 // barrier (every span of the CTA routed, the record list final) and the
-// merge at the end.
+// merge at the end.  Lane 0 alone runs the issue logic, on the warp's state
+// in shared memory, so the consuming lanes keep their registers for the
+// softmax state and the kernel needs no stack.
 #pragma once
 
 #include "decode_consumer.cuh"
@@ -16,34 +18,11 @@ namespace sekv {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Everything a CTA derives from its block index (uniform over the CTA).
-struct Ctx {
-  int g, j, b, c;
-  int f0, f1, k0, k1;
-  int nfp;      // full-resolution pages
-  int n_fixed;  // full-resolution pages + summary pages
-  int n_rp;     // routing pages (fused mode)
-  size_t gs;    // g * max_spans
-  size_t bs;    // b * max_spans
-};
-
-// Issue state of one warp (every lane holds the same values).
-struct WarpQ {
-  int head, tail;   // arena granule counters (monotone)
-  int ni, nd;       // items issued / consumed
-  int pk;           // pending claim: 0 none, 1 fixed page, 2 record
-  int pidx;         // its index (fixed page, or record entry)
-  int ppart, pnp;   // record: next part, parts
-  int fixed_out;    // fixed-page queue exhausted
-  int rec_out;      // record queue exhausted
-  int ok;           // no wait has run out
-};
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Place an item of `bytes` in warp w's arena: returns the granule counter of
+// Place an item of `bytes` in a warp's arena: returns the granule counter of
 // its start, or -1 if it does not fit yet.  An empty arena starts over at
 // its beginning, so that every item up to the arena's size fits eventually.
 __device__ __forceinline__ int arena_place(WarpQ& Q, uint32_t bytes) {
@@ -58,9 +37,10 @@ __device__ __forceinline__ int arena_place(WarpQ& Q, uint32_t bytes) {
   return start;
 }
 
-// Arm item `it` (lane 0): descriptor, then the barrier with its bytes, then
-// its copies.  The descriptor is published by the barrier's phase
-// completion, which the consuming lanes acquire when they wait on it.
+// Arm item `it` (lane 0): descriptor, then the barrier with its bytes; the
+// caller issues its copies next.  The descriptor is published by the
+// barrier's phase completion, which the consuming lanes acquire when they
+// wait on it.
 __device__ __forceinline__ void arm_item(SmemMisc* ms, int w, int slot, const Item& it,
                                          uint32_t bytes) {
   ms->desc[w][slot] = it;
@@ -70,101 +50,119 @@ __device__ __forceinline__ void arm_item(SmemMisc* ms, int w, int slot, const It
   mbar_arrive_expect_tx(&ms->bar[w][slot], bytes);
 }
 
-// Issue the warp's next items while it has room: first any claim still
-// pending, then new claims, records before fixed pages once routing is done.
-static __device__ __noinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
-                                        const Ctx& C, WarpQ& Q, bool routed) {
+// Issue the warp's next items while it has room (lane 0, on a register copy
+// of the warp's state): first any claim still pending, then new claims.
+// Before routing is done only the CTA's own pages, at most kPrologueItems
+// items; after it, records, then own pages, then the group's pool.  Pool
+// claims are made one ahead: `claim` holds the pending atomic's result, so
+// its round trip overlaps the warp's work (-1: none made yet).
+__device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
+                                           bool routed, int& claim) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const RecEntry* ents = reinterpret_cast<const RecEntry*>(smem + kOffEntries);
-  while (Q.ok && Q.ni - Q.nd < kMaxItems) {
-    if (Q.pk == 0 && routed && !Q.rec_out) {
-      int e = 0;
-      if (lane == 0) e = atomicAdd(&ms->rec_next, 1);
-      e = __shfl_sync(kFull, e, 0);
-      if (e < ms->n_rec) {
-        const RecEntry en = ents[e];
-        const int rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
-        if (rK > P.rank_lim || rV > P.rank_lim) {
-          if (lane == 0) set_device_error(P.status, DEV_BAD_RANK, rK > rV ? rK : rV);
-          continue;  // skipped
+  if (lane == 0) {
+    WarpQ Q = ms->wq[w];
+    const Ctx C = ms->ctx;
+    const int n_rec = ms->n_rec;
+    const int cap = routed ? kMaxItems : kPrologueItems;
+    const RecEntry* ents = reinterpret_cast<const RecEntry*>(smem + kOffEntries);
+    const uint64_t pol = policy_evict_first();
+    while (Q.ok && Q.ni - Q.nd < cap) {
+      if (Q.pk == 0 && routed && !Q.rec_out) {
+        const int e = atomicAdd(&ms->rec_next, 1);
+        if (e < n_rec) {
+          const RecEntry en = ents[e];
+          const int rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
+          if (rK > P.rank_lim || rV > P.rank_lim) {
+            set_device_error(P.status, DEV_BAD_RANK, rK > rV ? rK : rV);
+            continue;  // skipped
+          }
+          Q.pk = 2;
+          Q.pidx = e;
+          Q.ppart = 0;
+          Q.pnp = record_parts(en.body, rK, rV);
+        } else {
+          Q.rec_out = 1;
         }
-        Q.pk = 2;
-        Q.pidx = e;
-        Q.ppart = 0;
-        Q.pnp = record_parts(en.body, rK, rV);
-      } else {
-        Q.rec_out = 1;
       }
-    }
-    if (Q.pk == 0 && !Q.fixed_out) {
-      int f = 0;
-      if (lane == 0) f = atomicAdd(&ms->fixed_next, 1);
-      f = __shfl_sync(kFull, f, 0);
-      if (f < C.n_fixed) {
-        Q.pk = 1;
-        Q.pidx = f;
-      } else {
-        Q.fixed_out = 1;
+      if (Q.pk == 0 && !Q.fixed_out) {
+        const int f = atomicAdd(&ms->fixed_next, 1);
+        if (f < C.n_fixed) {
+          Q.pk = 1;
+          Q.pidx = f;
+        } else {
+          Q.fixed_out = 1;
+        }
       }
-    }
-    if (Q.pk == 0) break;
+      if (Q.pk == 0 && routed && !Q.pool_out) {
+        if (claim < 0) claim = atomicAdd(&P.groups[C.g].full_next, kPoolClaim);
+        const int first = C.pool0 + claim;
+        if (first < C.n_fp) {
+          Q.pk = 3;
+          Q.pidx = first;
+          Q.ppart = 0;
+          Q.pnp = (C.n_fp - first) < kPoolClaim ? (C.n_fp - first) : kPoolClaim;
+          claim = atomicAdd(&P.groups[C.g].full_next, kPoolClaim);  // the next one, ahead
+        } else {
+          Q.pool_out = 1;
+        }
+      }
+      if (Q.pk == 0) break;
 
-    Item it{};
-    uint32_t bytes = 0;
-    int64_t s0 = 0, s1 = 0;
-    uint32_t n0 = 0, n1 = 0;
-    int64_t roff = 0;
-    if (Q.pk == 1) {
-      const bool full = Q.pidx < C.nfp;
-      it.type = full ? IT_FULL : IT_SUM;
-      it.a = full ? C.f0 + kRows * Q.pidx : C.k0 + kRows * (Q.pidx - C.nfp);
-      const int e = full ? C.f1 : C.k1;
-      it.n = (e - it.a) < kRows ? (e - it.a) : kRows;
-      bytes = kRowPageBytes;
-    } else {
-      const RecEntry en = ents[Q.pidx];
-      const int b = en.body, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
-      const RecordLayout L = record_layout(b, rK, rV);
-      roff = (int64_t(uint32_t(en.off_lo)) | (int64_t(en.off_hi) << 32));
-      it.rk = rK;
-      it.rv = rV;
-      if (Q.pnp == 1) {
-        it.type = IT_REC;
-        it.n = b;
-        n0 = uint32_t(L.total);
-      } else if (Q.ppart == 0) {
-        it.type = IT_KEY;
-        n0 = uint32_t(L.uk);
-      } else if (Q.ppart < Q.pnp - 1) {
-        const int rows = split_rows(rK, rV);
-        const int i0 = (Q.ppart - 1) * rows;
-        it.type = IT_UT;
-        it.a = i0;
-        it.n = (b - i0) < rows ? (b - i0) : rows;
-        it.uv = 2 * it.n * r8(rK);
-        s0 = L.uk + 2 * int64_t(i0) * r8(rK);
-        n0 = uint32_t(it.uv);
-        s1 = L.uv + 2 * int64_t(i0) * r8(rV);
-        n1 = uint32_t(2 * it.n * r8(rV));
+      Item it{};
+      uint32_t bytes = 0;
+      int64_t s0 = 0, s1 = 0;
+      uint32_t n0 = 0, n1 = 0;
+      int64_t roff = 0;
+      if (Q.pk != 2) {
+        const bool full = Q.pk == 3 || Q.pidx < C.n_own;
+        it.type = full ? IT_FULL : IT_SUM;
+        it.a = Q.pk == 3 ? kRows * (Q.pidx + Q.ppart)
+                         : (full ? kRows * (C.own0 + Q.pidx) : C.k0 + kRows * (Q.pidx - C.n_own));
+        const int e = full ? C.n_full : C.k1;
+        it.n = (e - it.a) < kRows ? (e - it.a) : kRows;
+        bytes = kRowPageBytes;
       } else {
-        it.type = IT_VAL;
-        s0 = L.vpart;
-        n0 = uint32_t(L.total - L.vpart);
+        const RecEntry en = ents[Q.pidx];
+        const int b = en.body, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
+        const RecordLayout L = record_layout(b, rK, rV);
+        roff = (int64_t(uint32_t(en.off_lo)) | (int64_t(en.off_hi) << 32));
+        it.rk = rK;
+        it.rv = rV;
+        if (Q.pnp == 1) {
+          it.type = IT_REC;
+          it.n = b;
+          n0 = uint32_t(L.total);
+        } else if (Q.ppart == 0) {
+          it.type = IT_KEY;
+          n0 = uint32_t(L.uk);
+        } else if (Q.ppart < Q.pnp - 1) {
+          const int rows = split_rows(rK, rV);
+          const int i0 = (Q.ppart - 1) * rows;
+          it.type = IT_UT;
+          it.a = i0;
+          it.n = (b - i0) < rows ? (b - i0) : rows;
+          it.uv = 2 * it.n * r8(rK);
+          s0 = L.uk + 2 * int64_t(i0) * r8(rK);
+          n0 = uint32_t(it.uv);
+          s1 = L.uv + 2 * int64_t(i0) * r8(rV);
+          n1 = uint32_t(2 * it.n * r8(rV));
+        } else {
+          it.type = IT_VAL;
+          s0 = L.vpart;
+          n0 = uint32_t(L.total - L.vpart);
+        }
+        bytes = n0 + n1;
       }
-      bytes = n0 + n1;
-    }
-    const int start = arena_place(Q, bytes);
-    if (start < 0) break;  // the claim stays pending until space frees
-    const int slot = Q.ni % kMaxItems;
-    const int gsz = int((bytes + kGran - 1) / kGran);
-    it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
-    it.end = start + gsz;
-    if (lane == 0) {
+      const int start = arena_place(Q, bytes);
+      if (start < 0) break;  // the claim stays pending until space frees
+      const int slot = Q.ni % kMaxItems;
+      const int gsz = int((bytes + kGran - 1) / kGran);
+      it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
+      it.end = start + gsz;
       arm_item(ms, w, slot, it, bytes);
       uint8_t* dst = smem + it.boff;
       uint64_t* bar = &ms->bar[w][slot];
-      const uint64_t pol = policy_evict_first();
-      if (Q.pk == 1) {
+      if (Q.pk != 2) {
         const bool full = it.type == IT_FULL;
         tma_g2s_4d_hint(dst, full ? &P.tm_kfull : &P.tm_ksum, 0, it.a, 0, C.g, bar, pol);
         tma_g2s_4d_hint(dst + 2 * kRowHalf, full ? &P.tm_vfull : &P.tm_vsum, 0, it.a, 0, C.g,
@@ -174,32 +172,28 @@ static __device__ __noinline__ void issue_more(uint8_t* smem, SmemMisc* ms, cons
         if (n0) bulk_g2s_hint(dst, rec + s0, n0, bar, pol);
         if (n1) bulk_g2s_hint(dst + n0, rec + s1, n1, bar, pol);
       }
+      Q.head = it.end;
+      ++Q.ni;
+      if (Q.pk == 1 || ++Q.ppart == Q.pnp) Q.pk = 0;
     }
-    Q.head = it.end;
-    ++Q.ni;
-    if (Q.pk == 1 || ++Q.ppart == Q.pnp) Q.pk = 0;
+    ms->wq[w] = Q;
   }
+  __syncwarp();
 }
 
-// Wait (parked, bounded) for the warp's next item; false if the wait ran out.
-__device__ __forceinline__ bool wait_item(SmemMisc* ms, const WarpQ& Q) {
-  const int w = threadIdx.x >> 5;
-  return mbar_wait_parked(&ms->bar[w][Q.nd % kMaxItems], uint32_t((Q.nd / kMaxItems) & 1));
-}
-
-// Consume the warp's next (landed) item.
+// Consume the warp's item nd (landed); returns its end in the arena.
 template <int KS>
-__device__ __forceinline__ void consume_item(const uint8_t* smem, SmemMisc* ms, const Ctx& C,
-                                             const DecodeParams& P, WarpQ& Q, WarpAcc& A,
-                                             ExpAcc<KS>& X) {
+__device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
+                                            const DecodeParams& P, int nd, WarpAcc& A,
+                                            ExpAcc<KS>& X) {
   const int w = threadIdx.x >> 5;
-  const Item it = ms->desc[w][Q.nd % kMaxItems];
+  const Item it = ms->desc[w][nd % kMaxItems];
   const uint8_t* base = smem + it.boff;
   const uint32_t bu = smem_u32(base);
   const float* bias = reinterpret_cast<const float*>(smem + kOffBias);
   if (it.type == IT_FULL || it.type == IT_SUM) {
     consume_rows16(A, bu, bu + 2 * kRowHalf, it.n,
-                   it.type == IT_SUM ? bias + (it.a - C.k0) : nullptr, P.scale_log2);
+                   it.type == IT_SUM ? bias + (it.a - ms->ctx.k0) : nullptr, P.scale_log2);
   } else {
     int off_key = -1, off_uk = 0, off_uv = 0, off_val = -1, n = 0;
     if (it.type == IT_REC) {
@@ -221,36 +215,66 @@ __device__ __forceinline__ void consume_item(const uint8_t* smem, SmemMisc* ms, 
     if (n > 0) exp_tokens<KS>(A, X, base + off_uk, base + off_uv, n, it.rk, it.rv);
     if (off_val >= 0) exp_value<KS>(A, X, base + off_val, it.rv);
   }
+  return it.end;
+}
+
+// The warp's item nd is consumed and its arena space free (lane 0 records it).
+__device__ __forceinline__ void retire_item(SmemMisc* ms, int nd, int end) {
   __syncwarp();
-  Q.tail = it.end;
-  ++Q.nd;
+  if ((threadIdx.x & 31) == 0) {
+    WarpQ& Q = ms->wq[threadIdx.x >> 5];
+    Q.tail = end;
+    Q.nd = nd + 1;
+  }
+}
+
+// Issue routing page p (fused mode, lane 0) as the warp's next item; the
+// arena is empty or holds only earlier routing pages, so it always fits.
+__device__ __forceinline__ void issue_route_page(uint8_t* smem, SmemMisc* ms,
+                                                 const DecodeParams& P, int p) {
+  const int w = threadIdx.x >> 5;
+  WarpQ& Q = ms->wq[w];
+  const Ctx& C = ms->ctx;
+  const int start = arena_place(Q, kRoutePageBytes);
+  Item it{};
+  it.type = IT_ROUTE;
+  it.a = C.k0 + kRouteSpans * p;
+  it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
+  it.end = start + kRoutePageBytes / kGran;
+  const int slot = Q.ni % kMaxItems;
+  arm_item(ms, w, slot, it, kRoutePageBytes);
+  tma_g2s_4d_hint(smem + it.boff, &P.tm_sroute, 0, it.a, 0, C.g, &ms->bar[w][slot],
+                  policy_evict_first());
+  Q.head = it.end;
+  ++Q.ni;
 }
 
 // Routing page p of this CTA (fused mode), landed as the warp's next item:
 // expansion decisions for its spans, their summary biases and record entries.
-__device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const Ctx& C,
-                                           const DecodeParams& P, WarpQ& Q, int p, int body,
-                                           int rank, long long off) {
+__device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
+                                           int p, int body, int rank, long long off) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const float* ys = reinterpret_cast<const float*>(smem + kOffY);
   float* bias = reinterpret_cast<float*>(smem + kOffBias);
   RecEntry* ents = reinterpret_cast<RecEntry*>(smem + kOffEntries);
-  bool hit = false;
+  const int nd = ms->wq[w].nd;
+  const int k0 = ms->ctx.k0, k1 = ms->ctx.k1;
+  bool hit = false, landed = false;
   int end = 0;
-  if (Q.ok) {
-    if (wait_item(ms, Q)) {
-      const Item it = ms->desc[w][Q.nd % kMaxItems];
+  if (ms->wq[w].ok) {
+    landed = mbar_wait_parked(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1));
+    if (landed) {
+      const Item it = ms->desc[w][nd % kMaxItems];
       end = it.end;
       hit = route32(smem + it.boff, ys, ms->theta, P.G);
-    } else {
-      if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
-      Q.ok = 0;
+    } else if (lane == 0) {
+      set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
     }
   }
-  const int k = C.k0 + kRouteSpans * p + lane;
-  const bool valid = k < C.k1;
+  const int k = k0 + kRouteSpans * p + lane;
+  const bool valid = k < k1;
   const bool ex = valid && body > 0 && hit;
-  if (valid) bias[k - C.k0] = (body > 0 && !ex) ? log2f(float(body)) : kNegInf;
+  if (valid) bias[k - k0] = (body > 0 && !ex) ? log2f(float(body)) : kNegInf;
   const uint32_t bal = __ballot_sync(kFull, ex);
   int base = 0;
   if (lane == 0) {
@@ -266,82 +290,45 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const Ct
     en.rank = rank;
     ents[base + __popc(bal & ((1u << lane) - 1u))] = en;
   }
+  if (landed) {
+    retire_item(ms, nd, end);
+  } else {
+    __syncwarp();
+    if (lane == 0) ms->wq[w].ok = 0;
+  }
   __syncwarp();
-  if (Q.ok) {
-    Q.tail = end;
-    ++Q.nd;
-  }
-}
-
-// Issue routing page p (fused mode) as the warp's next item; the arena is
-// empty or holds only earlier routing pages, so it always fits.
-__device__ __forceinline__ void issue_route_page(uint8_t* smem, SmemMisc* ms, const Ctx& C,
-                                                 const DecodeParams& P, WarpQ& Q, int p) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int start = arena_place(Q, kRoutePageBytes);
-  Item it{};
-  it.type = IT_ROUTE;
-  it.a = C.k0 + kRouteSpans * p;
-  it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
-  it.end = start + kRoutePageBytes / kGran;
-  const int slot = Q.ni % kMaxItems;
-  if (lane == 0) {
-    arm_item(ms, w, slot, it, kRoutePageBytes);
-    tma_g2s_4d_hint(smem + it.boff, &P.tm_sroute, 0, it.a, 0, C.g, &ms->bar[w][slot],
-                    policy_evict_first());
-  }
-  Q.head = it.end;
-  ++Q.ni;
 }
 
 template <int KS>
 __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const DecodeParams& P) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  Ctx C;
-  C.j = blockIdx.x;
-  C.c = blockIdx.y;
-  C.b = blockIdx.z;
-  C.g = C.b * P.Hkv + C.c;
-  C.gs = size_t(C.g) * P.max_spans;
-  C.bs = size_t(C.b) * P.max_spans;
-  const int n_sp = P.n_spans[C.b];
-  const int n_full = P.n_sink + n_sp + P.n_recent;
-  fixed_range(C.j, P.cg, n_full, n_sp, C.f0, C.f1, C.k0, C.k1);
-  C.nfp = (C.f1 - C.f0 + kRows - 1) / kRows;
-  C.n_fixed = C.nfp + (C.k1 - C.k0 + kRows - 1) / kRows;
-  C.n_rp = P.fused ? (C.k1 - C.k0 + kRouteSpans - 1) / kRouteSpans : 0;
+  const Ctx& C = ms->ctx;
   const int G = P.G;
 
-  WarpQ Q{};
-  Q.ok = 1;
+  // ---- prologue: routing pages and the first own pages (no q needed) -----
   if (lane == 0) {
-    prefetch_tmap(&P.tm_kfull);
-    prefetch_tmap(&P.tm_vfull);
-    prefetch_tmap(&P.tm_ksum);
-    prefetch_tmap(&P.tm_vsum);
-    if (P.fused) prefetch_tmap(&P.tm_sroute);
+    for (int p = w; p < C.n_rp; p += kWarps) issue_route_page(smem, ms, P, p);
   }
-
-  // ---- prologue: routing pages and the first fixed pages (no q needed) ----
-  // routing pages p = w, w + 8 of this CTA, with their spans' metadata
+  int claim = -1;  // lane 0: the next pool claim, made ahead
+  issue_more(smem, ms, P, false, claim);
+  // the metadata of this warp's routing pages (p = w, w + 8)
   int rbody[2] = {0, 0}, rrank[2] = {0, 0};
   long long roff[2] = {0, 0};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int p = w + kWarps * i;
-    if (p < C.n_rp) {
-      issue_route_page(smem, ms, C, P, Q, p);
-      const int k = C.k0 + kRouteSpans * p + lane;
-      if (k < C.k1) {
-        rbody[i] = __ldg(P.body_len + C.bs + k);
-        rrank[i] = __ldg(P.rec_rank + C.gs + k);
-        roff[i] = __ldg(reinterpret_cast<const long long*>(P.rec_off) + C.gs + k);
-      }
+    const int k = C.k0 + kRouteSpans * (w + kWarps * i) + lane;
+    if (w + kWarps * i < C.n_rp && k < C.k1) {
+      rbody[i] = __ldg(P.body_len + C.bs + k);
+      rrank[i] = __ldg(P.rec_rank + C.gs + k);
+      roff[i] = __ldg(reinterpret_cast<const long long*>(P.rec_off) + C.gs + k);
     }
   }
+
+  // ---- the query (and in list mode the lists) come from earlier work ------
+  pdl_wait();
   // y = W_r q, rows 8w .. 8w + 7 of this warp: lane (r = lane / 4, quarter
-  // d = lane % 4) takes 32 of the 128 head dims; W_r is read before the
-  // dependency wait (the caller allows it), q after
+  // d = lane % 4) takes 32 of the 128 head dims (W_r is read here, in the
+  // same round trip as q, rather than held in registers across the wait)
   float4 wr[8];
   if (P.fused) {
     const float4* wrow = reinterpret_cast<const float4*>(
@@ -349,10 +336,6 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 #pragma unroll
     for (int i = 0; i < 8; ++i) wr[i] = __ldg(wrow + i);
   }
-  issue_more(smem, ms, P, C, Q, false);
-
-  // ---- the query (and in list mode the lists) come from earlier work ------
-  pdl_wait();
   float* qf = reinterpret_cast<float*>(smem + kOffQf);
   {
     // q as f32 [8][128] (rows past the group zero) for the routing projection
@@ -414,21 +397,21 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int p = w + kWarps * i;
-      if (p < C.n_rp) route_page(smem, ms, C, P, Q, p, rbody[i], rrank[i], roff[i]);
+      if (p < C.n_rp) route_page(smem, ms, P, p, rbody[i], rrank[i], roff[i]);
     }
   } else {
     // list mode: this CTA's expanded spans from the caller's ascending list
     // (every CTA checks the whole list; the first error wins)
     RecEntry* ents = reinterpret_cast<RecEntry*>(smem + kOffEntries);
     int n = P.list_n[C.g];
-    if (n < 0 || n > n_sp) {
+    if (n < 0 || n > C.n_sp) {
       if (tid == 0) set_device_error(P.status, DEV_BAD_LIST, C.g);
       n = 0;
     }
     for (int e = tid; e < n; e += kThreads) {
       const int k = P.list[C.gs + e];
       const int prev = e > 0 ? P.list[C.gs + e - 1] : -1;
-      bool ok = k > prev && k < n_sp;
+      bool ok = k > prev && k < C.n_sp;
       int body = 0, rank = 0;
       if (ok) {
         body = P.body_len[C.bs + k];
@@ -496,21 +479,30 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   ExpAcc<KS> X;
   X.had = false;
   for (;;) {
-    issue_more(smem, ms, P, C, Q, true);
-    if (Q.nd == Q.ni || !Q.ok) break;
-    if (!wait_item(ms, Q)) {
-      if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
-      Q.ok = 0;
+    issue_more(smem, ms, P, true, claim);
+    const int nd = ms->wq[w].nd;
+    if (nd == ms->wq[w].ni || !ms->wq[w].ok) break;
+    if (!mbar_wait_parked(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1))) {
+      __syncwarp();
+      if (lane == 0) {
+        set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
+        ms->wq[w].ok = 0;
+      }
+      __syncwarp();
       break;
     }
-    consume_item<KS>(smem, ms, C, P, Q, A, X);
+    const int end = consume_item<KS>(smem, ms, P, nd, A, X);
+    retire_item(ms, nd, end);
   }
   // after a timeout: every issued copy lands before the arena is reused
-  for (; Q.nd < Q.ni; ++Q.nd) {
-    if (!mbar_wait(&ms->bar[w][Q.nd % kMaxItems], uint32_t((Q.nd / kMaxItems) & 1),
-                   kWaitLimit)) {
-      if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 3);
-      break;
+  {
+    const int ni = ms->wq[w].ni;
+    for (int nd = ms->wq[w].nd; nd < ni; ++nd) {
+      if (!mbar_wait(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1),
+                     kWaitLimit)) {
+        if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 3);
+        break;
+      }
     }
   }
 
@@ -532,7 +524,9 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     }
   }
   __syncthreads();
-  Partial* mine = P.partials + size_t(C.g) * P.cg + C.j;
+  // this CTA's partial: m[8], l[8], then o[h][128] for the G heads only
+  const int pstride = 16 + G * kHeadDim;  // floats (a multiple of 4: 16-byte aligned)
+  float* mine = P.partials + (size_t(C.g) * P.cg + C.j) * pstride;
   {
     const int d = tid & (kHeadDim - 1);
     for (int h = tid >> 7; h < G; h += 2) {
@@ -550,10 +544,10 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
           O = fmaf(ws_[16 + h * kHeadDim + d], sc, O);
         }
       }
-      mine->o[h][d] = O;
+      mine[16 + h * kHeadDim + d] = O;
       if (d == 0) {
-        mine->m[h] = M;
-        mine->l[h] = L;
+        mine[h] = M;
+        mine[8 + h] = L;
       }
     }
   }
@@ -567,49 +561,67 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   if (!ms->is_last) return;
 
   // ---- last CTA of this group: merge the partials, write the output --------
+  // (the partials arrive by bulk copy, kMergeChunk CTAs per copy, so the
+  // merge costs one global round trip per chunk; an online log-sum-exp
+  // merge runs over the chunks)
   __threadfence();
   const int cg = P.cg;
-  const Partial* parts = P.partials + size_t(C.g) * cg;
-  float* sm_m = reinterpret_cast<float*>(smem);                 // [cg][8] m, then scales
-  float* sm_l = sm_m + kMaxCg * 8;                              // [cg][8] l
-  float* sm_ML = sm_l + kMaxCg * 8;                             // M[8], L[8]
-  for (int i = tid; i < cg * 8; i += kThreads) {
-    const int jj = i >> 3, h = i & 7;
-    sm_m[i] = h < G ? __ldcg(&parts[jj].m[h]) : kNegInf;
-    sm_l[i] = h < G ? __ldcg(&parts[jj].l[h]) : 0.f;
+  const float* parts = P.partials + size_t(C.g) * cg * pstride;
+  const float* cbuf = reinterpret_cast<const float*>(smem);  // chunk of partials
+  const int d = tid & (kHeadDim - 1), hsel = tid >> 7;  // this thread: dim d of heads hsel + 2i
+  float Mh[4], Lh[4], Oh[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    Mh[i] = kNegInf;
+    Lh[i] = 0.f;
+    Oh[i] = 0.f;
   }
-  __syncthreads();
-  if (tid < 8) {
-    float M = kNegInf;
-    for (int jj = 0; jj < cg; ++jj) M = fmaxf(M, sm_m[jj * 8 + tid]);
-    float L = 0.f;
-    if (M != kNegInf)
-      for (int jj = 0; jj < cg; ++jj) L = fmaf(sm_l[jj * 8 + tid], exp2f(sm_m[jj * 8 + tid] - M), L);
-    sm_ML[tid] = M;
-    sm_ML[8 + tid] = L;
+  for (int c0 = 0, ph = 0; c0 < cg; c0 += kMergeChunk, ph ^= 1) {
+    const int nc = (cg - c0) < kMergeChunk ? (cg - c0) : kMergeChunk;
+    __syncthreads();  // the previous chunk is consumed
+    if (tid == 0) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&ms->cmb_bar, uint32_t(nc * pstride * 4));
+      bulk_g2s(smem, parts + size_t(c0) * pstride, uint32_t(nc * pstride * 4), &ms->cmb_bar);
+    }
+    // every thread takes every barrier of this loop, even after a timeout
+    const bool landed = mbar_wait(&ms->cmb_bar, uint32_t(ph), kWaitLimit);
+    if (!landed && tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 7);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int h = hsel + 2 * i;
+      if (!landed || h >= G) continue;
+      float m_new = Mh[i];
+      for (int jj = 0; jj < nc; ++jj) m_new = fmaxf(m_new, cbuf[jj * pstride + h]);
+      if (m_new == kNegInf) continue;
+      const float a = exp2f(Mh[i] - m_new);  // 0 for the first chunk
+      float l = Lh[i] * a, o = Oh[i] * a;
+      for (int jj = 0; jj < nc; ++jj) {
+        const float* pj = cbuf + jj * pstride;
+        const float sc = exp2f(pj[h] - m_new);
+        l = fmaf(pj[8 + h], sc, l);
+        o = fmaf(pj[16 + h * kHeadDim + d], sc, o);
+      }
+      Mh[i] = m_new;
+      Lh[i] = l;
+      Oh[i] = o;
+    }
   }
-  __syncthreads();
-  for (int i = tid; i < cg * 8; i += kThreads) {
-    const float M = sm_ML[i & 7];
-    sm_m[i] = (M == kNegInf) ? 0.f : exp2f(sm_m[i] - M);
-  }
-  __syncthreads();
-  {
-    const int d = tid & (kHeadDim - 1);
-    for (int h = tid >> 7; h < G; h += 2) {
-      float O = 0.f;
-#pragma unroll 4
-      for (int jj = 0; jj < cg; ++jj) O = fmaf(__ldcg(&parts[jj].o[h][d]), sm_m[jj * 8 + h], O);
-      const float L = sm_ML[8 + h];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int h = hsel + 2 * i;
+    if (h < G) {
       const size_t row = size_t(C.b) * P.Hq + size_t(C.c) * G + h;
-      P.out[row * kHeadDim + d] = L > 0.f ? O / L : 0.f;
+      P.out[row * kHeadDim + d] = Lh[i] > 0.f ? Oh[i] / Lh[i] : 0.f;
       if (d == 0 && P.lse != nullptr)
-        P.lse[row] = L > 0.f ? (sm_ML[h] + log2f(L)) * kLn2 : kNegInf;
+        P.lse[row] = Lh[i] > 0.f ? (Mh[i] + log2f(Lh[i])) * kLn2 : kNegInf;
     }
   }
   if (P.fused && P.expanded_out != nullptr) {
     // the CTAs' ascending lists, one after the other
-    int* pre = reinterpret_cast<int*>(sm_ML + 16);  // [cg + 1]
+    int* pre = reinterpret_cast<int*>(smem + kMergeChunk * sizeof(Partial));  // [cg + 1]
+    // (past the largest chunk of partials)
+    __syncthreads();
     if (tid == 0) {
       int acc = 0;
       for (int jj = 0; jj < cg; ++jj) {
@@ -620,8 +632,8 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     }
     __syncthreads();
     for (int jj = w; jj < cg; jj += kWarps) {
-      int a0, a1, sk0, sk1;
-      fixed_range(jj, cg, n_full, n_sp, a0, a1, sk0, sk1);
+      int sk0, sk1;
+      span_range(jj, cg, C.n_sp, sk0, sk1);
       const int cnt = pre[jj + 1] - pre[jj];
       for (int i = lane; i < cnt; i += 32)
         P.expanded_out[C.gs + pre[jj] + i] = __ldcg(P.cta_list + C.gs + sk0 + i);
@@ -629,7 +641,10 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     if (tid == 0 && P.n_expanded_out != nullptr) P.n_expanded_out[C.g] = pre[cg];
   }
   __syncthreads();
-  if (tid == 0) P.groups[C.g].done = 0;
+  if (tid == 0) {
+    P.groups[C.g].done = 0;
+    P.groups[C.g].full_next = 0;
+  }
 }
 
 // grid: (cg, Hkv, B); block: 8 warps, each its own producer and consumer
@@ -640,14 +655,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   SmemMisc* ms = reinterpret_cast<SmemMisc*>(smem + kOffMisc);
+  if (threadIdx.x < kWarps) {
+    WarpQ& Q = ms->wq[threadIdx.x];
+    Q = WarpQ{};
+    Q.ok = 1;
+  }
   if (threadIdx.x == 0) {
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kMaxItems; ++s) mbar_init(&ms->bar[w][s], 1);
+    mbar_init(&ms->cmb_bar, 1);
     ms->n_rec = 0;
     ms->rec_next = 0;
     ms->fixed_next = 0;
     ms->is_last = 0;
     for (int p = 0; p < kMaxRoutePages; ++p) ms->pmask[p] = 0u;
+    Ctx& C = ms->ctx;
+    C.j = blockIdx.x;
+    C.c = blockIdx.y;
+    C.b = blockIdx.z;
+    C.g = C.b * P.Hkv + C.c;
+    C.gs = (long long)C.g * P.max_spans;
+    C.bs = (long long)C.b * P.max_spans;
+    C.n_sp = P.n_spans[C.b];
+    C.n_full = P.n_sink + C.n_sp + P.n_recent;
+    span_range(C.j, P.cg, C.n_sp, C.k0, C.k1);
+    C.n_fp = (C.n_full + kRows - 1) / kRows;
+    C.own0 = kStaticPages * C.j;
+    const int own = C.n_fp - C.own0;
+    C.n_own = own < 0 ? 0 : (own > kStaticPages ? kStaticPages : own);
+    C.pool0 = kStaticPages * P.cg;
+    C.n_fixed = C.n_own + (C.k1 - C.k0 + kRows - 1) / kRows;
+    C.n_rp = P.fused ? (C.k1 - C.k0 + kRouteSpans - 1) / kRouteSpans : 0;
     fence_mbar_init();
   }
   __syncthreads();

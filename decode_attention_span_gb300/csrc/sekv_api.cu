@@ -251,7 +251,7 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.groups = reinterpret_cast<GroupState*>(w + L.groups);
   P.cta_n = reinterpret_cast<int32_t*>(w + L.cta_n);
   P.cta_list = reinterpret_cast<int32_t*>(w + L.cta_list);
-  P.partials = reinterpret_cast<Partial*>(w + L.partials);
+  P.partials = reinterpret_cast<float*>(w + L.partials);
   P.B = cfg->batch;
   P.Hq = cfg->n_q_heads;
   P.Hkv = cfg->n_kv_heads;

@@ -32,7 +32,8 @@ enum DeviceError : int32_t {
 struct GroupState {        // one per (sequence, KV head); zero between calls
   int32_t done;            // decode: CTAs that have written their partial
   int32_t route_done;      // route kernel: chunks finished
-  int32_t pad[2];
+  int32_t full_next;       // decode: full-resolution pages taken from the group's pool
+  int32_t pad;
 };
 
 struct Partial {           // one CTA's softmax state for up to 8 heads
