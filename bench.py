@@ -49,6 +49,12 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--traffic-from", default=None, metavar="CSV",
+                    help="write profiles/decode_kernel_traffic.json from an ncu --csv capture of "
+                         "dram__bytes_read.sum / dram__bytes_write.sum and exit")
+    ap.add_argument("--traffic-workload", default="llama3_8b_128k")
+    ap.add_argument("--traffic-scale", type=float, default=1.0)
+    ap.add_argument("--traffic-command", default="")
     ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv"],
                     help="decode: the headline decode step; build: the prefill cache build; "
                          "fullkv: the same decode step over a full-KV cache (comparator)")
@@ -97,11 +103,11 @@ def max_over_ranks(x: float, ws: int) -> float:
 DECODE_SOURCES = ("decode_attn.cuh", "decode_consumer.cuh", "decode_kernel_impl.cuh",
                   "decode_ks1.cu", "decode_ks2.cu", "decode_ks3.cu", "decode_ks4.cu",
                   "sekv_common.cuh")
-DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_kernel_llama3_8b_128k.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
 
 
 def decode_source_hash() -> str:
-    """sha256 over the decode kernel's sources (the kernel the profile covers)."""
+    """sha256 over the decode kernel's sources (the kernel a capture covers)."""
     import hashlib
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
@@ -111,24 +117,66 @@ def decode_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, or None
-    when the kernel sources changed since it was taken or the summary covers
-    another workload."""
+    """DRAM bytes per decode launch (read + write) for `workload`, from the
+    JSON that ``--traffic-from`` wrote out of an ncu capture, or None when the
+    kernel sources changed since that capture or it covers another workload."""
     try:
-        text = open(DECODE_PROFILE, encoding="utf-8").read()
-    except OSError:
+        with open(TRAFFIC_JSON, encoding="utf-8") as f:
+            d = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        for key in ("source-sha256:", "traffic-bytes-per-launch:", "Workload:"):
-            if line.strip().startswith(key):
-                vals[key] = line.split(":", 1)[1].strip(" `:")
-    if vals.get("Workload:") != workload or vals.get("source-sha256:") != decode_source_hash():
+    e = d.get(workload)
+    if not e or e.get("source_sha256") != decode_source_hash():
         return None
+    return e.get("bytes_per_launch")
+
+
+def write_traffic(csv_path: str, workload: str, launch_scale: float, command: str):
+    """Parse an ncu --csv capture (metrics dram__bytes_read.sum and
+    dram__bytes_write.sum of the decode kernel) and record the mean DRAM bytes
+    per launch, times `launch_scale` (the capture's workload scaled to a full
+    launch), in profiles/decode_kernel_traffic.json under `workload`."""
+    import csv
+    per = {}
+    with open(csv_path, newline="", encoding="utf-8", errors="replace") as f:
+        rows = [r for r in csv.reader(f)]
+    head = None
+    for i, r in enumerate(rows):
+        if "Metric Name" in r and "Kernel Name" in r:
+            head = i
+            break
+    if head is None:
+        raise SystemExit(f"{csv_path}: no ncu metric table")
+    cols = rows[head]
+    ki, ii, mi, vi = (cols.index("Kernel Name"), cols.index("ID"), cols.index("Metric Name"),
+                      cols.index("Metric Value"))
+    unit_i = cols.index("Metric Unit") if "Metric Unit" in cols else None
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6,
+             "GB": 1e9, "B": 1}
+    for r in rows[head + 1:]:
+        if len(r) <= max(ki, ii, mi, vi) or "decode_kernel" not in r[ki]:
+            continue
+        if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        v = float(r[vi].replace(",", ""))
+        if unit_i is not None:
+            v *= scale.get(r[unit_i], 1)
+        per[r[ii]] = per.get(r[ii], 0.0) + v
+    if not per:
+        raise SystemExit(f"{csv_path}: no decode_kernel DRAM metrics")
+    mean = sum(per.values()) / len(per)
     try:
-        return int(vals["traffic-bytes-per-launch:"])
-    except (KeyError, ValueError):
-        return None
+        with open(TRAFFIC_JSON, encoding="utf-8") as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        d = {}
+    d[workload] = {"bytes_per_launch": int(round(mean * launch_scale)), "launches": len(per),
+                   "captured_bytes_per_launch": int(round(mean)), "launch_scale": launch_scale,
+                   "source_sha256": decode_source_hash(), "command": command}
+    with open(TRAFFIC_JSON, "w", encoding="utf-8") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({workload: d[workload]}))
 
 
 def measured_peaks():
@@ -382,45 +430,110 @@ def _group_arrays(arr, b, c):
     return out
 
 
-def oracle_sample(w, layer_arrays, seconds: float):
-    """Time the oracle's routing + attention on (layer, group) units until
-    `seconds` of CPU work; returns (mean seconds per unit, units, description).
+UNITS_PER_STEP_DOC = ("one timed sample is one (layer, sequence, KV head) unit: the oracle's "
+                      "routing + mixed-resolution attention of one group")
 
-    Thresholds for each unit are placed with the oracle's own logits (same
-    recipe as the GPU run: per-head quantile with a 1e-3 margin)."""
+
+def decode_config(w, ws_n: int) -> dict:
+    """The workload a decode line is quoted on (the same on both arms)."""
+    return {"workload": w.name, "layers": w.layers, "batch": w.batch, "ctx": w.ctx,
+            "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+            "expand_frac_target": w.expand_frac, "bases": "hbm-resident",
+            "l2": "inputs larger than L2 (distinct buffers per layer)",
+            "parallelism": f"replicas x{ws_n}",
+            "graph": "one CUDA graph per step, programmatic dependent launch"}
+
+
+def oracle_units(w, n: int):
+    """The oracle's inputs for the first n (sequence, KV head) groups of layer
+    0 of the workload, drawn on the CPU: the one unit sample both oracle legs
+    time (the cpu_baseline leg and --impl reference).  Thresholds come from
+    the oracle's own logits (per-head quantile, 1e-3 margin)."""
     import oracle
     from oracle import layout
     G = w.group
     p_head = gen.per_head_fraction(w.expand_frac, G)
+    arr = gen.abi_to_numpy(gen.decode_cache(w, 0, device="cpu"))
+    g = gen._gen(w.seed * 7919 + 1)
+    q = gen.query(g, w.batch, w.n_q_heads).float().numpy()
+    W = gen.routing_weights(g, w.n_kv_heads).numpy()
+    units = []
+    for b in range(w.batch):
+        for c in range(w.n_kv_heads):
+            if len(units) >= n:
+                return units
+            cache = layout.unpack_layer(_group_arrays(arr, b, c), w.n_sink, w.n_recent)
+            qg, Wg = q[b:b + 1, c * G:(c + 1) * G], W[c:c + 1]
+            z = oracle.route_logits(qg, Wg, cache)
+            theta = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)])
+            units.append((cache, qg, Wg, theta))
+    return units
+
+
+def time_units(units, n_warm: int, n_timed: int):
+    """Seconds per unit of the oracle's routing + attention, cycling over
+    `units`."""
+    import oracle
     times = []
-    t_start = time.perf_counter()
-    unit = 0
-    for (l, arr, q, W) in layer_arrays:
-        for b in range(w.batch):
-            for c in range(w.n_kv_heads):
-                sub = _group_arrays(arr, b, c)
-                cache = layout.unpack_layer(sub, w.n_sink, w.n_recent)
-                qg = q[b:b + 1, c * G:(c + 1) * G]
-                Wg = W[c:c + 1]
-                z = oracle.route_logits(qg, Wg, cache)
-                theta = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)])
-                t0 = time.perf_counter()
-                E, _ = oracle.route(qg, Wg, cache, theta)
-                oracle.decode_attention(qg, cache, E, 1.0 / math.sqrt(128.0))
-                times.append(time.perf_counter() - t0)
-                unit += 1
-                if time.perf_counter() - t_start > seconds:
-                    break
-            else:
-                continue
-            break
-        else:
-            continue
-        break
-    desc = (f"oracle routing + attention (fp64 numpy) on {unit} (layer, sequence, KV head) "
-            f"units of the workload, first layer(s) in order; steps/s = 1 / (mean unit time "
-            f"x {w.batch * w.n_kv_heads} units x {w.layers} layers)")
-    return float(np.mean(times)), unit, desc
+    for i in range(n_warm + n_timed):
+        cache, qg, Wg, theta = units[i % len(units)]
+        t0 = time.perf_counter()
+        E, _ = oracle.route(qg, Wg, cache, theta)
+        oracle.decode_attention(qg, cache, E, 1.0 / math.sqrt(128.0))
+        if i >= n_warm:
+            times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_baseline_leg(w, seconds: float) -> dict:
+    """The oracle on the host cores: the shared unit sample, about `seconds`
+    of timed work, scaled to steps/s."""
+    units = oracle_units(w, 8)
+    est = float(np.mean(time_units(units, 1, 1)))
+    n = max(2, int(seconds / max(est, 1e-6)))
+    times = time_units(units, 0, n)
+    units_per_step = w.batch * w.n_kv_heads * w.layers
+    value = 1.0 / (float(np.mean(times)) * units_per_step)
+    return {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{UNITS_PER_STEP_DOC}; {n} units timed, cycling over the first "
+                      f"{len(units)} groups of layer 0 (drawn on the CPU); steps/s = 1 / (mean "
+                      f"unit time x {units_per_step} units per step)",
+            "units_timed": n, "units_per_step": units_per_step}
+
+
+def parity_check(sk, cfg, ws, L, w) -> dict:
+    """The bench's own layer 0 against the oracle: sequence 0, KV head 0, at
+    the full workload size and in the timed launch configuration.  The
+    group's thresholds come from the oracle's own logits (1e-3 margin); the
+    GPU step is run again with them, outside the timed region."""
+    import oracle
+    from oracle import layout
+    G = w.group
+    arr = gen.abi_to_numpy(L["t"])
+    cache = layout.unpack_layer(_group_arrays(arr, 0, 0), w.n_sink, w.n_recent)
+    qg = L["q"].float().cpu().numpy()[0:1, 0:G]
+    Wg = L["W"].cpu().numpy()[0:1]
+    z = oracle.route_logits(qg, Wg, cache)
+    p_head = gen.per_head_fraction(w.expand_frac, G)
+    th = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)], np.float32)
+    E, _ = oracle.route(qg, Wg, cache, th)
+    scale = 1.0 / math.sqrt(128.0)
+    o_ref, lse_ref = oracle.decode_attention(qg, cache, E, scale)
+    theta = L["theta"].clone()
+    theta[:G] = torch.from_numpy(th).to(theta.device)
+    out, lse, lst, cnt = sk.decode_step(cfg, L["cache"], L["q"], L["W"], theta, scale, ws,
+                                        want_list=True)
+    torch.cuda.synchronize()
+    o = out[0, :G].double().cpu().numpy()
+    err = float(np.abs(o - o_ref[0]).max())
+    rel = float(np.linalg.norm(o - o_ref[0]) / max(np.linalg.norm(o_ref[0]), 1e-30))
+    n = int(cnt[0])
+    same = n == len(E[0][0]) and bool(np.array_equal(lst[:n].cpu().numpy(), E[0][0]))
+    return {"sample": "layer 0, sequence 0, KV head 0 (its query heads), full size, timed "
+                      "launch configuration, thresholds from the oracle's logits",
+            "max_abs": err, "rel_l2": rel, "expansion_set_equal": same, "expanded": n,
+            "tolerance": {"max_abs": 1e-2, "rel_l2": 5e-3},
+            "ok": bool(same and err <= 1e-2 and rel <= 5e-3)}
 
 
 def cpu_threads() -> int:
@@ -433,51 +546,25 @@ def cpu_threads() -> int:
 
 
 def run_reference(args, w, ws_n, rank):
-    """The oracle, as it stands, on host cores.  Each step is one (layer,
-    sequence, KV head) unit of the workload (units of the first layer,
-    reused cyclically); the full-step time is extrapolated from the mean."""
+    """The oracle, as it stands, on the host cores.  Each timed sample is one
+    (layer, sequence, KV head) unit of the workload (the shared unit sample);
+    ms_per_step is the time of one sample, and the value is steps/s of the
+    whole workload, extrapolated from the mean unit time."""
     if rank != 0:
         return
-    import oracle
-    from oracle import layout
-    from synth.gen import abi_to_numpy
-    G = w.group
-    p_head = gen.per_head_fraction(w.expand_frac, G)
-    d = gen.decode_cache(w, 0, device="cpu")
-    g = gen._gen(w.seed * 7919 + 1)
-    q = gen.query(g, w.batch, w.n_q_heads).float().numpy()
-    W = gen.routing_weights(g, w.n_kv_heads).numpy()
-    arr = abi_to_numpy(d)
-    units = []
-    for b in range(w.batch):
-        for c in range(w.n_kv_heads):
-            if len(units) >= min(8, args.steps + args.warmup):
-                break
-            cache = layout.unpack_layer(_group_arrays(arr, b, c), w.n_sink, w.n_recent)
-            qg, Wg = q[b:b + 1, c * G:(c + 1) * G], W[c:c + 1]
-            z = oracle.route_logits(qg, Wg, cache)
-            theta = np.array([gen.pick_threshold(z[0][h], p_head) for h in range(G)])
-            units.append((cache, qg, Wg, theta))
-    times = []
-    for i in range(args.warmup + args.steps):
-        cache, qg, Wg, theta = units[i % len(units)]
-        t0 = time.perf_counter()
-        E, _ = oracle.route(qg, Wg, cache, theta)
-        oracle.decode_attention(qg, cache, E, 1.0 / math.sqrt(128.0))
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    per_step = float(np.mean(times)) * w.batch * w.n_kv_heads * w.layers
-    value = 1.0 / per_step
-    desc = (f"oracle routing + attention (fp64 numpy), {args.steps} timed units of one "
-            f"(layer, sequence, KV head) each, cycling over {len(units)} units of layer 0; "
-            f"steps/s = 1 / (mean unit time x {w.batch * w.n_kv_heads} units x {w.layers} layers)")
+    units = oracle_units(w, min(8, args.steps + args.warmup))
+    times = time_units(units, args.warmup, args.steps)
+    units_per_step = w.batch * w.n_kv_heads * w.layers
+    mean = float(np.mean(times))
+    value = 1.0 / (mean * units_per_step)
+    desc = (f"{UNITS_PER_STEP_DOC}; {args.steps} units timed after {args.warmup} warm-up, "
+            f"cycling over the first {len(units)} groups of layer 0 (drawn on the CPU); steps/s "
+            f"= 1 / (mean unit time x {units_per_step} units per step)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+            "step_is": "one (layer, sequence, KV head) unit", "units_per_step": units_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch,
-                       "ctx": w.ctx, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
-                       "expand_frac": w.expand_frac},
+            "data": "synthetic", "impl": "reference", "config": decode_config(w, ws_n),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -641,6 +728,10 @@ def run_fullkv_bench(args, ws_n, rank, local):
 
 def main():
     args = parse()
+    if args.traffic_from:
+        write_traffic(args.traffic_from, args.traffic_workload, args.traffic_scale,
+                      args.traffic_command)
+        return
     ws_n, rank, local = dist_setup(args)
     if args.impl == "reference" and args.path != "decode":
         if rank == 0:
@@ -679,15 +770,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "ctx": w.ctx,
-                       "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
-                       "expand_frac_target": w.expand_frac,
-                       "expand_frac": sum(L["n_exp"] for L in layers) /
-                       max(1, sum(L["n_nonempty"] for L in layers)),
-                       "bases": "hbm-resident", "l2": "inputs larger than L2 "
-                       f"({bytes_step / 1e9:.2f} GB touched per step, distinct per layer)",
-                       "parallelism": f"replicas x{ws_n}",
-                       "graph": "one CUDA graph per step, programmatic dependent launch"},
+            "config": decode_config(w, ws_n),
+            "workload_stats": {"expand_frac": sum(L["n_exp"] for L in layers) /
+                               max(1, sum(L["n_nonempty"] for L in layers)),
+                               "gb_touched_per_step": bytes_step / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                          "peak_kind": peak_kind, "kernel": "sekv::decode_kernel",
@@ -706,16 +792,8 @@ def main():
                        "steps": e_steps, "max_abs_vs_resident": err}
         line["gpu_launches"] += e_steps * nl
     if not args.no_cpu_baseline and rank == 0:
-        from synth.gen import abi_to_numpy
-        la = []
-        for l in range(min(2, len(layers))):
-            L = layers[l]
-            la.append((l, abi_to_numpy(L["t"]), L["q"].float().cpu().numpy(),
-                       L["W"].cpu().numpy()))
-        mean_t, units, desc = oracle_sample(w, la, args.cpu_seconds)
-        v = 1.0 / (mean_t * w.batch * w.n_kv_heads * w.layers)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(),
-                                "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = cpu_baseline_leg(w, args.cpu_seconds)
+        line["parity"] = parity_check(sk, cfg, ws, layers[0], w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:

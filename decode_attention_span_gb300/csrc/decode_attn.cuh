@@ -39,7 +39,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kGran = 1024;                   // arena granule (TMA swizzle alignment)
 constexpr int kArenaGran = 24;                // arena of one warp, in granules
 constexpr int kArenaBytes = kArenaGran * kGran;
-constexpr int kMaxItems = 6;                  // items in flight per warp
+constexpr int kMaxItems = 2;                  // items in flight per warp
 constexpr int kRows = 16;                     // rows per full-resolution / summary page
 constexpr int kRowHalf = kRows * 128;         // one 128-byte half of a page's rows (2 KB)
 constexpr int kRowPageBytes = 4 * kRowHalf;   // K and V, both halves (8 KB)
@@ -53,7 +53,7 @@ constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) gr
 constexpr int kStaticPages = 2;               // full-resolution pages each CTA owns
 constexpr int kPoolClaim = 2;                 // pages per claim from the group's pool
 constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
-constexpr int kPrologueItems = 2;             // items per warp issued before the query
+constexpr int kPrologueItems = 1;             // items per warp issued before the query
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffArena = 0;

@@ -326,15 +326,16 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 
   // ---- the query (and in list mode the lists) come from earlier work ------
   pdl_wait();
-  // y = W_r q, rows 8w .. 8w + 7 of this warp: lane (r = lane / 4, quarter
-  // d = lane % 4) takes 32 of the 128 head dims (W_r is read here, in the
-  // same round trip as q, rather than held in registers across the wait)
+  // y = W_r q, rows 8w .. 8w + 7 of this warp: lane (r = lane / 4, dq =
+  // lane % 4) takes head dims 16 i + 4 dq .. + 3, i = 0..7 (the four dq of a
+  // row read adjacent 16-byte chunks: no bank conflicts on q).  W_r is read
+  // here, in the same round trip as q, not held in registers across the wait.
   float4 wr[8];
   if (P.fused) {
     const float4* wrow = reinterpret_cast<const float4*>(
-        P.W_r + (size_t(C.c) * kRouteDim + 8 * w + (lane >> 2)) * kHeadDim + 32 * (lane & 3));
+        P.W_r + (size_t(C.c) * kRouteDim + 8 * w + (lane >> 2)) * kHeadDim + 4 * (lane & 3));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wr[i] = __ldg(wrow + i);
+    for (int i = 0; i < 8; ++i) wr[i] = __ldg(wrow + 4 * i);
   }
   float* qf = reinterpret_cast<float*>(smem + kOffQf);
   {
@@ -379,7 +380,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 32 * dq + 4 * i);
+        const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 16 * i + 4 * dq);
         acc[h] = fmaf(wr[i].w, qv.w, fmaf(wr[i].z, qv.z, fmaf(wr[i].y, qv.y,
                       fmaf(wr[i].x, qv.x, acc[h]))));
       }

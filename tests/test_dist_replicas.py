@@ -76,11 +76,51 @@ def test_reference_arm_is_decode_only():
         assert line["impl"] == "reference" and "unavailable" in line
 
 
-def test_profiled_traffic_covers_its_own_workload_only():
-    """The committed ncu summary's DRAM bytes are reported only for the
-    workload it was taken on (and only while the kernel sources match)."""
+def test_profiled_traffic_covers_its_own_workload_only(tmp_path, monkeypatch):
+    """DRAM bytes per launch are reported only for the workload the capture
+    covers, and only while the kernel sources match the capture."""
     sys.path.insert(0, ROOT)
     import bench
+    csv_path = tmp_path / "cap.csv"
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"\n')
+    rows = []
+    for i, (rd, wr) in enumerate([(60.0, 1.5), (62.0, 1.5)]):
+        for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr)):
+            rows.append(f'"{i}","1","python","h","void sekv::decode_kernel<2>(sekv::DecodeParams)",'
+                        f'"1","7","(256, 1, 1)","(19, 8, 1)","0","10.3","Command line profiler '
+                        f'metrics","{m}","Mbyte","{v}"\n')
+    rows.append('"2","1","python","h","other_kernel","1","7","(1,1,1)","(1,1,1)","0","10.3",'
+                '"x","dram__bytes_read.sum","Mbyte","999"\n')
+    csv_path.write_text("==PROF== noise\n" + hdr + "".join(rows))
+    out = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_JSON", str(out))
+    bench.write_traffic(str(csv_path), "llama3_8b_128k", 8.0, "cmd")
+    # mean of (61.5, 63.5) MB per captured launch, scaled by 8
+    assert bench.profiled_traffic("llama3_8b_128k") == 8 * 62_500_000
     assert bench.profiled_traffic("qwen2_7b_stress") is None
-    t = bench.profiled_traffic("llama3_8b_128k")
-    assert t is None or (isinstance(t, int) and t > 0)
+    monkeypatch.setattr(bench, "decode_source_hash", lambda: "changed")
+    assert bench.profiled_traffic("llama3_8b_128k") is None
+
+
+def test_reference_arm_times_units_and_names_them():
+    """--impl reference: each timed sample is one (layer, sequence, KV head)
+    unit, ms_per_step is that sample's time (so steps x ms_per_step is the
+    timed wall time), the value is extrapolated to whole steps, and the
+    config is the sekv arm's."""
+    import json
+    import subprocess
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                        "--warmup", "1", "--config", "llama3_8b_32k", "--layers", "2"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    w = synth.get_config("llama3_8b_32k", layers=2)
+    assert line["impl"] == "reference" and line["steps"] == 3
+    assert line["units_per_step"] == 1 * 8 * 2
+    assert line["value"] == pytest.approx(1e3 / (line["ms_per_step"] * 16), rel=1e-9)
+    assert line["config"] == bench.decode_config(w, 1)
