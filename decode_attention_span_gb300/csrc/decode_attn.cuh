@@ -39,7 +39,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kGran = 1024;                   // arena granule (TMA swizzle alignment)
 constexpr int kArenaGran = 24;                // arena of one warp, in granules
 constexpr int kArenaBytes = kArenaGran * kGran;
-constexpr int kMaxItems = 2;                  // items in flight per warp
+constexpr int kMaxItems = 2;                  // items in flight per warp (main loop)
+constexpr int kSlots = 4;                     // item slots (descriptor + mbarrier) per warp
 constexpr int kRows = 16;                     // rows per full-resolution / summary page
 constexpr int kRowHalf = kRows * 128;         // one 128-byte half of a page's rows (2 KB)
 constexpr int kRowPageBytes = 4 * kRowHalf;   // K and V, both halves (8 KB)
@@ -53,7 +54,8 @@ constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) gr
 constexpr int kStaticPages = 2;               // full-resolution pages each CTA owns
 constexpr int kPoolClaim = 2;                 // pages per claim from the group's pool
 constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
-constexpr int kPrologueItems = 1;             // items per warp issued before the query
+constexpr int kPrologueItems = 2;             // items per warp issued before the query
+constexpr int kWrSliceBytes = 8 * kHeadDim * 4;  // W_r rows of one warp (4 KB)
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffArena = 0;
@@ -72,6 +74,7 @@ static_assert(kSmemBytes - kOffQfrag >= 16 * 1024 + 1024, "over-read margin");
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 enum ItemType : int {
+  IT_WR = 8,     // rows 8w .. 8w + 7 of W_r for warp w (consumed before routing)
   IT_ROUTE = 1,  // routing summaries of kRouteSpans spans (consumed before the barrier)
   IT_FULL = 2,   // kRows full-resolution rows (K and V), the CTA's own or from the pool
   IT_SUM = 3,    // kRows summary rows (K and V) of unexpanded spans
@@ -181,8 +184,8 @@ struct WarpQ {
 struct SmemMisc {
   Ctx ctx;
   WarpQ wq[kWarps];
-  Item desc[kWarps][kMaxItems];
-  uint64_t bar[kWarps][kMaxItems];
+  Item desc[kWarps][kSlots];
+  uint64_t bar[kWarps][kSlots];
   uint64_t cmb_bar;        // last CTA of a group: a chunk of partials landed
   unsigned int pmask[kMaxRoutePages];  // fused: expanded spans per routing page
   float theta[8];

@@ -3,7 +3,8 @@
 //
 // Per warp: an arena of kArenaGran granules used as a ring (items are placed
 // contiguously, wrapping to the arena start when one does not fit at the
-// end), up to kMaxItems items in flight, each with its own mbarrier.  The
+// end), up to kMaxItems items in flight (kSlots before routing: the routing
+// weights and up to two routing pages), each with its own mbarrier.  The
 // warp issues and consumes its items itself, in order, so no handover
 // between warps is needed; the only CTA-wide synchronisation is the routing
 // barrier (every span of the CTA routed, the record list final) and the
@@ -155,7 +156,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
       }
       const int start = arena_place(Q, bytes);
       if (start < 0) break;  // the claim stays pending until space frees
-      const int slot = Q.ni % kMaxItems;
+      const int slot = Q.ni % kSlots;
       const int gsz = int((bytes + kGran - 1) / kGran);
       it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
       it.end = start + gsz;
@@ -187,7 +188,7 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
                                             const DecodeParams& P, int nd, WarpAcc& A,
                                             ExpAcc<KS>& X) {
   const int w = threadIdx.x >> 5;
-  const Item it = ms->desc[w][nd % kMaxItems];
+  const Item it = ms->desc[w][nd % kSlots];
   const uint8_t* base = smem + it.boff;
   const uint32_t bu = smem_u32(base);
   const float* bias = reinterpret_cast<const float*>(smem + kOffBias);
@@ -241,7 +242,7 @@ __device__ __forceinline__ void issue_route_page(uint8_t* smem, SmemMisc* ms,
   it.a = C.k0 + kRouteSpans * p;
   it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
   it.end = start + kRoutePageBytes / kGran;
-  const int slot = Q.ni % kMaxItems;
+  const int slot = Q.ni % kSlots;
   arm_item(ms, w, slot, it, kRoutePageBytes);
   tma_g2s_4d_hint(smem + it.boff, &P.tm_sroute, 0, it.a, 0, C.g, &ms->bar[w][slot],
                   policy_evict_first());
@@ -262,9 +263,9 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   bool hit = false, landed = false;
   int end = 0;
   if (ms->wq[w].ok) {
-    landed = mbar_wait_parked(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1));
+    landed = mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1));
     if (landed) {
-      const Item it = ms->desc[w][nd % kMaxItems];
+      const Item it = ms->desc[w][nd % kSlots];
       end = it.end;
       hit = route32(smem + it.boff, ys, ms->theta, P.G);
     } else if (lane == 0) {
@@ -305,7 +306,22 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   const Ctx& C = ms->ctx;
   const int G = P.G;
 
-  // ---- prologue: routing pages and the first own pages (no q needed) -----
+  // ---- prologue: routing weights, routing pages and the first own pages
+  // (no q needed; the caller allows W_r to be read before the wait) --------
+  // rows 8w .. 8w + 7 of W_r (4 KB) land as this warp's first item
+  if (P.fused && lane == 0) {
+    WarpQ& Q = ms->wq[w];
+    const int start = arena_place(Q, kWrSliceBytes);
+    Item it{};
+    it.type = IT_WR;
+    it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
+    it.end = start + kWrSliceBytes / kGran;
+    arm_item(ms, w, Q.ni % kSlots, it, kWrSliceBytes);
+    bulk_g2s_hint(smem + it.boff, P.W_r + (size_t(C.c) * kRouteDim + 8 * w) * kHeadDim,
+                  kWrSliceBytes, &ms->bar[w][Q.ni % kSlots], policy_evict_last());
+    Q.head = it.end;
+    ++Q.ni;
+  }
   if (lane == 0) {
     for (int p = w; p < C.n_rp; p += kWarps) issue_route_page(smem, ms, P, p);
   }
@@ -326,17 +342,6 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 
   // ---- the query (and in list mode the lists) come from earlier work ------
   pdl_wait();
-  // y = W_r q, rows 8w .. 8w + 7 of this warp: lane (r = lane / 4, dq =
-  // lane % 4) takes head dims 16 i + 4 dq .. + 3, i = 0..7 (the four dq of a
-  // row read adjacent 16-byte chunks: no bank conflicts on q).  W_r is read
-  // here, in the same round trip as q, not held in registers across the wait.
-  float4 wr[8];
-  if (P.fused) {
-    const float4* wrow = reinterpret_cast<const float4*>(
-        P.W_r + (size_t(C.c) * kRouteDim + 8 * w + (lane >> 2)) * kHeadDim + 4 * (lane & 3));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wr[i] = __ldg(wrow + 4 * i);
-  }
   float* qf = reinterpret_cast<float*>(smem + kOffQf);
   {
     // q as f32 [8][128] (rows past the group zero) for the routing projection
@@ -371,18 +376,30 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   __syncthreads();
 
   if (P.fused) {
+    // y = W_r q, rows 8w .. 8w + 7 of this warp, from the slice in its arena:
+    // lane (r = lane / 4, dq = lane % 4) sums the head-dim chunks (16 bytes)
+    // c = dq + 4 m, m = 0..7, in the rotated order m = (i + r) mod 8, so that
+    // at each step i the 32 lanes read 32 different chunks (no bank conflicts
+    // on W_r rows 512 bytes apart, nor on q)
     float* ys = reinterpret_cast<float*>(smem + kOffY);
+    const int nd = ms->wq[w].nd;
+    const bool wr_ok =
+        mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1));
+    if (!wr_ok && lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
+    const Item wit = ms->desc[w][nd % kSlots];
+    const float* wrs = reinterpret_cast<const float*>(smem + wit.boff);
+    const int r = lane >> 2, dq = lane & 3;
     float acc[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-    const int dq = lane & 3;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
+      const int c = dq + 4 * ((i + r) & 7);
+      const float4 wv = *reinterpret_cast<const float4*>(wrs + r * kHeadDim + 4 * c);
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 16 * i + 4 * dq);
-        acc[h] = fmaf(wr[i].w, qv.w, fmaf(wr[i].z, qv.z, fmaf(wr[i].y, qv.y,
-                      fmaf(wr[i].x, qv.x, acc[h]))));
+        const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 4 * c);
+        acc[h] = fmaf(wv.w, qv.w, fmaf(wv.z, qv.z, fmaf(wv.y, qv.y, fmaf(wv.x, qv.x, acc[h]))));
       }
     }
 #pragma unroll
@@ -392,7 +409,13 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     }
     if (dq == 0) {
 #pragma unroll
-      for (int h = 0; h < 8; ++h) ys[h * kRouteDim + 8 * w + (lane >> 2)] = acc[h];
+      for (int h = 0; h < 8; ++h) ys[h * kRouteDim + 8 * w + r] = acc[h];
+    }
+    if (wr_ok) {
+      retire_item(ms, nd, wit.end);
+    } else {
+      __syncwarp();
+      if (lane == 0) ms->wq[w].ok = 0;
     }
     __syncthreads();
 #pragma unroll
@@ -483,7 +506,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     issue_more(smem, ms, P, true, claim);
     const int nd = ms->wq[w].nd;
     if (nd == ms->wq[w].ni || !ms->wq[w].ok) break;
-    if (!mbar_wait_parked(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1))) {
+    if (!mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1))) {
       __syncwarp();
       if (lane == 0) {
         set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);
@@ -499,7 +522,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   {
     const int ni = ms->wq[w].ni;
     for (int nd = ms->wq[w].nd; nd < ni; ++nd) {
-      if (!mbar_wait(&ms->bar[w][nd % kMaxItems], uint32_t((nd / kMaxItems) & 1),
+      if (!mbar_wait(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1),
                      kWaitLimit)) {
         if (lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 3);
         break;
@@ -663,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < kMaxItems; ++s) mbar_init(&ms->bar[w][s], 1);
+      for (int s = 0; s < kSlots; ++s) mbar_init(&ms->bar[w][s], 1);
     mbar_init(&ms->cmb_bar, 1);
     ms->n_rec = 0;
     ms->rec_next = 0;
