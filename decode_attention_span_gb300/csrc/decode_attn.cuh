@@ -41,18 +41,21 @@ constexpr int kArenaGran = 24;                // arena of one warp, in granules
 constexpr int kArenaBytes = kArenaGran * kGran;
 constexpr int kMaxItems = 2;                  // items in flight per warp (main loop)
 constexpr int kSlots = 4;                     // item slots (descriptor + mbarrier) per warp
-constexpr int kRows = 16;                     // rows per full-resolution / summary page
-constexpr int kRowHalf = kRows * 128;         // one 128-byte half of a page's rows (2 KB)
+constexpr int kRows = 16;                     // rows per summary page (one mma tile)
+constexpr int kRowHalf = kRows * 128;         // one 128-byte half of a summary page's rows (2 KB)
 constexpr int kRowPageBytes = 4 * kRowHalf;   // K and V, both halves (8 KB)
+constexpr int kFullRows = 32;                 // rows per full-resolution page (two tiles)
+constexpr int kFullHalf = kFullRows * 128;    // one 128-byte half of its rows (4 KB)
+constexpr int kFullPageBytes = 4 * kFullHalf; // K and V, both halves (16 KB)
 constexpr int kRouteSpans = 32;               // spans per routing page
 constexpr int kRoutePageBytes = kRouteSpans * 256;  // 8 KB
 constexpr int kSpanCap = 512;                 // spans of one CTA (bias cache, entries)
 constexpr int kMaxRoutePages = kSpanCap / kRouteSpans;
-constexpr int kWholeMax = 16384;              // records up to this size land whole
+constexpr int kWholeMax = 20480;              // records up to this size land whole
 constexpr int kTileMax = 12288;               // U-row tiles of larger records
 constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) group
-constexpr int kStaticPages = 2;               // full-resolution pages each CTA owns
-constexpr int kPoolClaim = 2;                 // pages per claim from the group's pool
+constexpr int kStaticPages = 1;               // full-resolution pages each CTA owns
+constexpr int kPoolClaim = 1;                 // pages per claim from the group's pool
 constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
 constexpr int kPrologueItems = 2;             // items per warp issued before the query
 constexpr int kWrSliceBytes = 8 * kHeadDim * 4;  // W_r rows of one warp (4 KB)
@@ -76,7 +79,7 @@ static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 enum ItemType : int {
   IT_WR = 8,     // rows 8w .. 8w + 7 of W_r for warp w (consumed before routing)
   IT_ROUTE = 1,  // routing summaries of kRouteSpans spans (consumed before the barrier)
-  IT_FULL = 2,   // kRows full-resolution rows (K and V), the CTA's own or from the pool
+  IT_FULL = 2,   // kFullRows full-resolution rows (K and V), the CTA's own or from the pool
   IT_SUM = 3,    // kRows summary rows (K and V) of unexpanded spans
   IT_REC = 4,    // one whole basis record
   IT_KEY = 5,    // key part of a split record (header, sigma_K, g_K, Vt_K)

@@ -91,21 +91,23 @@ __device__ __forceinline__ float rebase_if_needed(WarpAcc& A, float mx) {
   return alpha;
 }
 
-// One full-resolution or summary page: up to kRows (16) rows whose two
-// 128-byte halves are 128B-swizzled boxes (keys: dims 0-63 at kb, 64-127 at
-// kb + kRowHalf; values likewise at vb), folded into the warp's softmax state
-// with at most one rescale.  bias_row: for summary pages the logit bias of
-// the page's spans (log2|S|, or -inf for a span that does not enter as a
-// summary); nullptr for full rows.  Rows >= n are masked.
+// One tile of 16 full-resolution or summary rows whose two 128-byte halves
+// sit in 128B-swizzled boxes `half` bytes apart (keys: dims 0-63 at kb,
+// 64-127 at kb + half; values likewise at vb; kb and vb point at the tile's
+// first row, and a box's swizzle runs on in its later rows), folded into the
+// warp's softmax state with at most one rescale.  bias_row: for summary pages
+// the logit bias of the page's spans (log2|S|, or -inf for a span that does
+// not enter as a summary); nullptr for full rows.  Rows >= n are masked.
 __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
-                                               const float* bias_row, float scale_log2) {
+                                               const float* bias_row, float scale_log2,
+                                               int half) {
   const int lane = threadIdx.x & 31;
   float s[2][2];
   s[0][0] = s[0][1] = s[1][0] = s[1][1] = 0.f;
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {  // 32 head dims per step
     const uint4 q = lds128(A.qfrag + (i * 32 + lane) * 16);
-    const uint32_t box = kb + (i >> 1) * kRowHalf;
+    const uint32_t box = kb + (i >> 1) * half;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       uint32_t b0, b1, b2, b3;
@@ -148,8 +150,7 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
   for (int dp = 0; dp < 8; ++dp) {
     const int d0 = 16 * dp;
     uint32_t b0, b1, b2, b3;
-    ldsm_x4_t(swz128(vb + (d0 >> 6) * kRowHalf, key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1, b2,
-              b3);
+    ldsm_x4_t(swz128(vb + (d0 >> 6) * half, key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1, b2, b3);
     b0 &= t0; b2 &= t0; b1 &= t1; b3 &= t1;
     mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], a0, a2, b0, b1);
     mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], a0, a2, b2, b3);

@@ -117,11 +117,11 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
       if (Q.pk != 2) {
         const bool full = Q.pk == 3 || Q.pidx < C.n_own;
         it.type = full ? IT_FULL : IT_SUM;
-        it.a = Q.pk == 3 ? kRows * (Q.pidx + Q.ppart)
-                         : (full ? kRows * (C.own0 + Q.pidx) : C.k0 + kRows * (Q.pidx - C.n_own));
-        const int e = full ? C.n_full : C.k1;
-        it.n = (e - it.a) < kRows ? (e - it.a) : kRows;
-        bytes = kRowPageBytes;
+        it.a = Q.pk == 3 ? kFullRows * (Q.pidx + Q.ppart)
+                         : (full ? kFullRows * (C.own0 + Q.pidx) : C.k0 + kRows * (Q.pidx - C.n_own));
+        const int e = full ? C.n_full : C.k1, rows = full ? kFullRows : kRows;
+        it.n = (e - it.a) < rows ? (e - it.a) : rows;
+        bytes = full ? kFullPageBytes : kRowPageBytes;
       } else {
         const RecEntry en = ents[Q.pidx];
         const int b = en.body, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
@@ -166,8 +166,8 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
       if (Q.pk != 2) {
         const bool full = it.type == IT_FULL;
         tma_g2s_4d_hint(dst, full ? &P.tm_kfull : &P.tm_ksum, 0, it.a, 0, C.g, bar, pol);
-        tma_g2s_4d_hint(dst + 2 * kRowHalf, full ? &P.tm_vfull : &P.tm_vsum, 0, it.a, 0, C.g,
-                        bar, pol);
+        tma_g2s_4d_hint(dst + (full ? 2 * kFullHalf : 2 * kRowHalf), full ? &P.tm_vfull : &P.tm_vsum,
+                        0, it.a, 0, C.g, bar, pol);
       } else {
         const uint8_t* rec = P.store + roff;
         if (n0) bulk_g2s_hint(dst, rec + s0, n0, bar, pol);
@@ -192,9 +192,14 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
   const uint8_t* base = smem + it.boff;
   const uint32_t bu = smem_u32(base);
   const float* bias = reinterpret_cast<const float*>(smem + kOffBias);
-  if (it.type == IT_FULL || it.type == IT_SUM) {
-    consume_rows16(A, bu, bu + 2 * kRowHalf, it.n,
-                   it.type == IT_SUM ? bias + (it.a - ms->ctx.k0) : nullptr, P.scale_log2);
+  if (it.type == IT_FULL) {
+    // two 16-row tiles (the second one only if the page has rows there)
+    for (int t0 = 0; t0 < it.n; t0 += kRows)
+      consume_rows16(A, bu + t0 * 128, bu + 2 * kFullHalf + t0 * 128, it.n - t0, nullptr,
+                     P.scale_log2, kFullHalf);
+  } else if (it.type == IT_SUM) {
+    consume_rows16(A, bu, bu + 2 * kRowHalf, it.n, bias + (it.a - ms->ctx.k0), P.scale_log2,
+                   kRowHalf);
   } else {
     int off_key = -1, off_uk = 0, off_uv = 0, off_val = -1, n = 0;
     if (it.type == IT_REC) {
@@ -592,13 +597,13 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   const int cg = P.cg;
   const float* parts = P.partials + size_t(C.g) * cg * pstride;
   const float* cbuf = reinterpret_cast<const float*>(smem);  // chunk of partials
+  float* sc = reinterpret_cast<float*>(smem + kMergeChunk * sizeof(Partial));  // [32][8] scales
+  float* MLa = sc + kMergeChunk * 8;  // running M[8], L[8], and this chunk's rescale a[8]
   const int d = tid & (kHeadDim - 1), hsel = tid >> 7;  // this thread: dim d of heads hsel + 2i
-  float Mh[4], Lh[4], Oh[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    Mh[i] = kNegInf;
-    Lh[i] = 0.f;
-    Oh[i] = 0.f;
+  float Oh[4] = {0.f, 0.f, 0.f, 0.f};
+  if (tid < 8) {
+    MLa[tid] = kNegInf;
+    MLa[8 + tid] = 0.f;
   }
   for (int c0 = 0, ph = 0; c0 < cg; c0 += kMergeChunk, ph ^= 1) {
     const int nc = (cg - c0) < kMergeChunk ? (cg - c0) : kMergeChunk;
@@ -611,40 +616,61 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     // every thread takes every barrier of this loop, even after a timeout
     const bool landed = mbar_wait(&ms->cmb_bar, uint32_t(ph), kWaitLimit);
     if (!landed && tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 7);
+    // warp h: log-sum-exp statistics of head h over the chunk's CTAs (lane =
+    // CTA), one shuffle reduction each, and every CTA's rescale factor
+    if (w < G) {
+      const float m = (landed && lane < nc) ? cbuf[lane * pstride + w] : kNegInf;
+      const float l = (landed && lane < nc) ? cbuf[lane * pstride + 8 + w] : 0.f;
+      float mc = m;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
+      const float m_old = MLa[w];
+      const float m_new = fmaxf(m_old, mc);
+      const float s_j = (m_new == kNegInf) ? 0.f : exp2f(m - m_new);
+      float lc = l * s_j;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lc += __shfl_xor_sync(kFull, lc, o);
+      if (lane < kMergeChunk) sc[lane * 8 + w] = s_j;
+      __syncwarp();
+      if (lane == 0) {
+        const float a = (m_new == kNegInf) ? 1.f : exp2f(m_old - m_new);  // 0 on the first chunk
+        MLa[16 + w] = a;
+        MLa[w] = m_new;
+        MLa[8 + w] = MLa[8 + w] * a + lc;
+      }
+    }
+    __syncthreads();
+    // every thread: its outputs, rescaled, plus the chunk's weighted sums
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int h = hsel + 2 * i;
-      if (!landed || h >= G) continue;
-      float m_new = Mh[i];
-      for (int jj = 0; jj < nc; ++jj) m_new = fmaxf(m_new, cbuf[jj * pstride + h]);
-      if (m_new == kNegInf) continue;
-      const float a = exp2f(Mh[i] - m_new);  // 0 for the first chunk
-      float l = Lh[i] * a, o = Oh[i] * a;
-      for (int jj = 0; jj < nc; ++jj) {
-        const float* pj = cbuf + jj * pstride;
-        const float sc = exp2f(pj[h] - m_new);
-        l = fmaf(pj[8 + h], sc, l);
-        o = fmaf(pj[16 + h * kHeadDim + d], sc, o);
+      if (h >= G) continue;
+      float o0 = Oh[i] * MLa[16 + h], o1 = 0.f, o2 = 0.f, o3 = 0.f;
+      int jj = 0;
+      for (; jj + 4 <= nc; jj += 4) {
+        o0 = fmaf(cbuf[(jj + 0) * pstride + 16 + h * kHeadDim + d], sc[(jj + 0) * 8 + h], o0);
+        o1 = fmaf(cbuf[(jj + 1) * pstride + 16 + h * kHeadDim + d], sc[(jj + 1) * 8 + h], o1);
+        o2 = fmaf(cbuf[(jj + 2) * pstride + 16 + h * kHeadDim + d], sc[(jj + 2) * 8 + h], o2);
+        o3 = fmaf(cbuf[(jj + 3) * pstride + 16 + h * kHeadDim + d], sc[(jj + 3) * 8 + h], o3);
       }
-      Mh[i] = m_new;
-      Lh[i] = l;
-      Oh[i] = o;
+      for (; jj < nc; ++jj)
+        o0 = fmaf(cbuf[jj * pstride + 16 + h * kHeadDim + d], sc[jj * 8 + h], o0);
+      Oh[i] = (o0 + o1) + (o2 + o3);
     }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int h = hsel + 2 * i;
     if (h < G) {
+      const float L = MLa[8 + h];
       const size_t row = size_t(C.b) * P.Hq + size_t(C.c) * G + h;
-      P.out[row * kHeadDim + d] = Lh[i] > 0.f ? Oh[i] / Lh[i] : 0.f;
-      if (d == 0 && P.lse != nullptr)
-        P.lse[row] = Lh[i] > 0.f ? (Mh[i] + log2f(Lh[i])) * kLn2 : kNegInf;
+      P.out[row * kHeadDim + d] = L > 0.f ? Oh[i] / L : 0.f;
+      if (d == 0 && P.lse != nullptr) P.lse[row] = L > 0.f ? (MLa[h] + log2f(L)) * kLn2 : kNegInf;
     }
   }
   if (P.fused && P.expanded_out != nullptr) {
     // the CTAs' ascending lists, one after the other
-    int* pre = reinterpret_cast<int*>(smem + kMergeChunk * sizeof(Partial));  // [cg + 1]
-    // (past the largest chunk of partials)
+    int* pre = reinterpret_cast<int*>(MLa + 24);  // [cg + 1]
     __syncthreads();
     if (tid == 0) {
       int acc = 0;
@@ -703,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     C.n_sp = P.n_spans[C.b];
     C.n_full = P.n_sink + C.n_sp + P.n_recent;
     span_range(C.j, P.cg, C.n_sp, C.k0, C.k1);
-    C.n_fp = (C.n_full + kRows - 1) / kRows;
+    C.n_fp = (C.n_full + kFullRows - 1) / kFullRows;
     C.own0 = kStaticPages * C.j;
     const int own = C.n_fp - C.own0;
     C.n_own = own < 0 ? 0 : (own > kStaticPages ? kStaticPages : own);

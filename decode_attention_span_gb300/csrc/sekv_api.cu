@@ -232,8 +232,8 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   const int ng = L.ng;
   const uint64_t cap_full = uint64_t(cfg->n_sink) + cfg->max_spans + cfg->n_recent;
   bool ok = true;
-  ok &= encode_rows4d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, kRows);
-  ok &= encode_rows4d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, kRows);
+  ok &= encode_rows4d(&P.tm_kfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_full, 128, cap_full, ng, 2, kFullRows);
+  ok &= encode_rows4d(&P.tm_vfull, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_full, 128, cap_full, ng, 2, kFullRows);
   ok &= encode_rows4d(&P.tm_ksum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k_sum, 128, cfg->max_spans, ng, 2, kRows);
   ok &= encode_rows4d(&P.tm_vsum, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v_sum, 128, cfg->max_spans, ng, 2, kRows);
   if (fused) {
