@@ -349,35 +349,28 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   pdl_wait();
   float* qf = reinterpret_cast<float*>(smem + kOffQf);
   {
-    // q as f32 [8][128] (rows past the group zero) for the routing projection
+    // one round trip: thread t loads q[h][d .. d + 3] (h = t / 32, d = 4 (t % 32);
+    // rows past the group read as zero) and, for t < 8, theta.  It stores
+    // them as f32 for the routing projection and as the bf16 pairs of the
+    // query's mma A fragments (rows 0..7 = heads, grouped by 32 dims: pair
+    // (h, 32 i + 8 k + 2 j) is component k of lane 4 h + j's fragment i).
     const int h = tid >> 5, d = 4 * (tid & 31);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (h < G) {
-      const __nv_bfloat16* qr = P.q + (size_t(C.b) * P.Hq + size_t(C.c) * G + h) * kHeadDim + d;
-      const uint2 u = *reinterpret_cast<const uint2*>(qr);
-      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-      v = make_float4(lo.x, lo.y, hi.x, hi.y);
-    }
-    *reinterpret_cast<float4*>(qf + h * kHeadDim + d) = v;
-  }
-  if (w == 0) {
-    // query A fragments (rows 0..7 = heads, zero past G), grouped by 32 dims
-    const int r0 = lane >> 2;
-    const __nv_bfloat16* qg = P.q + (size_t(C.b) * P.Hq + size_t(C.c) * G) * kHeadDim;
+    uint2 u = make_uint2(0u, 0u);
+    if (h < G)
+      u = *reinterpret_cast<const uint2*>(P.q + (size_t(C.b) * P.Hq + size_t(C.c) * G + h) *
+                                                    kHeadDim + d);
+    const float th = (P.fused && tid < G) ? P.theta[C.c * G + tid] : 0.f;
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    *reinterpret_cast<float4*>(qf + h * kHeadDim + d) = make_float4(lo.x, lo.y, hi.x, hi.y);
+    uint32_t* qfr = reinterpret_cast<uint32_t*>(smem + kOffQfrag);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int k = 32 * i + 2 * (lane & 3);
-      const __nv_bfloat16* qr = qg + r0 * kHeadDim + k;
-      uint4 v;
-      v.x = r0 < G ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-      v.y = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
-      v.z = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 16) : 0u;
-      v.w = r0 < G ? *reinterpret_cast<const uint32_t*>(qr + 24) : 0u;
-      sts128(smem_u32(smem + kOffQfrag) + (i * 32 + lane) * 16, v);
+    for (int e = 0; e < 2; ++e) {
+      const int dd = d + 2 * e, i = dd >> 5, k = (dd & 31) >> 3, j = (dd & 7) >> 1;
+      qfr[(i * 32 + 4 * h + j) * 4 + k] = e ? u.y : u.x;
     }
+    if (tid < 8) ms->theta[tid] = th;
   }
-  if (P.fused && tid < 8) ms->theta[tid] = tid < G ? P.theta[C.c * G + tid] : 0.f;
   __syncthreads();
 
   if (P.fused) {
