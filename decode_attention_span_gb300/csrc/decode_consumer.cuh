@@ -1,9 +1,14 @@
-// Consumer warps of the decode kernel: routing and the online softmax.
+// Consumer math of the decode kernel: the routing logits and the online
+// softmax over full-resolution rows, summary rows and expanded records.
 //
-// The routines are written rolled (runtime loops, one copy of each body):
-// the whole kernel's code has to stay resident in the SM's instruction cache
-// while four warps run different routines at once.  Operands a rolled loop
-// indexes (the query fragments) sit in a small per-warp shared scratch.
+// Every product runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate) in
+// transposed form: keys, tokens, ranks or head dims are the 16 M rows and
+// the query heads of the GQA group (at most 8) are the N columns, so no
+// tile row is wasted.  A lane (g = lane / 4, q = lane % 4) holds, of an
+// M x 8 result tile, rows g and g + 8 of columns (heads) 2q and 2q + 1.
+// Probabilities and coefficients produced in that layout become the B
+// operand of the next product through movmatrix (an 8 x 8 transpose in
+// registers).  The query's B fragments sit in shared memory (qfrag).
 #pragma once
 
 #include "decode_attn.cuh"
@@ -13,10 +18,11 @@ namespace sekv {
 constexpr float kNegInf = -__builtin_huge_valf();
 
 struct WarpAcc {
-  float o[16][2];  // output accumulator, row r0 = lane/4, dims 8t + 2(lane%4) + {0,1}
-  float m_row;     // running max of row r0 (log2 domain)
-  float l_part;    // this lane's share of the row sum
-  uint32_t qfrag;  // shared address of this warp's query A fragments (4 x 32 lanes x 16 B)
+  float o[8][4];   // O^T tiles: tile t holds dims 16 t + g (c0: head 2q, c1: head 2q + 1)
+                   // and 16 t + g + 8 (c2: head 2q, c3: head 2q + 1)
+  float m[2];      // running max of heads 2q, 2q + 1 (log2 domain; equal in a column)
+  float l[2];      // this lane's share of the sums of heads 2q, 2q + 1
+  uint32_t qfrag;  // shared address of the query's B fragments (4 x 32 lanes x 16 B)
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -33,21 +39,33 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+// D = A * B + D, one m16n8k16 bf16 tile with fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// exp2 of (x - m) that treats an all -inf row as contributing nothing.
-__device__ __forceinline__ void softmax_rescale(float m_old, float m_new, float& alpha,
-                                                float& msub) {
-  if (m_new == kNegInf) {
-    alpha = 1.f;
-    msub = 0.f;
-  } else {
-    alpha = exp2f(m_old - m_new);
-    msub = m_new;
-  }
+// Transpose of an 8 x 8 matrix of bf16 pairs held one row-pair per lane.
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// max / sum over the eight lanes that share a column pair (same lane % 4)
+__device__ __forceinline__ float col_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+__device__ __forceinline__ float col_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
 }
 
 __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -63,32 +81,64 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Lazy online-softmax re-basing: the running max m only moves when a new
-// logit exceeds it by more than kRebase (log2 units), so exponentials stay
-// below 2^kRebase and most tiles skip the shuffles and the rescale.  The
-// output is normalised by the sum taken against the same m, so the choice of
-// m changes only rounding.
+// Lazy online-softmax re-basing: the running max m of a head only moves when
+// a new logit exceeds it by more than kRebase (log2 units), so exponentials
+// stay below 2^kRebase and most tiles skip the reductions and the rescale.
+// The output is normalised by the sum taken against the same m, so the
+// choice of m changes only rounding.
 constexpr float kRebase = 8.f;
 
-// Re-base the warp's state to cover the row maxima mx (rows lane/4) if
-// some lane's exceeds the running max by more than kRebase; returns alpha
-// (1 when nothing moved).
-__device__ __forceinline__ float rebase_if_needed(WarpAcc& A, float mx) {
-  float alpha = 1.f;
-  if (__any_sync(0xffffffffu, mx > A.m_row + kRebase)) {
-    mx = quad_max(mx);
-    const float m_new = fmaxf(A.m_row, mx);
-    float msub;
-    softmax_rescale(A.m_row, m_new, alpha, msub);
-    A.m_row = m_new;
-    A.l_part *= alpha;
+__device__ __forceinline__ float rescale_factor(float m_old, float m_new) {
+  return m_new == kNegInf ? 1.f : exp2f(m_old - m_new);
+}
+
+// Re-base the warp's state to cover this lane's tile maxima mx0, mx1 (heads
+// 2q, 2q + 1) if some lane's exceeds the running max by more than kRebase;
+// returns the two rescale factors (1 when nothing moved).
+__device__ __forceinline__ float2 rebase_if_needed(WarpAcc& A, float mx0, float mx1) {
+  float2 alpha = make_float2(1.f, 1.f);
+  if (__any_sync(0xffffffffu, mx0 > A.m[0] + kRebase || mx1 > A.m[1] + kRebase)) {
+    const float n0 = fmaxf(A.m[0], col_max(mx0)), n1 = fmaxf(A.m[1], col_max(mx1));
+    alpha.x = rescale_factor(A.m[0], n0);
+    alpha.y = rescale_factor(A.m[1], n1);
+    A.m[0] = n0;
+    A.m[1] = n1;
+    A.l[0] *= alpha.x;
+    A.l[1] *= alpha.y;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      A.o[t][0] *= alpha;
-      A.o[t][1] *= alpha;
+    for (int t = 0; t < 8; ++t) {
+      A.o[t][0] *= alpha.x;
+      A.o[t][1] *= alpha.y;
+      A.o[t][2] *= alpha.x;
+      A.o[t][3] *= alpha.y;
     }
   }
   return alpha;
+}
+
+// Probabilities of a 16 x 8 score tile s (rows g, g + 8; heads 2q, 2q + 1)
+// against the running max, added into the sums, and returned as the B
+// fragments (rows = keys/tokens, columns = heads) of the following product.
+__device__ __forceinline__ void probs_to_b(WarpAcc& A, float (&s)[4], uint32_t& b0,
+                                           uint32_t& b1) {
+  const float m0 = A.m[0] == kNegInf ? 0.f : A.m[0];
+  const float m1 = A.m[1] == kNegInf ? 0.f : A.m[1];
+  s[0] = ex2_approx(s[0] - m0);
+  s[1] = ex2_approx(s[1] - m1);
+  s[2] = ex2_approx(s[2] - m0);
+  s[3] = ex2_approx(s[3] - m1);
+  A.l[0] += s[0] + s[2];
+  A.l[1] += s[1] + s[3];
+  b0 = movtrans(pack_bf16(s[0], s[1]));
+  b1 = movtrans(pack_bf16(s[2], s[3]));
+}
+
+// Masks of the bf16 pairs at k indices j, j + 1 (m0) and j + 8, j + 9 (m1),
+// j = base + 2q, against a count (keys, tokens or ranks past it read as 0).
+__device__ __forceinline__ void pair_masks(int base, int count, uint32_t& m0, uint32_t& m1) {
+  const int j = base + 2 * (threadIdx.x & 3);
+  m0 = (j < count ? 0xffffu : 0u) | (j + 1 < count ? 0xffff0000u : 0u);
+  m1 = (j + 8 < count ? 0xffffu : 0u) | (j + 9 < count ? 0xffff0000u : 0u);
 }
 
 // One tile of 16 full-resolution or summary rows whose two 128-byte halves
@@ -98,62 +148,49 @@ __device__ __forceinline__ float rebase_if_needed(WarpAcc& A, float mx) {
 // warp's softmax state with at most one rescale.  bias_row: for summary pages
 // the logit bias of the page's spans (log2|S|, or -inf for a span that does
 // not enter as a summary); nullptr for full rows.  Rows >= n are masked.
+//   S^T (16 keys x 8 heads) = K (16 x 128) q^T, then O^T += V^T P^T.
 __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
                                                const float* bias_row, float scale_log2,
                                                int half) {
-  const int lane = threadIdx.x & 31;
-  float s[2][2];
-  s[0][0] = s[0][1] = s[1][0] = s[1][1] = 0.f;
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  const int krow = (lane & 7) + 8 * (mi & 1);
 #pragma unroll 1
-  for (int i = 0; i < 4; ++i) {  // 32 head dims per step
-    const uint4 q = lds128(A.qfrag + (i * 32 + lane) * 16);
+  for (int i = 0; i < 4; ++i) {  // head dims 32 i .. 32 i + 31: k-steps 2 i, 2 i + 1
+    const uint4 qv = lds128(A.qfrag + (i * 32 + lane) * 16);
     const uint32_t box = kb + (i >> 1) * half;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(swz128(box, 8 * nt + (lane & 7), (i & 1) * 4 + (lane >> 3)), b0, b1, b2, b3);
-      mma_bf16_rows8(s[nt][0], s[nt][1], q.x, q.y, b0, b1);
-      mma_bf16_rows8(s[nt][0], s[nt][1], q.z, q.w, b2, b3);
-    }
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(swz128(box, krow, 4 * (i & 1) + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s0, a0, a1, a2, a3, qv.x, qv.y);
+    ldsm_x4(swz128(box, krow, 4 * (i & 1) + 2 + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s1, a0, a1, a2, a3, qv.z, qv.w);
   }
-  float mx = kNegInf;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = 8 * nt + 2 * (lane & 3) + e;
-      bool valid = key < n;
-      float bias = 0.f;
-      if (bias_row != nullptr && valid) {
-        bias = bias_row[key];
-        valid = bias != kNegInf;
-      }
-      s[nt][e] = valid ? fmaf(s[nt][e], scale_log2, bias) : kNegInf;
-      mx = fmaxf(mx, s[nt][e]);
-    }
-  rebase_if_needed(A, mx);
-  const float msub = A.m_row == kNegInf ? 0.f : A.m_row;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) s[nt][e] = ex2_approx(s[nt][e] - msub);
-  A.l_part += (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
-  const int mi = lane >> 3;
-  const uint32_t a0 = pack_bf16(s[0][0], s[0][1]);
-  const uint32_t a2 = pack_bf16(s[1][0], s[1][1]);
+  float s[4];
+  float bias0 = 0.f, bias1 = 0.f;
+  bool v0 = g < n, v1 = g + 8 < n;
+  if (bias_row != nullptr) {
+    bias0 = v0 ? bias_row[g] : kNegInf;
+    bias1 = v1 ? bias_row[g + 8] : kNegInf;
+    v0 = v0 && bias0 != kNegInf;
+    v1 = v1 && bias1 != kNegInf;
+  }
+  s[0] = v0 ? fmaf(s0[0] + s1[0], scale_log2, bias0) : kNegInf;
+  s[1] = v0 ? fmaf(s0[1] + s1[1], scale_log2, bias0) : kNegInf;
+  s[2] = v1 ? fmaf(s0[2] + s1[2], scale_log2, bias1) : kNegInf;
+  s[3] = v1 ? fmaf(s0[3] + s1[3], scale_log2, bias1) : kNegInf;
+  rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
+  uint32_t b0, b1;
+  probs_to_b(A, s, b0, b1);
   // value rows past n (zero fill or unrelated rows) must not reach o
-  const int kt = 2 * (lane & 3);
-  const uint32_t t0 = (kt < n ? 0xffffu : 0u) | (kt + 1 < n ? 0xffff0000u : 0u);
-  const uint32_t t1 = (kt + 8 < n ? 0xffffu : 0u) | (kt + 9 < n ? 0xffff0000u : 0u);
-  const int key = 8 * (mi & 1) + (lane & 7);
+  uint32_t t0, t1;
+  pair_masks(0, n, t0, t1);
+  const int vrow = (lane & 7) + 8 * (mi >> 1);
 #pragma unroll
-  for (int dp = 0; dp < 8; ++dp) {
-    const int d0 = 16 * dp;
-    uint32_t b0, b1, b2, b3;
-    ldsm_x4_t(swz128(vb + (d0 >> 6) * half, key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1, b2, b3);
-    b0 &= t0; b2 &= t0; b1 &= t1; b3 &= t1;
-    mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], a0, a2, b0, b1);
-    mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], a0, a2, b2, b3);
+  for (int dt = 0; dt < 8; ++dt) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(swz128(vb + (dt >> 2) * half, vrow, 2 * (dt & 3) + (mi & 1)), a0, a1, a2, a3);
+    a0 &= t0; a1 &= t0; a2 &= t1; a3 &= t1;
+    mma16816(A.o[dt], a0, a1, a2, a3, b0, b1);
   }
 }
 
@@ -189,148 +226,117 @@ __device__ __forceinline__ bool route32(const uint8_t* page, const float* ys, co
 }
 
 // ---------------------------------------------------------------------------
-// Expanded spans, all on the tensor cores (query heads = M rows):
-//   key part:    c = diag(sigma_K g_K) Vt_K q  (scale*log2(e) folded in),
-//                kept as bf16 hi + lo A fragments (near-fp32 precision)
-//   body tokens: logits = c^T U_K^T, softmax, w += p^T U_V
-//   value part:  o += diag(sigma_V g_V) w  times Vt_V (hi + lo)
-// One warp handles a whole record.  KS = rank k-steps of 16 (ranks up to
-// 16 KS): every loop has a fixed trip count; ranks past the record's own are
-// masked arithmetically (no data-dependent branches in the inner loops).
+// Expanded spans (one warp per record), in factor space:
+//   key part:    c^T (ranks x heads) = diag(sigma_K g_K) Vt_K q^T, scale*log2(e)
+//                folded in, kept as bf16 hi + lo B fragments (near-fp32)
+//   body tokens: S^T = U_K c (tokens x heads), softmax, w^T += U_V^T P^T
+//   value part:  O^T += Vt_V^T diag(sigma_V g_V) w^T (hi + lo)
+// KS = rank k-steps of 16 (ranks up to 16 KS): every loop has a fixed trip
+// count; ranks past the record's own are masked arithmetically (no
+// data-dependent branches in the inner loops).
 // ---------------------------------------------------------------------------
 template <int KS>
 struct ExpAcc {
-  uint32_t ch[KS][2];    // c hi A-fragments for k-steps of 16 ranks: {a0, a2}
-  uint32_t cl[KS][2];    // c lo parts
-  float wacc[2 * KS][2];  // w (heads x rV) in C layout: tile jt = columns 8jt..8jt+7
+  uint32_t ch[KS][2];  // c hi B fragments, k-step = ranks 16 ks .. 16 ks + 15
+  uint32_t cl[KS][2];  // c lo parts
+  float w[KS][4];      // w^T tiles (ranks 16 T + g, + 8; heads 2q, 2q + 1)
   bool had;
 };
-
-// Masks of the bf16 pairs a lane holds in a B fragment of k-step ks whose
-// k index is a rank: pair j, j+1 (m0) and j+8, j+9 (m1), j = 16 ks + 2 (lane%4).
-__device__ __forceinline__ void rank_masks(int ks, int r, uint32_t& m0, uint32_t& m1) {
-  const int j = 16 * ks + 2 * (threadIdx.x & 3);
-  m0 = (j < r ? 0xffffu : 0u) | (j + 1 < r ? 0xffff0000u : 0u);
-  m1 = (j + 8 < r ? 0xffffu : 0u) | (j + 9 < r ? 0xffff0000u : 0u);
-}
 
 template <int KS>
 __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const uint8_t* part,
                                         int rK, float scale_log2) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   const float* sig = reinterpret_cast<const float*>(part + 16);
   const float* gat = sig + r4(rK);
   const uint32_t vt = smem_u32(part + 16 + 8 * r4(rK));
-  float cv[2 * KS][2];
+  float cv[KS][4];
 #pragma unroll
-  for (int nt = 0; nt < 2 * KS; ++nt) cv[nt][0] = cv[nt][1] = 0.f;
-  uint4 qv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) qv[i] = lds128(A.qfrag + (i * 32 + lane) * 16);
-  // Vt_K rows past rK read the record's next bytes; their columns of c are
+  for (int t = 0; t < KS; ++t) cv[t][0] = cv[t][1] = cv[t][2] = cv[t][3] = 0.f;
+  // Vt_K rows past rK read the record's next bytes; their rows of c are
   // dropped by the selects below
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // 32 head dims per step
+  for (int i = 0; i < 4; ++i) {  // head dims 32 i .. 32 i + 31
+    const uint4 qv = lds128(A.qfrag + (i * 32 + lane) * 16);
 #pragma unroll
-    for (int nt = 0; nt < 2 * KS; ++nt) {
-      uint32_t b0, b1, b2, b3;
-      const int row = 8 * nt + (lane & 7), chunk = 4 * i + (lane >> 3);
-      ldsm_x4(vt + row * 256 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
-      mma_bf16_rows8(cv[nt][0], cv[nt][1], qv[i].x, qv[i].y, b0, b1);
-      mma_bf16_rows8(cv[nt][0], cv[nt][1], qv[i].z, qv[i].w, b2, b3);
+    for (int t = 0; t < KS; ++t) {
+      const int row = 16 * t + (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int chunk = 4 * i + 2 * h + (mi >> 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(vt + row * 256 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+        mma16816(cv[t], a0, a1, a2, a3, h ? qv.z : qv.x, h ? qv.w : qv.y);
+      }
     }
   }
 #pragma unroll
-  for (int nt = 0; nt < 2 * KS; ++nt) {
-    const int j0 = 8 * nt + 2 * (lane & 3);
-    cv[nt][0] = j0 < rK ? cv[nt][0] * sig[j0] * gat[j0] * scale_log2 : 0.f;
-    cv[nt][1] = j0 + 1 < rK ? cv[nt][1] * sig[j0 + 1] * gat[j0 + 1] * scale_log2 : 0.f;
+  for (int t = 0; t < KS; ++t) {
+    const int r0 = 16 * t + g, r1 = r0 + 8;
+    const float f0 = r0 < rK ? sig[r0] * gat[r0] * scale_log2 : 0.f;
+    const float f1 = r1 < rK ? sig[r1] * gat[r1] * scale_log2 : 0.f;
+    const float c0 = r0 < rK ? cv[t][0] * f0 : 0.f, c1 = r0 < rK ? cv[t][1] * f0 : 0.f;
+    const float c2 = r1 < rK ? cv[t][2] * f1 : 0.f, c3 = r1 < rK ? cv[t][3] * f1 : 0.f;
+    uint32_t h01, l01, h23, l23;
+    split_bf16(c0, c1, h01, l01);
+    split_bf16(c2, c3, h23, l23);
+    X.ch[t][0] = movtrans(h01);
+    X.ch[t][1] = movtrans(h23);
+    X.cl[t][0] = movtrans(l01);
+    X.cl[t][1] = movtrans(l23);
+    X.w[t][0] = X.w[t][1] = X.w[t][2] = X.w[t][3] = 0.f;
   }
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    split_bf16(cv[2 * ks][0], cv[2 * ks][1], X.ch[ks][0], X.cl[ks][0]);
-    split_bf16(cv[2 * ks + 1][0], cv[2 * ks + 1][1], X.ch[ks][1], X.cl[ks][1]);
-  }
-#pragma unroll
-  for (int t = 0; t < 2 * KS; ++t) X.wacc[t][0] = X.wacc[t][1] = 0.f;
   X.had = false;
-}
-
-
-// Scores (log2 domain, scale folded into c) of the 16 body tokens
-// [rbase, rbase + 16) for the query heads, C layout: s[nt][e] is head
-// lane/4, token rbase + 8 nt + 2 (lane%4) + e; tokens >= n get -inf.
-template <int KS>
-__device__ __forceinline__ void token_scores(const ExpAcc<KS>& X, uint32_t uku, int sk,
-                                             int rbase, int n, int rK, float (&s)[2][2]) {
-  const int lane = threadIdx.x & 31, mi = lane >> 3;
-  s[0][0] = s[0][1] = s[1][0] = s[1][1] = 0.f;
-  const int tok = rbase + 8 * (mi >> 1) + (lane & 7);
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t b0, b1, b2, b3, m0, m1;
-    ldsm_x4(uku + tok * sk + (2 * ks + (mi & 1)) * 16, b0, b1, b2, b3);
-    rank_masks(ks, rK, m0, m1);
-    b0 &= m0; b2 &= m0; b1 &= m1; b3 &= m1;
-    mma_bf16_rows8(s[0][0], s[0][1], X.ch[ks][0], X.ch[ks][1], b0, b1);
-    mma_bf16_rows8(s[1][0], s[1][1], X.ch[ks][0], X.ch[ks][1], b2, b3);
-    mma_bf16_rows8(s[0][0], s[0][1], X.cl[ks][0], X.cl[ks][1], b0, b1);
-    mma_bf16_rows8(s[1][0], s[1][1], X.cl[ks][0], X.cl[ks][1], b2, b3);
-  }
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-      if (rbase + 8 * nt + 2 * (lane & 3) + e >= n) s[nt][e] = kNegInf;
 }
 
 // Body tokens [0, n) of this page; U_K rows at uk, U_V rows at uv (row
 // strides r8(rK), r8(rV) bf16), one pass of 16-token tiles with lazy
-// re-basing (the tiles are independent unless a re-base is needed).  Rows
-// or ranks past the valid ones read neighbouring shared memory and are
-// masked, never multiplied.
+// re-basing.  Rows or ranks past the valid ones read neighbouring shared
+// memory and are masked, never multiplied.
 template <int KS>
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* uk,
                                            const uint8_t* uv, int n, int rK, int rV) {
   if (n <= 0) return;
-  const int lane = threadIdx.x & 31;
+  (void)rV;
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   const int sk = 2 * r8(rK), sv = 2 * r8(rV);  // row strides in bytes
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
-  const int mi = lane >> 3;
   X.had = true;
-#pragma unroll 2
+#pragma unroll 1
   for (int rb = 0; rb < n; rb += 16) {
-    float s[2][2];
-    token_scores<KS>(X, uku, sk, rb, n, rK, s);
-    const float alpha =
-        rebase_if_needed(A, fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
-    if (alpha != 1.f) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tq = rb + (lane & 7) + 8 * (mi & 1);
 #pragma unroll
-      for (int t = 0; t < 2 * KS; ++t) {
-        X.wacc[t][0] *= alpha;
-        X.wacc[t][1] *= alpha;
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a0, a1, a2, a3, m0, m1;
+      ldsm_x4(uku + tq * sk + (16 * ks + 8 * (mi >> 1)) * 2, a0, a1, a2, a3);
+      pair_masks(16 * ks, rK, m0, m1);
+      a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
+      mma16816(s, a0, a1, a2, a3, X.ch[ks][0], X.ch[ks][1]);
+      mma16816(s, a0, a1, a2, a3, X.cl[ks][0], X.cl[ks][1]);
+    }
+    if (rb + g >= n) s[0] = s[1] = kNegInf;
+    if (rb + g + 8 >= n) s[2] = s[3] = kNegInf;
+    const float2 alpha = rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
+    if (alpha.x != 1.f || alpha.y != 1.f) {
+#pragma unroll
+      for (int t = 0; t < KS; ++t) {
+        X.w[t][0] *= alpha.x;
+        X.w[t][1] *= alpha.y;
+        X.w[t][2] *= alpha.x;
+        X.w[t][3] *= alpha.y;
       }
     }
-    const float msub = A.m_row == kNegInf ? 0.f : A.m_row;
+    uint32_t b0, b1, t0, t1;
+    probs_to_b(A, s, b0, b1);
+    pair_masks(rb, n, t0, t1);
+    const int tv = rb + (lane & 7) + 8 * (mi >> 1);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) s[nt][e] = ex2_approx(s[nt][e] - msub);
-    // into the running sum right away: a later re-base rescales it
-    A.l_part += (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
-    const uint32_t a0 = pack_bf16(s[0][0], s[0][1]);
-    const uint32_t a2 = pack_bf16(s[1][0], s[1][1]);
-    const int tk = rb + 2 * (lane & 3);  // tokens held by b0/b2 (+8 in b1/b3)
-    const uint32_t t0 = (tk < n ? 0xffffu : 0u) | (tk + 1 < n ? 0xffff0000u : 0u);
-    const uint32_t t1 = (tk + 8 < n ? 0xffffu : 0u) | (tk + 9 < n ? 0xffff0000u : 0u);
-    const int tok = rb + 8 * (mi & 1) + (lane & 7);
-#pragma unroll
-    for (int jp = 0; jp < KS; ++jp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(uvu + tok * sv + (2 * jp + (mi >> 1)) * 16, b0, b1, b2, b3);
-      b0 &= t0; b2 &= t0; b1 &= t1; b3 &= t1;
-      mma_bf16_rows8(X.wacc[2 * jp][0], X.wacc[2 * jp][1], a0, a2, b0, b1);
-      mma_bf16_rows8(X.wacc[2 * jp + 1][0], X.wacc[2 * jp + 1][1], a0, a2, b2, b3);
+    for (int t = 0; t < KS; ++t) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(uvu + tv * sv + (16 * t + 8 * (mi & 1)) * 2, a0, a1, a2, a3);
+      a0 &= t0; a1 &= t0; a2 &= t1; a3 &= t1;
+      mma16816(X.w[t], a0, a1, a2, a3, b0, b1);
     }
   }
 }
@@ -339,33 +345,34 @@ template <int KS>
 __device__ __forceinline__ void exp_value(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* part,
                                           int rV) {
   if (!X.had) return;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   const float* sig = reinterpret_cast<const float*>(part);
   const float* gat = sig + r4(rV);
   const uint32_t vt = smem_u32(part + 8 * r4(rV));
-  const int mi = lane >> 3;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    // coefficients of ranks 16 ks .. 16 ks + 15 as A fragments, hi and lo
-    const int j0 = 16 * ks + 2 * (lane & 3);
-    const float c0 = j0 < rV ? X.wacc[2 * ks][0] * sig[j0] * gat[j0] : 0.f;
-    const float c1 = j0 + 1 < rV ? X.wacc[2 * ks][1] * sig[j0 + 1] * gat[j0 + 1] : 0.f;
-    const float c2 = j0 + 8 < rV ? X.wacc[2 * ks + 1][0] * sig[j0 + 8] * gat[j0 + 8] : 0.f;
-    const float c3 = j0 + 9 < rV ? X.wacc[2 * ks + 1][1] * sig[j0 + 9] * gat[j0 + 9] : 0.f;
-    uint32_t h0, l0, h2, l2, m0, m1;
-    split_bf16(c0, c1, h0, l0);
-    split_bf16(c2, c3, h2, l2);
-    rank_masks(ks, rV, m0, m1);
-    const int j = 16 * ks + 8 * (mi & 1) + (lane & 7);  // Vt_V row addressed by this lane
+  for (int t = 0; t < KS; ++t) {
+    // coefficients diag(sigma_V g_V) w^T of ranks 16 t .. 16 t + 15 as B
+    // fragments, hi and lo
+    const int r0 = 16 * t + g, r1 = r0 + 8;
+    const float f0 = r0 < rV ? sig[r0] * gat[r0] : 0.f;
+    const float f1 = r1 < rV ? sig[r1] * gat[r1] : 0.f;
+    const float c0 = r0 < rV ? X.w[t][0] * f0 : 0.f, c1 = r0 < rV ? X.w[t][1] * f0 : 0.f;
+    const float c2 = r1 < rV ? X.w[t][2] * f1 : 0.f, c3 = r1 < rV ? X.w[t][3] * f1 : 0.f;
+    uint32_t h01, l01, h23, l23, m0, m1;
+    split_bf16(c0, c1, h01, l01);
+    split_bf16(c2, c3, h23, l23);
+    const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
+    const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
+    pair_masks(16 * t, rV, m0, m1);
+    const int row = 16 * t + (lane & 7) + 8 * (mi >> 1);  // Vt_V row (rank) of this lane
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vt + j * 256 + (((2 * dp + (mi >> 1)) ^ (j & 7)) << 4), b0, b1, b2, b3);
-      b0 &= m0; b2 &= m0; b1 &= m1; b3 &= m1;
-      mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], h0, h2, b0, b1);
-      mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], h0, h2, b2, b3);
-      mma_bf16_rows8(A.o[2 * dp][0], A.o[2 * dp][1], l0, l2, b0, b1);
-      mma_bf16_rows8(A.o[2 * dp + 1][0], A.o[2 * dp + 1][1], l0, l2, b2, b3);
+    for (int dt = 0; dt < 8; ++dt) {
+      uint32_t a0, a1, a2, a3;
+      const int chunk = 2 * dt + (mi & 1);
+      ldsm_x4_t(vt + row * 256 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+      a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
+      mma16816(A.o[dt], a0, a1, a2, a3, bh0, bh1);
+      mma16816(A.o[dt], a0, a1, a2, a3, bl0, bl1);
     }
   }
 }

@@ -495,9 +495,9 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   WarpAcc A;
   A.qfrag = smem_u32(smem + kOffQfrag);
 #pragma unroll
-  for (int t = 0; t < 16; ++t) A.o[t][0] = A.o[t][1] = 0.f;
-  A.m_row = kNegInf;
-  A.l_part = 0.f;
+  for (int t = 0; t < 8; ++t) A.o[t][0] = A.o[t][1] = A.o[t][2] = A.o[t][3] = 0.f;
+  A.m[0] = A.m[1] = kNegInf;
+  A.l[0] = A.l[1] = 0.f;
   ExpAcc<KS> X;
   X.had = false;
   for (;;) {
@@ -532,17 +532,20 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   // (each warp writes into its own arena, which is idle now)
   {
     float* wst = reinterpret_cast<float*>(smem + kOffArena + w * kArenaBytes);  // m[8] l[8] o[8][128]
-    const int r0 = lane >> 2;
-    float l_row = A.l_part + __shfl_xor_sync(kFull, A.l_part, 1);
-    l_row += __shfl_xor_sync(kFull, l_row, 2);
-    if ((lane & 3) == 0) {
-      wst[r0] = r0 < G ? A.m_row : kNegInf;
-      wst[8 + r0] = r0 < G ? l_row : 0.f;
+    const int g = lane >> 2, h0 = 2 * (lane & 3);  // this lane: dims 16 t + g (+ 8), heads h0, h0 + 1
+    const float l0 = col_sum(A.l[0]), l1 = col_sum(A.l[1]);
+    if (g == 0) {
+      wst[h0] = h0 < G ? A.m[0] : kNegInf;
+      wst[h0 + 1] = h0 + 1 < G ? A.m[1] : kNegInf;
+      wst[8 + h0] = h0 < G ? l0 : 0.f;
+      wst[8 + h0 + 1] = h0 + 1 < G ? l1 : 0.f;
     }
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      wst[16 + r0 * kHeadDim + 8 * t + 2 * (lane & 3)] = A.o[t][0];
-      wst[16 + r0 * kHeadDim + 8 * t + 2 * (lane & 3) + 1] = A.o[t][1];
+    for (int t = 0; t < 8; ++t) {
+      wst[16 + h0 * kHeadDim + 16 * t + g] = A.o[t][0];
+      wst[16 + (h0 + 1) * kHeadDim + 16 * t + g] = A.o[t][1];
+      wst[16 + h0 * kHeadDim + 16 * t + g + 8] = A.o[t][2];
+      wst[16 + (h0 + 1) * kHeadDim + 16 * t + g + 8] = A.o[t][3];
     }
   }
   __syncthreads();

@@ -220,19 +220,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// D = A * B + D for one m16n8k16 bf16 tile; rows 8..15 of A are zero in this
-// library (at most 8 query heads), so only the first two accumulators (row
-// lane/4) are kept; the other two are fed zero and discarded.
-__device__ __forceinline__ void mma_bf16_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
-                                               uint32_t b0, uint32_t b1) {
-  float z2, z3;
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
-      " {%8,%9}, {%0,%1,%10,%11};"
-      : "+f"(d0), "+f"(d1), "=f"(z2), "=f"(z3)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
