@@ -15,6 +15,9 @@ from .sekv import (  # noqa: F401
     decode_step,
     decode_step_noalloc,
     fetch_bases,
+    fetch_bases_copy,
+    fetch_bases_cached,
+    BasisCache,
     build_spans,
     alloc_cache,
     record_size,

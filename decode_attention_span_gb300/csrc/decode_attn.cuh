@@ -129,6 +129,7 @@ struct DecodeParams {
   float scale_log2;
   int fused;
   int rank_lim;                  // largest record rank the kernel instance handles (16 KS)
+  unsigned long long wait_ns;    // limit of a parked wait for an item (SEKV_FLAG_SHORT_WAITS: 0)
 };
 
 template <int KS>

@@ -268,7 +268,7 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   bool hit = false, landed = false;
   int end = 0;
   if (ms->wq[w].ok) {
-    landed = mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1));
+    landed = mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1), P.wait_ns);
     if (landed) {
       const Item it = ms->desc[w][nd % kSlots];
       end = it.end;
@@ -382,7 +382,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     float* ys = reinterpret_cast<float*>(smem + kOffY);
     const int nd = ms->wq[w].nd;
     const bool wr_ok =
-        mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1));
+        mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1), P.wait_ns);
     if (!wr_ok && lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
     const Item wit = ms->desc[w][nd % kSlots];
     const float* wrs = reinterpret_cast<const float*>(smem + wit.boff);
@@ -504,7 +504,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     issue_more(smem, ms, P, true, claim);
     const int nd = ms->wq[w].nd;
     if (nd == ms->wq[w].ni || !ms->wq[w].ok) break;
-    if (!mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1))) {
+    if (!mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1), P.wait_ns)) {
       __syncwarp();
       if (lane == 0) {
         set_device_error(P.status, DEV_WAIT_TIMEOUT, 4);

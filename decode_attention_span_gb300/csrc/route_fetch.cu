@@ -203,3 +203,199 @@ __global__ void __launch_bounds__(256) fetch_kernel(const FetchParams P) {
 }
 
 }  // namespace sekv
+
+namespace sekv {
+
+// ----------------------------------------------------------------------------
+// residency cache: plan (one CTA per group), then copy (kFetchParts per group)
+// ----------------------------------------------------------------------------
+
+// Block-wide exclusive prefix of v (256 threads); *total receives the sum.
+__device__ __forceinline__ long long block_excl_scan(long long v, long long* sh, long long* total) {
+  const int tid = threadIdx.x;
+  sh[tid] = v;
+  __syncthreads();
+  for (int o = 1; o < 256; o <<= 1) {
+    const long long u = tid >= o ? sh[tid - o] : 0;
+    __syncthreads();
+    sh[tid] += u;
+    __syncthreads();
+  }
+  const long long incl = sh[tid];
+  *total = sh[255];
+  __syncthreads();
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(256) cache_plan_kernel(const CacheParams P) {
+  __shared__ long long scan[256];
+  __shared__ int victims[kCacheMaxSlots];
+  __shared__ int s_nvict, s_last;
+  const int g = blockIdx.x, b = g / P.Hkv, tid = threadIdx.x;
+  const size_t gs = size_t(g) * P.max_spans, gsl = size_t(g) * P.n_slots;
+  const int n_sp = P.n_spans[b];
+  int ne = P.n_expanded[g];
+  if (ne < 0 || ne > n_sp) {
+    if (tid == 0) set_device_error(P.status, DEV_BAD_LIST, g);
+    ne = 0;
+  }
+  const int epoch = P.epoch[g] + 1;
+  // Entry classes: 0 = a hit (or a bad entry), 1 = a miss that goes to a
+  // slot, 2 = a miss that goes to staging.  Reads only tables that no
+  // concurrent write of this call can change for the entry's own span.
+  auto classify = [&](int e, int& k, int64_t& sz) -> int {
+    k = P.expanded[gs + e];
+    const int prev = e > 0 ? P.expanded[gs + e - 1] : -1;
+    if (k < 0 || k >= n_sp || k <= prev) {
+      k = -1;
+      return 0;
+    }
+    if (P.slot_of[gs + k] >= 0) return 0;
+    const int rank = P.rec_rank[gs + k];
+    sz = record_bytes(P.body_len[size_t(b) * P.max_spans + k], rank & 0xffff,
+                      (rank >> 16) & 0xffff);
+    return sz <= P.slot_bytes ? 1 : 2;
+  };
+  // pass 1: hits keep their slots (marked as used by this call); count the
+  // misses that fit a slot
+  long long hit_n = 0, miss_n = 0;
+  for (int e = tid; e < ne; e += 256) {
+    int k;
+    int64_t sz = 0;
+    const int cls = classify(e, k, sz);
+    if (k < 0) {
+      set_device_error(P.status, DEV_BAD_LIST, e);
+    } else if (cls == 0) {
+      const int s = P.slot_of[gs + k];
+      P.stamp[gsl + s] = epoch;
+      P.staged_off[gs + e] = P.pool_base + (int64_t(gsl) + s) * P.slot_bytes;
+      ++hit_n;
+    } else if (cls == 1) {
+      ++miss_n;
+    }
+  }
+  long long n_hits, n_miss;
+  block_excl_scan(hit_n, scan, &n_hits);
+  block_excl_scan(miss_n, scan, &n_miss);
+  // victims: the first slots from the clock hand on that no entry of this
+  // call uses (free, or last used by an earlier call)
+  if (tid == 0) {
+    s_nvict = 0;
+    s_last = -1;
+  }
+  __syncthreads();
+  const int want = int(n_miss < P.n_slots ? n_miss : P.n_slots);
+  const int hand = P.hand[g];
+  for (int c0 = 0; c0 < P.n_slots && s_nvict < want; c0 += 256) {
+    const int i = c0 + tid;
+    int s = -1;
+    bool ok = false;
+    if (i < P.n_slots) {
+      s = (hand + i) % P.n_slots;
+      ok = P.span_of[gsl + s] < 0 || P.stamp[gsl + s] < epoch;
+    }
+    long long tot;
+    const long long before = block_excl_scan(ok ? 1 : 0, scan, &tot);
+    const int base = s_nvict;
+    if (ok && base + before < want) {
+      victims[base + before] = s;
+      if (base + before == want - 1) s_last = i;
+    }
+    __syncthreads();
+    if (tid == 0) s_nvict = int(base + tot < want ? base + tot : want);
+    __syncthreads();
+  }
+  const int nv = s_nvict;
+  // pass 2 (twice: measure, then commit): misses in list order; the first nv
+  // that fit a slot take the victims, the rest go to staging, which must
+  // hold them all before anything is evicted
+  for (int commit = 0; commit < 2; ++commit) {
+    long long carry_m = 0, carry_s = 0, carry_p = 0, carry_b = 0;
+    for (int e0 = 0; e0 < ne; e0 += 256) {
+      const int e = e0 + tid;
+      int k = -1, cls = 0;
+      int64_t sz = 0;
+      if (e < ne) cls = classify(e, k, sz);
+      __syncthreads();  // every lane has read the tables before this chunk writes them
+      long long tm, ts, tp;
+      const long long jm = carry_m + block_excl_scan(cls == 1 ? 1 : 0, scan, &tm);
+      if (cls == 1 && jm >= nv) cls = 2;
+      const long long js = carry_s + block_excl_scan(cls == 2 ? sz : 0, scan, &ts);
+      long long tb;
+      const long long jp = carry_p + block_excl_scan(cls != 0 ? 1 : 0, scan, &tp);
+      block_excl_scan(cls != 0 ? sz : 0, scan, &tb);
+      if (commit && cls != 0) {
+        int64_t dst;
+        if (cls == 1) {
+          const int v = victims[jm];
+          const int old = P.span_of[gsl + v];
+          if (old >= 0) P.slot_of[gs + old] = -1;
+          P.span_of[gsl + v] = k;
+          P.slot_of[gs + k] = v;
+          P.stamp[gsl + v] = epoch;
+          dst = P.pool_base + (int64_t(gsl) + v) * P.slot_bytes;
+        } else {
+          dst = int64_t(g) * P.per_group + js;
+        }
+        P.staged_off[gs + e] = dst;
+        int64_t* pl = P.plan + (gs + jp) * 3;
+        pl[0] = P.rec_off[gs + k];
+        pl[1] = dst;
+        pl[2] = sz;
+      }
+      carry_m += tm;
+      carry_s += ts;
+      carry_p += tp;
+      carry_b += tb;
+    }
+    if (!commit && carry_s > P.per_group) {
+      // nothing is evicted or copied for this group
+      if (tid == 0) {
+        set_device_error(P.status, DEV_STAGING_FULL, g);
+        P.plan_n[g] = 0;
+        if (P.hits) P.hits[g] = int(n_hits);
+        if (P.copied) P.copied[g] = 0;
+      }
+      return;
+    }
+    if (commit && tid == 0) {
+      P.plan_n[g] = int(carry_p);
+      if (P.copied) P.copied[g] = carry_b;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    P.epoch[g] = epoch;
+    if (s_last >= 0) P.hand[g] = (hand + s_last + 1) % P.n_slots;
+    if (P.hits) P.hits[g] = int(n_hits);
+  }
+}
+
+// grid (B*Hkv, kFetchParts): part p copies the plan's entries c with
+// c % kFetchParts == p from the host store over the host link.
+__global__ void __launch_bounds__(256) cache_copy_kernel(const CacheParams P) {
+  const int g = blockIdx.x, part = blockIdx.y, tid = threadIdx.x;
+  const size_t gs = size_t(g) * P.max_spans;
+  const int n = P.plan_n[g];
+  for (int c = part; c < n; c += kFetchParts) {
+    const int64_t* pl = P.plan + (gs + c) * 3;
+    const int4* src = reinterpret_cast<const int4*>(P.store + pl[0]);
+    int4* dst = reinterpret_cast<int4*>(P.staging + pl[1]);
+    const long long n16 = pl[2] / 16;
+    for (long long i0 = 0; i0 < n16; i0 += 256 * kFetchUnroll) {
+      int4 v[kFetchUnroll];
+#pragma unroll
+      for (int u = 0; u < kFetchUnroll; ++u) {
+        const long long i = i0 + tid + 256 * u;
+        if (i < n16) v[u] = __ldcs(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kFetchUnroll; ++u) {
+        const long long i = i0 + tid + 256 * u;
+        if (i < n16) dst[i] = v[u];
+      }
+    }
+  }
+}
+
+}  // namespace sekv

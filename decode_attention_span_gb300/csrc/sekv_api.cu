@@ -102,6 +102,8 @@ WsLayout ws_layout(const sekv_config* cfg, int sms) {
   L.partials = off;   off += align256(ng * L.cg * sizeof(Partial));
   L.route_list = off; off += align256(ng * ms * 4);
   L.route_cnt = off;  off += align256(ng * L.route_chunks * 4);
+  L.plan = off;       off += align256(ng * ms * 3 * 8);
+  L.plan_n = off;     off += align256(ng * 4);
   L.total = off;
   return L;
 }
@@ -261,6 +263,7 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.max_spans = cfg->max_spans;
   P.cg = L.cg;
   P.fused = fused ? 1 : 0;
+  P.wait_ns = (cfg->flags & SEKV_FLAG_SHORT_WAITS) ? 0ull : 2000000000ull;
   return SEKV_OK;
 }
 
@@ -463,3 +466,187 @@ extern "C" sekv_status sekv_fetch_bases(const sekv_config* cfg, const sekv_layer
 }
 
 
+
+extern "C" sekv_status sekv_fetch_bases_copy(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                             const int32_t* expanded_host,
+                                             const int32_t* n_expanded_host,
+                                             const int64_t* rec_off_host, void* staging,
+                                             int64_t staging_per_group, int64_t* staged_off_host,
+                                             int64_t* staged_off, int32_t* n_copies,
+                                             cudaStream_t copy_stream, cudaEvent_t done) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  if (!cache || !cache->store || !cache->store_on_host) return SEKV_ERR_INVALID;
+  if (!expanded_host || !n_expanded_host || !rec_off_host || !staging || !staged_off_host ||
+      !staged_off || !done)
+    return SEKV_ERR_INVALID;
+  if (staging_per_group <= 0 || staging_per_group % 16 != 0 || !aligned16(staging) ||
+      !aligned16(cache->store))
+    return SEKV_ERR_INVALID;
+  const int ng = cfg->batch * cfg->n_kv_heads;
+  const size_t ms = size_t(cfg->max_spans);
+  const uint8_t* store = static_cast<const uint8_t*>(cache->store);
+  // plan every copy before issuing any: offsets, sizes from the headers, checks
+  int64_t copies = 0;
+  for (int g = 0; g < ng; ++g) {
+    const int ne = n_expanded_host[g];
+    if (ne < 0 || ne > cfg->max_spans) return SEKV_ERR_INVALID;
+    int64_t pos = 0;
+    for (int e = 0; e < ne; ++e) {
+      const int k = expanded_host[g * ms + e];
+      if (k < 0 || k >= cfg->max_spans || (e > 0 && k <= expanded_host[g * ms + e - 1]))
+        return SEKV_ERR_INVALID;
+      const int64_t off = rec_off_host[g * ms + k];
+      if (off < 0 || off % 16 != 0) return SEKV_ERR_INVALID;
+      const int32_t* hdr = reinterpret_cast<const int32_t*>(store + off);
+      const int64_t sz = sekv_record_size(hdr[0], hdr[1], hdr[2]);
+      if (sz <= 0 || hdr[1] > SEKV_MAX_RANK || hdr[2] > SEKV_MAX_RANK) return SEKV_ERR_INVALID;
+      staged_off_host[g * ms + e] = int64_t(g) * staging_per_group + pos;
+      pos += sz;
+    }
+    if (pos > staging_per_group) return SEKV_ERR_CAPACITY;
+  }
+  // one copy per run of records that follow each other in the store and land
+  // next to each other in staging
+  uint8_t* stg = static_cast<uint8_t*>(staging);
+  for (int g = 0; g < ng; ++g) {
+    const int ne = n_expanded_host[g];
+    int e = 0;
+    while (e < ne) {
+      const int64_t src0 = rec_off_host[g * ms + expanded_host[g * ms + e]];
+      const int64_t dst0 = staged_off_host[g * ms + e];
+      int64_t len = 0;
+      int e1 = e;
+      while (e1 < ne) {
+        const int64_t off = rec_off_host[g * ms + expanded_host[g * ms + e1]];
+        if (off != src0 + len) break;
+        const int32_t* hdr = reinterpret_cast<const int32_t*>(store + off);
+        len += sekv_record_size(hdr[0], hdr[1], hdr[2]);
+        ++e1;
+      }
+      if (cudaMemcpyAsync(stg + dst0, store + src0, size_t(len), cudaMemcpyHostToDevice,
+                          copy_stream) != cudaSuccess)
+        return SEKV_ERR_CUDA;
+      ++copies;
+      e = e1;
+    }
+  }
+  if (cudaMemcpyAsync(staged_off, staged_off_host, size_t(ng) * ms * sizeof(int64_t),
+                      cudaMemcpyHostToDevice, copy_stream) != cudaSuccess)
+    return SEKV_ERR_CUDA;
+  if (cudaEventRecord(done, copy_stream) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (n_copies) *n_copies = int32_t(copies);
+  return SEKV_OK;
+}
+
+// ----------------------------------------------------------------------------
+// residency cache of basis records
+// ----------------------------------------------------------------------------
+namespace {
+
+struct CacheTable {
+  size_t slot_of, span_of, stamp, epoch, hand, total;
+};
+
+CacheTable cache_table(const sekv_config* cfg, int32_t n_slots) {
+  CacheTable T{};
+  const size_t ng = size_t(cfg->batch) * cfg->n_kv_heads, ms = cfg->max_spans;
+  size_t off = 0;
+  T.slot_of = off; off += align256(ng * ms * 4);
+  T.span_of = off; off += align256(ng * size_t(n_slots) * 4);
+  T.stamp = off;   off += align256(ng * size_t(n_slots) * 4);
+  T.epoch = off;   off += align256(ng * 4);
+  T.hand = off;    off += align256(ng * 4);
+  T.total = off;
+  return T;
+}
+
+}  // namespace
+
+extern "C" size_t sekv_basis_cache_bytes(const sekv_config* cfg, int32_t n_slots) {
+  sekv_status why;
+  if (!config_ok(cfg, &why) || n_slots < 1 || n_slots > kCacheMaxSlots) return 0;
+  return cache_table(cfg, n_slots).total;
+}
+
+extern "C" sekv_status sekv_basis_cache_init(const sekv_config* cfg, void* table,
+                                             int32_t n_slots, cudaStream_t stream) {
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  if (!table || n_slots < 1 || n_slots > kCacheMaxSlots) return SEKV_ERR_INVALID;
+  const CacheTable T = cache_table(cfg, n_slots);
+  uint8_t* t = static_cast<uint8_t*>(table);
+  // slot_of and span_of: -1 (empty); stamps, epochs and hands: 0
+  if (cudaMemsetAsync(t, 0xff, T.stamp, stream) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (cudaMemsetAsync(t + T.stamp, 0, T.total - T.stamp, stream) != cudaSuccess)
+    return SEKV_ERR_CUDA;
+  return SEKV_OK;
+}
+
+extern "C" sekv_status sekv_fetch_bases_cached(const sekv_config* cfg,
+                                               const sekv_layer_cache* cache,
+                                               const int32_t* expanded, const int32_t* n_expanded,
+                                               void* staging, int64_t staging_per_group,
+                                               void* table, int32_t n_slots, int32_t slot_bytes,
+                                               int64_t* staged_off, int32_t* hits,
+                                               int64_t* copied, void* workspace,
+                                               size_t workspace_bytes, cudaStream_t stream) {
+  reset_launches();
+  sekv_status why;
+  if (!config_ok(cfg, &why)) return why;
+  if (!cache || !cache->n_spans || !cache->body_len || !cache->rec_off || !cache->rec_rank ||
+      !cache->store || !cache->store_on_host)
+    return SEKV_ERR_INVALID;
+  if (!expanded || !n_expanded || !staging || !staged_off || !workspace || !table)
+    return SEKV_ERR_INVALID;
+  if (staging_per_group <= 0 || staging_per_group % 16 != 0 || !aligned16(staging) ||
+      !aligned16(cache->store) || n_slots < 1 || n_slots > kCacheMaxSlots || slot_bytes < 16 ||
+      slot_bytes % 16 != 0)
+    return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  const WsLayout L = ws_layout(cfg, sms);
+  if (workspace_bytes < L.total) return SEKV_ERR_CAPACITY;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, cache->store) != cudaSuccess ||
+      pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) {
+    cudaGetLastError();
+    return SEKV_ERR_INVALID;  // not page-locked host memory the device can address
+  }
+  const CacheTable T = cache_table(cfg, n_slots);
+  uint8_t* t = static_cast<uint8_t*>(table);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  CacheParams P;
+  P.n_spans = cache->n_spans;
+  P.body_len = cache->body_len;
+  P.rec_off = cache->rec_off;
+  P.rec_rank = cache->rec_rank;
+  P.store = static_cast<const uint8_t*>(pa.devicePointer);
+  P.expanded = expanded;
+  P.n_expanded = n_expanded;
+  P.staging = static_cast<uint8_t*>(staging);
+  P.per_group = staging_per_group;
+  P.pool_base = int64_t(L.ng) * staging_per_group;
+  P.slot_of = reinterpret_cast<int32_t*>(t + T.slot_of);
+  P.span_of = reinterpret_cast<int32_t*>(t + T.span_of);
+  P.stamp = reinterpret_cast<int32_t*>(t + T.stamp);
+  P.epoch = reinterpret_cast<int32_t*>(t + T.epoch);
+  P.hand = reinterpret_cast<int32_t*>(t + T.hand);
+  P.plan = reinterpret_cast<int64_t*>(w + L.plan);
+  P.plan_n = reinterpret_cast<int32_t*>(w + L.plan_n);
+  P.staged_off = staged_off;
+  P.hits = hits;
+  P.copied = copied;
+  P.status = reinterpret_cast<int32_t*>(w + L.status);
+  P.Hkv = cfg->n_kv_heads;
+  P.max_spans = cfg->max_spans;
+  P.n_slots = n_slots;
+  P.slot_bytes = slot_bytes;
+  cache_plan_kernel<<<L.ng, 256, 0, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  cache_copy_kernel<<<dim3(L.ng, kFetchParts), 256, 0, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(2);
+  return SEKV_OK;
+}

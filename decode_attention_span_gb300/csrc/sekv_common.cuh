@@ -43,7 +43,7 @@ struct Partial {           // one CTA's softmax state for up to 8 heads
 };
 
 struct WsLayout {
-  size_t status, groups, cta_n, cta_list, partials, route_list, route_cnt, total;
+  size_t status, groups, cta_n, cta_list, partials, route_list, route_cnt, plan, plan_n, total;
   int ng, cg, route_chunks;
 };
 
@@ -131,14 +131,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
 }
 
 // Bounded wait in which the hardware parks the warp instead of a polling loop
-// (no shared-memory traffic while it waits); returns false after about two
-// seconds (the caller flags an error).
-__device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity) {
+// (no shared-memory traffic while it waits); returns false once `limit_ns`
+// nanoseconds have passed without the phase completing (the caller flags an
+// error).  limit_ns == 0 gives up at once if the phase is not complete at the
+// first test.
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity,
+                                                 uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity, 20000u)) return true;
-    if ((i & 15u) == 15u && globaltimer_ns() - t0 > 2000000000ull) return false;
+    if ((i & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

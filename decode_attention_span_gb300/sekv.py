@@ -23,6 +23,7 @@ _c_i32, _c_f32, _c_vp, _c_sz, _c_i64 = (ctypes.c_int32, ctypes.c_float, ctypes.c
 
 SEKV_CALL_ROUTE, SEKV_CALL_FETCH, SEKV_CALL_DECODE, SEKV_CALL_BUILD = 0, 1, 2, 3
 FLAG_OVERLAP_PREVIOUS = 1
+FLAG_SHORT_WAITS = 2
 STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SEKV_ERR_CUDA",
           -4: "SEKV_ERR_TIMEOUT", -5: "SEKV_ERR_UNSUPPORTED", -6: "SEKV_ERR_DEVICE"}
 
@@ -30,6 +31,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
            "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_build_spans",
+           "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
+           "sekv_fetch_bases_cached",
            "sekv_status_string", "sekv_last_launch_count")
 
 
@@ -89,6 +92,20 @@ def lib() -> ctypes.CDLL:
         L.sekv_fetch_bases.restype = _c_i32
         L.sekv_fetch_bases.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]
+        L.sekv_basis_cache_bytes.restype = _c_sz
+        L.sekv_basis_cache_bytes.argtypes = [ctypes.POINTER(SekvConfig), _c_i32]
+        L.sekv_basis_cache_init.restype = _c_i32
+        L.sekv_basis_cache_init.argtypes = [ctypes.POINTER(SekvConfig), _c_vp, _c_i32, _c_vp]
+        L.sekv_fetch_bases_cached.restype = _c_i32
+        L.sekv_fetch_bases_cached.argtypes = [ctypes.POINTER(SekvConfig),
+                                              ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp, _c_vp,
+                                              _c_i64, _c_vp, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp,
+                                              _c_vp, _c_sz, _c_vp]
+        L.sekv_fetch_bases_copy.restype = _c_i32
+        L.sekv_fetch_bases_copy.argtypes = [ctypes.POINTER(SekvConfig),
+                                            ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp, _c_vp,
+                                            _c_vp, _c_i64, _c_vp, _c_vp, ctypes.POINTER(_c_i32),
+                                            _c_vp, _c_vp]
         L.sekv_decode_attention.restype = _c_i32
         L.sekv_decode_attention.argtypes = [ctypes.POINTER(SekvConfig),
                                             ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp, _c_vp,
@@ -331,6 +348,66 @@ def fetch_bases(cfg: Config, cache: LayerCache, expanded, n_expanded, staging, p
            lib().sekv_fetch_bases(ctypes.byref(c), ctypes.byref(cache.c), _ptr(expanded),
                                   _ptr(n_expanded), _ptr(staging), int(per_group),
                                   _ptr(staged_off), ws.ptr(), ws.nbytes, _stream(stream)))
+    return staging, staged_off
+
+
+def fetch_bases_copy(cfg: Config, cache: LayerCache, expanded_host, n_expanded_host,
+                     rec_off_host, staging, per_group: int, staged_off_host, staged_off,
+                     done_event, copy_stream) -> int:
+    """sekv_fetch_bases_copy: the host-driven fetch (one cudaMemcpyAsync per
+    run of adjacent records on `copy_stream`, then `done_event` recorded).
+    The lists and record offsets are host tensors; returns the copies issued."""
+    _need(expanded_host, "expanded_host", torch.int32, cuda=False)
+    _need(n_expanded_host, "n_expanded_host", torch.int32, cuda=False)
+    _need(rec_off_host, "rec_off_host", torch.int64, cuda=False)
+    _need(staged_off_host, "staged_off_host", torch.int64, cuda=False)
+    _need(staging, "staging", torch.uint8); _need(staged_off, "staged_off", torch.int64)
+    if done_event.cuda_event == 0:
+        done_event.record(copy_stream)  # torch creates the CUDA event at its first record
+    n = _c_i32(0)
+    c = cfg.c()
+    _check("sekv_fetch_bases_copy",
+           lib().sekv_fetch_bases_copy(ctypes.byref(c), ctypes.byref(cache.c), _ptr(expanded_host),
+                                       _ptr(n_expanded_host), _ptr(rec_off_host), _ptr(staging),
+                                       int(per_group), _ptr(staged_off_host), _ptr(staged_off),
+                                       ctypes.byref(n), ctypes.c_void_p(copy_stream.cuda_stream),
+                                       ctypes.c_void_p(done_event.cuda_event)))
+    return n.value
+
+
+class BasisCache:
+    """Residency cache table of one layer (sekv_basis_cache_*): n_slots slots
+    of slot_bytes per (sequence, KV head) group, living after the staging
+    area of the caller's staging buffer (see staging_bytes)."""
+
+    def __init__(self, cfg: Config, n_slots: int, slot_bytes: int, device=None):
+        c = cfg.c()
+        n = int(lib().sekv_basis_cache_bytes(ctypes.byref(c), n_slots))
+        if n == 0:
+            raise SekvError("sekv_basis_cache_bytes", -1)
+        self.n_slots, self.slot_bytes = n_slots, slot_bytes
+        self.table = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+        _check("sekv_basis_cache_init", lib().sekv_basis_cache_init(ctypes.byref(c),
+                                                                     _ptr(self.table), n_slots,
+                                                                     _stream()))
+
+    def staging_bytes(self, cfg: Config, per_group: int) -> int:
+        return cfg.batch * cfg.n_kv_heads * (per_group + self.n_slots * self.slot_bytes)
+
+
+def fetch_bases_cached(cfg: Config, cache: LayerCache, expanded, n_expanded, staging,
+                       per_group: int, bcache: BasisCache, staged_off, ws: Workspace, hits=None,
+                       copied=None, stream=None):
+    _need(staging, "staging", torch.uint8); _need(staged_off, "staged_off", torch.int64)
+    if staging.numel() < bcache.staging_bytes(cfg, per_group):
+        raise ValueError("staging: smaller than the staging area plus the cache's slots")
+    c = cfg.c()
+    _check("sekv_fetch_bases_cached",
+           lib().sekv_fetch_bases_cached(ctypes.byref(c), ctypes.byref(cache.c), _ptr(expanded),
+                                         _ptr(n_expanded), _ptr(staging), int(per_group),
+                                         _ptr(bcache.table), bcache.n_slots, bcache.slot_bytes,
+                                         _ptr(staged_off), _ptr(hits), _ptr(copied), ws.ptr(),
+                                         ws.nbytes, _stream(stream)))
     return staging, staged_off
 
 

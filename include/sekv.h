@@ -81,6 +81,15 @@ typedef struct sekv_config {
  * launch gaps between layers. */
 #define SEKV_FLAG_OVERLAP_PREVIOUS 1
 
+/* Fault-path testing only: every wait of a decode kernel for a copy to land
+ * gives up at once if the copy has not landed when it is first tested
+ * (normally it waits up to about two seconds).  Some wait then runs out, the
+ * call's results are unreliable and sekv_workspace_status reports
+ * SEKV_ERR_TIMEOUT (code 2); the kernel still waits, within its own bound,
+ * for every copy it issued before it exits, so the GPU and the workspace
+ * stay usable for the next call. */
+#define SEKV_FLAG_SHORT_WAITS 2
+
 /*
  * One layer of the span cache.  [DE]/[ZH] Methodik 2 and 3: per span the GPU
  * holds an anchor token at full resolution, a routing summary and (this
@@ -168,11 +177,9 @@ sekv_status sekv_workspace_init(void* workspace, size_t bytes, cudaStream_t stre
  *           (sequence, KV head) whose count is out of range), or a build
  *           that found more spans than max_spans (detail: the sequence);
  *   code 2  a bounded wait ran out (SEKV_ERR_TIMEOUT; detail: which wait --
- *           1 producer waiting for a consumer slot, 2 publication of the other
- *           CTAs' routing, 3 copies landing before exit, 4 consumer waiting for
- *           a page, 5 routing weights landing, 6 producer looking for a free
- *           consumer slot, 7 partials landing in the merge, 8 a warp finishing
- *           a record handed over to it);
+ *           3 copies still landing when a warp drains before exit, 4 a warp
+ *           waiting for its next page or record, 5 the routing weights or a
+ *           routing page landing, 7 partials landing in the merge);
  *   code 3  the records do not fit: a fetch group's records exceed its
  *           staging share (detail: the group), or a build's records exceed
  *           the store (detail: the bytes needed, in MiB);
@@ -225,6 +232,79 @@ sekv_status sekv_fetch_bases(const sekv_config* cfg, const sekv_layer_cache* cac
                              void* staging, int64_t staging_per_group,
                              int64_t* staged_off, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * sekv_fetch_bases_copy -- the same fetch driven from the host: one
+ * cudaMemcpyAsync per run of adjacent records, on `copy_stream`, then the
+ * record offsets, then `done` is recorded on `copy_stream` (the caller makes
+ * the attention's stream wait on it).  [DE]/[ZH] Methodik 3: the expanded
+ * span's basis is loaded asynchronously from the CPU.
+ * The expansion lists and the record offsets must be on the host: this is
+ * the path's one device-to-host control crossing per layer (the caller copies
+ * sekv_route's lists back and synchronises before the call).  Records of list
+ * entries whose store offsets follow each other are copied together.
+ *   cache                 store on the host (pinned); only store is read
+ *   expanded_host, n_expanded_host   host copies of sekv_route's lists
+ *   rec_off_host          host copy of cache->rec_off, int64 [B][Hkv][max_spans]
+ *   staging, staging_per_group       as in sekv_fetch_bases
+ *   staged_off_host       pinned host scratch, int64 [B][Hkv][max_spans]
+ *   staged_off            device, int64 [B][Hkv][max_spans] (out, as in
+ *                         sekv_fetch_bases, copied from staged_off_host)
+ *   n_copies              out (may be NULL): the record copies issued
+ * Record sizes come from the records' headers in the host store.  A group
+ * whose records exceed staging_per_group, a list entry out of range, or a
+ * header that disagrees with the span returns SEKV_ERR_CAPACITY or
+ * SEKV_ERR_INVALID before any copy is issued.  The host blocks only to issue
+ * the copies; nothing waits for them.
+ */
+sekv_status sekv_fetch_bases_copy(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                  const int32_t* expanded_host, const int32_t* n_expanded_host,
+                                  const int64_t* rec_off_host, void* staging,
+                                  int64_t staging_per_group, int64_t* staged_off_host,
+                                  int64_t* staged_off, int32_t* n_copies,
+                                  cudaStream_t copy_stream, cudaEvent_t done);
+
+/*
+ * Residency cache of basis records in device memory, kept from call to call
+ * (this build's answer to the pages' CPU-GPU bandwidth limit, [DE] Bedeutung
+ * / [ZH] 意义: an expanded span whose record is still resident costs no
+ * host-link traffic).  Per (sequence, KV head) group: n_slots slots of
+ * slot_bytes each, a table span -> slot, and for every slot its span and the
+ * last call that used it.  Records larger than a slot are never cached.
+ * The slots live right after the staging area in the caller's staging
+ * buffer: group g's slot s starts at byte
+ *   B*Hkv*staging_per_group + (g*n_slots + s)*slot_bytes
+ * of `staging`, so staged offsets of cached and uncached records share one
+ * base.  The table lives in a caller buffer of sekv_basis_cache_bytes()
+ * bytes, which sekv_basis_cache_init() sets to "empty" (once, before the first
+ * fetch).  One cache serves one layer's store.
+ */
+size_t sekv_basis_cache_bytes(const sekv_config* cfg, int32_t n_slots);
+sekv_status sekv_basis_cache_init(const sekv_config* cfg, void* table, int32_t n_slots,
+                                  cudaStream_t stream);
+
+/*
+ * sekv_fetch_bases_cached -- sekv_fetch_bases through the residency cache.
+ * For each list entry: a span whose record is resident (hit) gets its slot's
+ * offset; a miss that fits a slot takes a slot that no entry of this call
+ * uses (the first such slots from the group's clock hand on, evicting what
+ * they held) and its record is copied there from the host store; a miss that
+ * does not fit a slot, or finds no free slot, is copied to the staging area
+ * as in sekv_fetch_bases.  Two kernels on `stream` (plan, then copy).
+ *   staging     device, >= B*Hkv*(staging_per_group + n_slots*slot_bytes)
+ *   slot_bytes  multiple of 16
+ *   hits        int32 [B][Hkv] (device, out, may be NULL): hits per group
+ *   copied      int64 [B][Hkv] (device, out, may be NULL): record bytes this
+ *               call copies over the host link, per group
+ * Errors as in sekv_fetch_bases (the staging share per group applies to the
+ * records that do not go to slots).
+ */
+sekv_status sekv_fetch_bases_cached(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                    const int32_t* expanded, const int32_t* n_expanded,
+                                    void* staging, int64_t staging_per_group, void* table,
+                                    int32_t n_slots, int32_t slot_bytes, int64_t* staged_off,
+                                    int32_t* hits, int64_t* copied, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * sekv_decode_attention -- mixed-resolution attention of one layer for a

@@ -234,3 +234,107 @@ def test_invalid_arguments_rejected_on_host(sk):
         sk.decode_step(cfg, cache, case.q.cuda(), case.W.cuda(),
                        torch.from_numpy(case.theta).cuda(), SCALE, small)
     assert e.value.status == -2
+
+
+def test_short_waits_time_out_and_leave_the_gpu_usable(sk):
+    """With SEKV_FLAG_SHORT_WAITS every wait for a copy gives up if the copy
+    has not landed at its first test: some wait runs out, the device status
+    reports a timeout (code 2, never a fault), every issued copy still lands
+    before the kernel exits, and the next regular call on the same
+    workspace is correct."""
+    case = decode_case("llama3_8b_32k", ctx=16384)
+    cfg = sk_config(sk, case)
+    cache = sk.LayerCache(to_dev(case))
+    ws = sk.Workspace(cfg)
+    short = sk.Config(**{**cfg.__dict__, "flags": sk.sekv.FLAG_SHORT_WAITS})
+    th = torch.from_numpy(case.theta).cuda()
+    sk.decode_step(short, cache, case.q.cuda(), case.W.cuda(), th, SCALE, ws)
+    code, detail = ws.status()
+    assert code == 2 and detail in (3, 4, 5, 7), (code, detail)
+    assert ws.status() == (0, 0)
+    out, lse, _, _ = sk.decode_step(cfg, cache, case.q.cuda(), case.W.cuda(), th, SCALE, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    compare_out(out.cpu().numpy(), case.o, "after the timed-out call")
+
+
+def test_fetch_copy_path_matches_oracle(sk):
+    """The host-driven fetch (one cudaMemcpyAsync per run of adjacent
+    records on a side stream, then an event the attention waits on) gives
+    the oracle's attention."""
+    case = decode_case("llama3_8b_32k", ctx=8192, batch=2, expand_frac=0.2)
+    cfg = sk_config(sk, case)
+    dev = to_dev(case)
+    host = dict(dev)
+    host["store"] = case.tensors["store"].pin_memory()
+    cache_h = sk.LayerCache(host, store_on_host=True)
+    ws = sk.Workspace(cfg)
+    lst, cnt, _ = sk.route(cfg, cache_h, case.q.cuda(), case.W.cuda(),
+                           torch.from_numpy(case.theta).cuda(), ws)
+    lst_h = lst.cpu()
+    cnt_h = cnt.cpu()
+    rec_off_h = case.tensors["rec_off"].contiguous()
+    NG = case.wcfg.batch * case.wcfg.n_kv_heads
+    ms = case.tensors["max_spans"]
+    per_group = 8 << 20
+    staging = torch.empty(NG * per_group, dtype=torch.uint8, device="cuda")
+    staged_off = torch.empty(NG * ms, dtype=torch.int64, device="cuda")
+    staged_off_h = torch.empty(NG * ms, dtype=torch.int64).pin_memory()
+    side = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    n = sk.fetch_bases_copy(cfg, cache_h, lst_h, cnt_h, rec_off_h, staging, per_group,
+                            staged_off_h, staged_off, done, side)
+    assert 0 < n <= int(cnt_h.sum())
+    torch.cuda.current_stream().wait_event(done)
+    out, _ = sk.decode_attention(cfg, cache_h, case.q.cuda(), lst, cnt, SCALE, ws,
+                                 staging=staging, staged_off=staged_off)
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    compare_out(out.cpu().numpy(), case.o, "copy fetch")
+
+
+@pytest.mark.parametrize("n_slots", [512, 8])
+def test_cached_fetch_matches_oracle_hits_and_evictions(sk, n_slots):
+    """Fetch through the residency cache: a first call misses everywhere, a
+    second call with the same lists hits everywhere (when the pool holds
+    them), a different query hits partly; with 8 slots per group most
+    records evict others or go to staging.  Every call's attention is the
+    oracle's."""
+    cases = [decode_case("llama3_8b_32k", ctx=8192, expand_frac=0.2, seed=s) for s in (7, 8)]
+    cfg = sk_config(sk, cases[0])
+    dev = to_dev(cases[0])
+    host = dict(dev)
+    host["store"] = cases[0].tensors["store"].pin_memory()
+    cache_h = sk.LayerCache(host, store_on_host=True)
+    ws = sk.Workspace(cfg)
+    NG = cfg.batch * cfg.n_kv_heads
+    ms = cfg.max_spans
+    per_group = 8 << 20
+    bc = sk.BasisCache(cfg, n_slots, 20480)
+    staging = torch.empty(bc.staging_bytes(cfg, per_group), dtype=torch.uint8, device="cuda")
+    staged_off = torch.empty(NG * ms, dtype=torch.int64, device="cuda")
+    hits = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    for i, case in enumerate([cases[0], cases[0], cases[1], cases[0]]):
+        lst, cnt, _ = sk.route(cfg, cache_h, case.q.cuda(), case.W.cuda(),
+                               torch.from_numpy(case.theta).cuda(), ws)
+        sk.fetch_bases_cached(cfg, cache_h, lst, cnt, staging, per_group, bc, staged_off, ws,
+                              hits=hits)
+        out, _ = sk.decode_attention(cfg, cache_h, case.q.cuda(), lst, cnt, SCALE, ws,
+                                     staging=staging, staged_off=staged_off)
+        torch.cuda.synchronize()
+        assert ws.status() == (0, 0)
+        compare_out(out.cpu().numpy(), case.o, f"cached fetch call {i} ({n_slots} slots)")
+        h, c = hits.cpu(), cnt.cpu()
+        if i == 0:
+            assert int(h.sum()) == 0
+        if i == 1 and n_slots == 512:
+            # everything that fits a 20 KB slot is resident from call 0
+            big = 0
+            for g in range(NG):
+                for k in lst[g * ms:g * ms + int(c[g])].cpu().tolist():
+                    rk = int(case.tensors["rec_rank"].view(-1)[g * ms + k])
+                    body = int(case.tensors["body_len"].view(-1)[(g // cfg.n_kv_heads) * ms + k])
+                    big += sk.record_size(body, rk & 0xFFFF, rk >> 16) > 20480
+            assert int(h.sum()) == int(c.sum()) - big
+        if n_slots == 8:
+            assert (h <= 8).all()
