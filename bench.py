@@ -363,57 +363,225 @@ def run_resident(sk, cfg, ws, layers, steps, warmup, ws_n, clocks):
     return ms, ck
 
 
-def run_tiered(sk, cfg, layers, steps, warmup, ws_n, dev):
-    """End to end through the C ABI: per step, every layer's query goes H2D from
-    pinned memory, routing runs on the GPU, the expanded spans' bases are
-    fetched from the pinned host tier over the host link, attention runs on
-    the staged bases, and the outputs come back D2H."""
+def h2d_peak_gbs(dev, nbytes: int = 1 << 30) -> float:
+    """Host-link peak: one large pinned host -> device copy, best of 6, timed
+    with CUDA events."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(6):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del src, dst
+    return best
+
+
+QUERY_SETS = 8        # distinct queries per layer, used in turn by successive steps
+QUERY_DRIFT = 0.3     # q_s = sqrt(1 - d^2) q_(s-1) + d n, n ~ N(0, 1)
+CACHE_SLOTS = 256     # residency cache slots per (sequence, KV head), 20 KB each
+CACHE_SLOT_BYTES = 20480
+STAGING_PER_GROUP = 8 << 20
+
+
+def drifting_queries(layers, seed: int):
+    """QUERY_SETS query sets per layer: set 0 is the layer's query; each next
+    set moves away from the previous one by QUERY_DRIFT (successive decode
+    tokens' queries are correlated, so their expansion sets overlap)."""
+    g = torch.Generator().manual_seed(seed)
+    sets = [torch.stack([L["q"].cpu() for L in layers])]
+    c = math.sqrt(1.0 - QUERY_DRIFT ** 2)
+    for _ in range(QUERY_SETS - 1):
+        prev = sets[-1].float()
+        nxt = c * prev + QUERY_DRIFT * torch.randn(prev.shape, generator=g)
+        sets.append(nxt.to(torch.bfloat16))
+    return [x.pin_memory() for x in sets]
+
+
+def run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev):
+    """End to end through the C ABI with host buffers.  Each step copies every
+    layer's query from pinned host memory, routes it, fetches the expanded
+    spans' bases through the residency cache (misses over the host link from
+    the pinned host store), attends, and reads every layer's output back.
+    Routing and fetch of a layer run on a side stream that runs ahead of the
+    attention stream, so the fetch of layer l+1 overlaps the attention of
+    layer l (every layer's query is an input of the step).  Successive steps
+    use drifting query sets (drifting_queries), so the cache sees the partial
+    reuse of consecutive tokens."""
     scale = sk.default_scale()
     cfg_t = sk.Config(**{**cfg.__dict__, "flags": 0})
-    ws = sk.Workspace(cfg_t, dev)
+    ws_main = sk.Workspace(cfg_t, dev)
+    ws_sides = [sk.Workspace(cfg_t, dev), sk.Workspace(cfg_t, dev)]
     L_n, B, Hq = len(layers), cfg.batch, cfg.n_q_heads
-    NG = B * cfg.n_kv_heads
-    q_host = torch.stack([L["q"].cpu() for L in layers]).pin_memory()
-    q_dev = torch.empty_like(q_host, device=dev)
+    NG, ms = B * cfg.n_kv_heads, cfg.max_spans
+    q_sets = drifting_queries(layers, w.seed * 31 + 5)
+    q_dev = torch.empty_like(q_sets[0], device=dev)
     out_dev = torch.empty(L_n, B, Hq, 128, device=dev)
     out_host = torch.empty(L_n, B, Hq, 128).pin_memory()
-    caches = []
+    per = []
     for L in layers:
         host = dict(L["t"])
         host["store"] = L["t"]["store"].cpu().pin_memory()
-        caches.append(sk.LayerCache(host, store_on_host=True))
-    per_group = 16 << 20
-    staging = torch.empty(NG * per_group, dtype=torch.uint8, device=dev)
-    staged_off = torch.empty(NG * cfg.max_spans, dtype=torch.int64, device=dev)
-    lst = torch.empty(NG * cfg.max_spans, dtype=torch.int32, device=dev)
-    cnt = torch.empty(NG, dtype=torch.int32, device=dev)
+        bc = sk.BasisCache(cfg_t, CACHE_SLOTS, CACHE_SLOT_BYTES, dev)
+        per.append(dict(cache=sk.LayerCache(host, store_on_host=True), bc=bc,
+                        staging=torch.empty(bc.staging_bytes(cfg_t, STAGING_PER_GROUP),
+                                            dtype=torch.uint8, device=dev),
+                        staged_off=torch.empty(NG * ms, dtype=torch.int64, device=dev),
+                        lst=torch.empty(NG * ms, dtype=torch.int32, device=dev),
+                        cnt=torch.empty(NG, dtype=torch.int32, device=dev),
+                        hits=torch.zeros(NG, dtype=torch.int32, device=dev),
+                        copied=torch.zeros(NG, dtype=torch.int64, device=dev),
+                        ev=torch.cuda.Event()))
+    # two side streams take the layers in turn, so that one layer's routing
+    # and planning overlap the previous layer's copies over the host link
+    sides = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ev_q, ev_end = torch.cuda.Event(), [torch.cuda.Event(), torch.cuda.Event()]
     launches = [0]
 
-    def step():
+    def step(s):
+        main = torch.cuda.current_stream()
         n = 0
-        q_dev.copy_(q_host, non_blocking=True)
+        q_dev.copy_(q_sets[s], non_blocking=True)
+        ev_q.record(main)
+        for sd in sides:
+            sd.wait_event(ev_q)
         for i, L in enumerate(layers):
-            sk.route(cfg_t, caches[i], q_dev[i], L["W"], L["theta"], ws, expanded=lst,
-                     n_expanded=cnt)
+            X = per[i]
+            side, ws_side = sides[i % 2], ws_sides[i % 2]
+            sk.route(cfg_t, X["cache"], q_dev[i], L["W"], L["theta"], ws_side, expanded=X["lst"],
+                     n_expanded=X["cnt"], stream=side)
             n += sk.last_launch_count()
-            sk.fetch_bases(cfg_t, caches[i], lst, cnt, staging, per_group, staged_off, ws)
+            sk.fetch_bases_cached(cfg_t, X["cache"], X["lst"], X["cnt"], X["staging"],
+                                  STAGING_PER_GROUP, X["bc"], X["staged_off"], ws_side,
+                                  hits=X["hits"], copied=X["copied"], stream=side)
             n += sk.last_launch_count()
-            sk.decode_attention(cfg_t, caches[i], q_dev[i], lst, cnt, scale, ws,
-                                staging=staging, staged_off=staged_off, out=out_dev[i])
+            X["ev"].record(side)
+            main.wait_event(X["ev"])
+            sk.decode_attention(cfg_t, X["cache"], q_dev[i], X["lst"], X["cnt"], scale, ws_main,
+                                staging=X["staging"], staged_off=X["staged_off"],
+                                out=out_dev[i], stream=main)
             n += sk.last_launch_count()
+        for sd, ev in zip(sides, ev_end):
+            ev.record(sd)
+            main.wait_event(ev)
         out_host.copy_(out_dev, non_blocking=True)
         launches[0] = n
 
     stream = torch.cuda.Stream()
-    ms, _ = time_graph(step, steps, warmup, stream, ws_n, None)
-    code, detail = ws.status()
-    if code:
-        raise RuntimeError(f"device status {code} ({detail}) after the tiered run")
-    ref = torch.stack([L["out"] for L in layers]).cpu()
-    err = float((out_host - ref).abs().max())
-    h2d = q_host.numel() * 2 + sum(L["fetched"] for L in layers)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for s in range(QUERY_SETS):
+            step(s)
+        torch.cuda.synchronize()
+        for s in range(QUERY_SETS):
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                step(s)
+            graphs.append(gph)
+    for i in range(max(warmup, 3) + QUERY_SETS):
+        with torch.cuda.stream(stream):
+            graphs[i % QUERY_SETS].replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % QUERY_SETS].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    ms_total = e0.elapsed_time(e1)
+    for W_ in (*ws_sides, ws_main):
+        code, detail = W_.status()
+        if code:
+            raise RuntimeError(f"device status {code} ({detail}) after the tiered run")
+    last = (steps - 1) % QUERY_SETS
+    n_exp = sum(int(X["cnt"].sum()) for X in per)
+    hits = sum(int(X["hits"].sum()) for X in per)
+    copied = sum(int(X["copied"].sum()) for X in per)
+    # the last step's outputs against the resident path on the same queries
+    ws_r = sk.Workspace(cfg_t, dev)
+    err = 0.0
+    for i, L in enumerate(layers):
+        o, _, _, _ = sk.decode_step(cfg_t, L["cache"], q_sets[last][i].to(dev), L["W"], L["theta"],
+                                    scale, ws_r)
+        err = max(err, float((out_host[i] - o.cpu()).abs().max()))
+    h2d = q_sets[0].numel() * 2 + copied
     d2h = out_host.numel() * 4
-    return ms, h2d, d2h, launches[0], err
+    return dict(ms=ms_total, steps=steps, h2d=h2d, d2h=d2h, launches=launches[0], err=err,
+                hit_frac=hits / max(1, n_exp), copied=copied, n_exp=n_exp,
+                fetch_paths=fetch_path_times(sk, cfg_t, layers, per, q_sets, dev))
+
+
+def fetch_path_times(sk, cfg, layers, per, q_sets, dev):
+    """One step's fetch of every layer's expanded bases (query set 0) by the
+    three forms, timed on their own: the gather kernel over mapped pinned
+    memory, the host-driven copies (lists back to the host, one
+    cudaMemcpyAsync per run of adjacent records, an event), and the warm
+    residency cache."""
+    ws = sk.Workspace(cfg, dev)
+    NG, ms = cfg.batch * cfg.n_kv_heads, cfg.max_spans
+    q = q_sets[0].to(dev)
+    lists = []
+    for i, L in enumerate(layers):
+        lst, cnt, _ = sk.route(cfg, per[i]["cache"], q[i], L["W"], L["theta"], ws)
+        lists.append((lst, cnt))
+    torch.cuda.synchronize()
+    staging = torch.empty(NG * STAGING_PER_GROUP, dtype=torch.uint8, device=dev)
+    staged_off = torch.empty(NG * ms, dtype=torch.int64, device=dev)
+    # gather kernel
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(len(layers)):
+        sk.fetch_bases(cfg, per[i]["cache"], lists[i][0], lists[i][1], staging, STAGING_PER_GROUP,
+                       staged_off, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    gather_ms = e0.elapsed_time(e1)
+    # host-driven copies, including the lists' trip to the host
+    side = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    lst_h = torch.empty(NG * ms, dtype=torch.int32).pin_memory()
+    cnt_h = torch.empty(NG, dtype=torch.int32).pin_memory()
+    off_h = torch.empty(NG * ms, dtype=torch.int64).pin_memory()
+    rec_off_h = [L["t"]["rec_off"].cpu().contiguous() for L in layers]
+    copies = 0
+    t0 = time.perf_counter()
+    for i in range(len(layers)):
+        lst_h.copy_(lists[i][0], non_blocking=True)
+        cnt_h.copy_(lists[i][1], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        copies += sk.fetch_bases_copy(cfg, per[i]["cache"], lst_h, cnt_h, rec_off_h[i], staging,
+                                      STAGING_PER_GROUP, off_h, staged_off, done, side)
+        done.synchronize()
+    copy_ms = (time.perf_counter() - t0) * 1e3
+    # residency cache, warm (the tables hold the timed run's last state)
+    e0.record()
+    for i in range(len(layers)):
+        X = per[i]
+        sk.fetch_bases_cached(cfg, X["cache"], lists[i][0], lists[i][1], X["staging"],
+                              STAGING_PER_GROUP, X["bc"], X["staged_off"], ws, hits=X["hits"],
+                              copied=X["copied"])
+    e1.record()
+    torch.cuda.synchronize()
+    cached_ms = e0.elapsed_time(e1)
+    rec_bytes = sum(L["fetched"] for L in layers)
+    return {"record_bytes_per_step": rec_bytes,
+            "gather_kernel_ms_per_step": gather_ms,
+            "gather_kernel_gbs": rec_bytes / (gather_ms / 1e3) / 1e9,
+            "memcpy_per_run_ms_per_step": copy_ms, "memcpy_copies_per_step": copies,
+            "memcpy_per_run_gbs": rec_bytes / (copy_ms / 1e3) / 1e9,
+            "cached_ms_per_step": cached_ms,
+            "note": "query set 0 of every layer; the memcpy form is host wall time including "
+                    "the lists' device-to-host trip and a synchronisation per layer"}
 
 
 # ----------------------------------------------------------------------------
@@ -781,16 +949,26 @@ def main():
                          "avg_launch_us": launch_s * 1e6},
             "clocks": ck, "gpu_launches": args.steps * len(layers)}
     if not args.no_e2e:
-        e_steps = max(10, args.steps // 4)
-        ms_e, h2d, d2h, nl, err = run_tiered(sk, cfg, layers, e_steps, args.warmup, ws_n, dev)
-        ms_e = max_over_ranks(ms_e, ws_n)
+        e_steps = max(16, args.steps // 4)
+        peak_h2d = h2d_peak_gbs(dev)
+        r = run_tiered(sk, cfg, w, layers, e_steps, args.warmup, ws_n, dev)
+        ms_e = max_over_ranks(r["ms"], ws_n)
+        step_s = ms_e / e_steps / 1e3
         line["e2e"] = {"value": ws_n * e_steps / (ms_e / 1e3), "unit": UNIT,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "path": "tiered: q H2D, route, fetch bases from pinned host over the "
-                               "host link, attend, out D2H; one CUDA graph per step",
-                       "h2d_gbs": h2d / (ms_e / e_steps / 1e3) / 1e9,
-                       "steps": e_steps, "max_abs_vs_resident": err}
-        line["gpu_launches"] += e_steps * nl
+                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                       "path": "tiered: q H2D; per layer route + residency-cached fetch of the "
+                               "bases from pinned host memory on a side stream running ahead "
+                               "of attention; out D2H; one CUDA graph per step",
+                       "queries": f"{QUERY_SETS} drifting query sets in turn (drift "
+                                  f"{QUERY_DRIFT} per step)",
+                       "cache": {"slots_per_group": CACHE_SLOTS, "slot_bytes": CACHE_SLOT_BYTES,
+                                 "hit_frac": r["hit_frac"], "expanded_per_step": r["n_exp"],
+                                 "record_bytes_copied_per_step": r["copied"]},
+                       "h2d_gbs": r["h2d"] / step_s / 1e9, "h2d_peak_gbs": peak_h2d,
+                       "h2d_frac_of_peak": r["h2d"] / step_s / 1e9 / peak_h2d,
+                       "fetch_paths": r["fetch_paths"],
+                       "steps": e_steps, "max_abs_vs_resident": r["err"]}
+        line["gpu_launches"] += e_steps * r["launches"]
     if not args.no_cpu_baseline and rank == 0:
         line["cpu_baseline"] = cpu_baseline_leg(w, args.cpu_seconds)
         line["parity"] = parity_check(sk, cfg, ws, layers[0], w)
