@@ -763,6 +763,35 @@ def build_bytes(w, inp, out) -> int:
     return int(rd + wr + recb.item())
 
 
+def fp32_peak_tflops(dev) -> dict:
+    """fp32 arithmetic rate: a cuBLAS SGEMM (8192^3, TF32 off) timed with CUDA
+    events, best of 5, and the nominal 152 SMs x 128 fma/clock x 2 x max clock."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    n = 8192
+    a = torch.randn(n, n, device=dev)
+    b = torch.randn(n, n, device=dev)
+    best = 0.0
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, 2.0 * n ** 3 / (e0.elapsed_time(e1) / 1e3) / 1e12)
+    torch.backends.cuda.matmul.allow_tf32 = prev
+    props = torch.cuda.get_device_properties(dev)
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except (OSError, ValueError):
+        pass
+    return {"measured": best,
+            "nominal": props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12}
+
+
 def run_build_bench(args, ws_n, rank, local):
     """Prefill cache build at 128K (Mistral-7B shape): segmentation, summaries
     and the batched gated span SVD of every span, one layer per call.  Two
@@ -794,6 +823,7 @@ def run_build_bench(args, ws_n, rank, local):
             sk.build_spans(cfg, L["K"], L["V"], L["H"], L["W"], L["g"], L["out"], ws, stream=stream)
     torch.cuda.synchronize()
     ws.raise_on_error()
+    sk.build_flops(ws)  # clear the warm-up calls' count
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(ws_n)
     torch.cuda.synchronize()
@@ -811,12 +841,15 @@ def run_build_bench(args, ws_n, rank, local):
     ck = clocks.stop()
     barrier(ws_n)
     ws.raise_on_error()
+    flops = sk.build_flops(ws) / args.steps
     ms_total = max_over_ranks(e0.elapsed_time(e1), ws_n)
     per_call = ms_total / 1e3 / args.steps
     tokens = w.batch * w.ctx
     nbytes = sum(build_bytes(w, L["inp"], L["out"]) for L in layers) / 2
     peak, peak_kind = measured_peaks()
     achieved = nbytes / per_call / 1e9
+    fp32 = fp32_peak_tflops(dev)
+    alu = flops / per_call / 1e12
     if rank != 0:
         return
     line = {"metric": "prefill cache build tokens/s at 128K ctx (one layer per call)",
@@ -828,10 +861,17 @@ def run_build_bench(args, ws_n, rank, local):
                        "kv_heads": w.n_kv_heads, "rank_cap": w.rank_cap,
                        "spans_per_head": int(np.mean([int(L["out"]["n_spans"][0]) for L in layers])),
                        "l2": "two layers of distinct inputs alternate (1 GB of K/V)"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                         "bytes_per_call": nbytes,
-                         "note": "the batched Jacobi SVD is ALU-bound; this is the HBM fraction"},
+            "roofline": {"bound": "alu", "achieved": alu, "peak": fp32["measured"],
+                         "unit": "TFLOP/s", "frac": alu / fp32["measured"], "traffic": None,
+                         "peak_kind": "measured fp32 (cuBLAS SGEMM, TF32 off)",
+                         "flops_per_call": flops,
+                         "flops_counted": "fp32 operations the span SVDs performed (fma = 2): "
+                                          "Gram matrices, the Jacobi sweeps actually run, "
+                                          "projections (counted by the kernel)",
+                         "fp32_nominal_tflops": fp32["nominal"],
+                         "frac_of_nominal": alu / fp32["nominal"]},
+            "hbm": {"achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "peak_kind": peak_kind, "bytes_per_call": nbytes},
             "clocks": ck, "gpu_launches": None}
     print(json.dumps(line), flush=True)
 

@@ -19,6 +19,7 @@ from .sekv import (  # noqa: F401
     fetch_bases_cached,
     BasisCache,
     build_spans,
+    build_flops,
     alloc_cache,
     record_size,
     last_launch_count,

@@ -35,6 +35,7 @@ struct BuildParams {
   int64_t store_capacity;
   // workspace
   int32_t* status;
+  unsigned long long* flops;  // fp32 operations the span SVDs performed (fma = 2), summed
   int32_t* starts;         // [B][max_spans] anchor positions
   int64_t* rel_off;        // [B*Hkv][max_spans] record offset within its group
   int64_t* gtotal;         // [B*Hkv]

@@ -86,6 +86,7 @@ extern "C" sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len,
   P.store = static_cast<uint8_t*>(out->store);
   P.store_capacity = out->store_capacity;
   P.status = reinterpret_cast<int32_t*>(w + L.status);
+  P.flops = reinterpret_cast<unsigned long long*>(w + L.status + 16);
   P.starts = reinterpret_cast<int32_t*>(w + L.starts);
   P.rel_off = reinterpret_cast<int64_t*>(w + L.rel_off);
   P.gtotal = reinterpret_cast<int64_t*>(w + L.gtotal);
@@ -121,5 +122,16 @@ extern "C" sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len,
   if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
   if (launch_svd_all(P, sms, stream) != cudaSuccess) return SEKV_ERR_CUDA;
   count_launch(8);
+  return SEKV_OK;
+}
+
+extern "C" sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, int64_t* flops) {
+  if (!workspace || !flops) return SEKV_ERR_INVALID;
+  unsigned long long v = 0;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (cudaMemcpy(&v, w + 16, 8, cudaMemcpyDeviceToHost) != cudaSuccess) return SEKV_ERR_CUDA;
+  if (cudaMemset(w + 16, 0, 8) != cudaSuccess) return SEKV_ERR_CUDA;
+  *flops = int64_t(v);
   return SEKV_OK;
 }

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
 
     // ---- cyclic Jacobi, parallel (tournament) ordering ---------------------
     const int nn = (n + 1) & ~1;
+    int sweeps = 0;  // sweeps that rotated (for the operation count)
     for (int sweep = 0; sweep < 24; ++sweep) {
       float off = 0.f, dg = 0.f;
       for (int e = tid; e < n * n; e += NT) {
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       // diagonal; stop once it is under 1e-12 of it (inside the build's
       // accuracy bars: sigma 1e-3 relative, reconstruction 5e-3)
       if (!(off > 1e-12f * dg)) break;
+      ++sweeps;
       for (int rd = 0; rd < nn - 1; ++rd) {
         __syncthreads();
         for (int kk = tid; kk < nn / 2; kk += NT) {
@@ -224,6 +226,19 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       __syncthreads();
     }
     __syncthreads();
+    if (tid == 0 && P.flops != nullptr) {
+      // fp32 operations of this body (an fma counts 2): the Gram matrix, every
+      // sweep's norms and rotations of G's rows and columns and of the
+      // eigenvectors (3 per updated element), and the projection onto the
+      // other side for the r kept components
+      const unsigned long long nq = (unsigned long long)n;
+      const unsigned long long gram =
+          LARGE ? 128ull * 129ull * (unsigned long long)bl : nq * (nq + 1ull) * 128ull;
+      const unsigned long long sweep_ops =
+          2ull * nq * nq + (unsigned long long)(nn - 1) * (nn / 2) * nq * 18ull;
+      const unsigned long long proj = 2ull * (unsigned long long)r * 128ull * (unsigned long long)bl;
+      atomicAdd(P.flops, gram + (unsigned long long)sweeps * sweep_ops + proj);
+    }
     // ---- order eigenvalues descending (ties by index) ----------------------
     for (int i = tid; i < n; i += NT) {
       const float li = G[i * LD + i];

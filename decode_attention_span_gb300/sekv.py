@@ -32,7 +32,7 @@ EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
            "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
-           "sekv_fetch_bases_cached",
+           "sekv_fetch_bases_cached", "sekv_build_flops",
            "sekv_status_string", "sekv_last_launch_count")
 
 
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.sekv_fetch_bases.restype = _c_i32
         L.sekv_fetch_bases.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]
+        L.sekv_build_flops.restype = _c_i32
+        L.sekv_build_flops.argtypes = [_c_vp, _c_vp, ctypes.POINTER(_c_i64)]
         L.sekv_basis_cache_bytes.restype = _c_sz
         L.sekv_basis_cache_bytes.argtypes = [ctypes.POINTER(SekvConfig), _c_i32]
         L.sekv_basis_cache_init.restype = _c_i32
@@ -441,6 +443,14 @@ def build_spans(cfg: Config, K, V, H, W_r, gates, out: Dict[str, torch.Tensor], 
                                   _ptr(gates), ctypes.byref(o), ws.ptr(), ws.nbytes,
                                   _stream(stream)))
     return out
+
+
+def build_flops(ws: Workspace, stream=None) -> int:
+    """fp32 operations the span SVDs of the builds on `ws` performed since the
+    last read (sekv_build_flops); synchronises and clears the count."""
+    v = _c_i64(0)
+    _check("sekv_build_flops", lib().sekv_build_flops(ws.ptr(), _stream(stream), ctypes.byref(v)))
+    return v.value
 
 
 def default_scale() -> float:

@@ -418,6 +418,13 @@ sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len, const void
                              const float* gates, const sekv_cache_out* out, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* Measurement helper (no counterpart on the pages): synchronise `stream` and
+ * return in *flops the fp32 operations (an fma counts 2) that the span SVDs
+ * of the sekv_build_spans calls on this build workspace performed since the
+ * last read -- Gram matrices, the Jacobi sweeps actually run, projections --
+ * then clear the count.  For reporting the build's arithmetic rate. */
+sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, int64_t* flops);
+
 /* Human-readable name of a status. */
 const char* sekv_status_string(sekv_status status);
 

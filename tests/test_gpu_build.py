@@ -30,16 +30,17 @@ def sk():
     return sk
 
 
-def run_build(sk, w, inp):
+def run_build(sk, w, inp, store_bytes=256 << 20):
     ms = inp["max_spans"]
     cfg = sk.Config(w.batch, w.n_q_heads, w.n_kv_heads, w.n_sink, w.n_recent, ms, w.rank_cap,
                     w.len_min, w.len_max, w.tau)
     ws = sk.Workspace(cfg, which=sk.sekv.SEKV_CALL_BUILD, ctx_len=w.ctx)
-    out = sk.alloc_cache(cfg, 256 << 20)
+    out = sk.alloc_cache(cfg, store_bytes)
     sk.build_spans(cfg, inp["K"].cuda(), inp["V"].cuda(), torch.from_numpy(inp["H"]).cuda(),
                    inp["W_r"].cuda(), torch.from_numpy(inp["gates"]).cuda(), out, ws)
     torch.cuda.synchronize()
     assert ws.status() == (0, 0)
+    out["_ws"] = ws
     return cfg, out
 
 
@@ -98,6 +99,16 @@ def test_build_pr1(sk):
     inp = gen.build_inputs(w, 0)
     cfg, out = run_build(sk, w, inp)
     check_build(w, inp, out)
+    # the operation count covers at least the Gram matrices (n(n+1)/2 dot
+    # products of length m = 128 or the body, both sides of every span) and
+    # is cleared by the read
+    b = out["body_len"][0, :int(out["n_spans"][0])].cpu().numpy().astype(np.int64)
+    n = np.minimum(b, 128)
+    m = np.where(b > 128, b, 128)
+    gram = int(np.sum(n * (n + 1) * m)) * w.n_kv_heads * 2
+    flops = sk.build_flops(out["_ws"])
+    assert flops >= gram > 0
+    assert sk.build_flops(out["_ws"]) == 0
 
 
 @pytest.mark.parametrize("over", [
@@ -134,3 +145,76 @@ def test_build_then_decode(sk):
     for c in range(w.n_kv_heads):
         assert np.array_equal(lst[c, :cnt[c]], E[0][c])
     compare_out(o.cpu().numpy(), o_ref, "built cache")
+
+
+def test_build_128k_every_head_sampled_spans(sk):
+    """One layer of the 128K prefill build at its stated shape (8 KV heads,
+    131,072 tokens, about 4,100 spans per head): every span boundary, anchor
+    and rank is checked; summaries, singular values and reconstructions on a
+    stated sample of 40 spans per head (spread over the sequence, plus the
+    longest bodies), each against the oracle's routines for that span."""
+    w = synth.get_config("mistral_7b_build_128k", layers=1)
+    inp = gen.build_inputs(w, 0, device="cuda")
+    cfg, out = run_build(sk, w, inp, store_bytes=1 << 30)
+    K, V = inp["K"], inp["V"]
+    H = inp["H"][0]
+    anchors, lens = oracle.segment(H, w.n_sink, w.n_recent, w.tau, w.len_min, w.len_max)
+    n_sp = len(lens)
+    assert int(out["n_spans"][0]) == n_sp and n_sp > 3800
+    assert np.array_equal(out["body_len"][0, :n_sp].cpu().numpy(), lens - 1)
+    m1 = w.ctx - w.n_recent
+    full_idx = torch.as_tensor(np.concatenate([np.arange(w.n_sink), anchors,
+                                               np.arange(m1, w.ctx)]), device="cuda")
+    nf = len(full_idx)
+    assert torch.equal(out["k_full"][0, :, :nf], K[0][:, full_idx])
+    assert torch.equal(out["v_full"][0, :, :nf], V[0][:, full_idx])
+    gates = inp["gates"]
+    rr = out["rec_rank"][0, :, :n_sp].cpu().numpy()
+    # ranks of every span from the gates (longest prefix above 0.5, at most
+    # min(rank_cap, body)) -- the rule of oracle.span_svd
+    for c in range(w.n_kv_heads):
+        for side, rk in ((0, rr[c] & 0xFFFF), (1, rr[c] >> 16)):
+            g = gates[0, c, side, :n_sp] > 0.5
+            R = np.minimum(w.rank_cap, lens - 1)
+            prefix = np.where(g.all(axis=1), w.rank_cap, np.argmin(g, axis=1))
+            assert np.array_equal(rk, np.minimum(prefix, R) * (lens > 1)), (c, side)
+    body = lens - 1
+    sample = sorted(set(np.linspace(0, n_sp - 1, 32).astype(int).tolist()) |
+                    set(np.argsort(-body)[:8].tolist()))
+    store = out["store"]
+    rec_off = out["rec_off"][0].cpu().numpy()
+    s_route = out["s_route"][0].cpu().numpy()
+    k_sum = out["k_sum"][0].float().cpu().numpy()
+    v_sum = out["v_sum"][0].float().cpu().numpy()
+    W = inp["W_r"].cpu().numpy()
+    worst = dict(s=0.0, ulps=0.0, sigma=0.0, recon=0.0)
+    for c in range(w.n_kv_heads):
+        for k in sample:
+            lo, hi = int(anchors[k]) + 1, int(anchors[k]) + int(lens[k])
+            if hi <= lo:
+                continue
+            Kb = K[0, c, lo:hi].double().cpu().numpy()
+            Vb = V[0, c, lo:hi].double().cpu().numpy()
+            s_ref = oracle.routing_summary(Kb, H[lo:hi], W[c]).astype(np.float32)
+            worst["s"] = max(worst["s"], float(np.abs(s_route[c, k] - s_ref).max()))
+            km, vm = oracle.attention_summary(Kb, Vb)
+            for got, ref in ((k_sum[c, k], oracle.bf16_round(km)), (v_sum[c, k], oracle.bf16_round(vm))):
+                worst["ulps"] = max(worst["ulps"], float((np.abs(got - ref) / ulp_bf16(ref)).max()))
+            size = sk.record_size(hi - lo, int(rr[c, k] & 0xFFFF), int(rr[c, k] >> 16))
+            raw = store[int(rec_off[c, k]):int(rec_off[c, k]) + size].cpu().numpy()
+            F = layout.unpack_record(np.concatenate([raw, np.zeros(16, np.uint8)]), 0, hi - lo)
+            for side, M in (("K", Kb), ("V", Vb)):
+                fr = oracle.span_svd(M, gates[0, c, 0 if side == "K" else 1, k], w.rank_cap)
+                sg = getattr(F, "s" + side)
+                assert len(sg) == fr.rank
+                if fr.rank == 0:
+                    continue
+                worst["sigma"] = max(worst["sigma"], float(np.max(np.abs(sg - fr.sigma) / fr.sigma)))
+                Rg = oracle.reconstruct(getattr(F, "U" + side), sg, getattr(F, "g" + side),
+                                        getattr(F, "Vt" + side))
+                Rr = oracle.reconstruct(fr.U, fr.sigma, fr.gate, fr.Vt)
+                worst["recon"] = max(worst["recon"], float(np.linalg.norm(Rg - Rr) / np.linalg.norm(Rr)))
+    assert worst["s"] <= TOL_S_ROUTE, worst
+    assert worst["ulps"] <= 1.0, worst
+    assert worst["sigma"] <= TOL_SIGMA, worst
+    assert worst["recon"] <= TOL_RECON, worst
