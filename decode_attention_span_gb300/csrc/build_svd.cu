@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
   int* pp = reinterpret_cast<int*>(sn + 72);
   int* qq = pp + 72;
   int* ord = qq + 72;          // [NMAX]
-  float* red = reinterpret_cast<float*>(ord + 136);  // [32]
+  float* red = reinterpret_cast<float*>(ord + 136);  // warp values [32], warp indices [32], sign
   __shared__ int s_item;
   const int tid = threadIdx.x;
   const int count = P.counters[cls];
@@ -151,86 +151,119 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
           G[pj[t] * LD + pi[t]] = acc[t];
         }
     }
-    for (int e = tid; e < n * n; e += NT) Q[(e / n) * LD + (e % n)] = (e / n == e % n) ? 1.f : 0.f;
+    // Q = I; an odd n pairs its last index with a dummy index n in every
+    // round of the tournament, whose row and column of G and column of Q are
+    // kept zero (its rotation is the identity)
+    constexpr int NX = NMAX / 2 < 32 ? NMAX / 2 : 32;  // pair (column) lanes
+    constexpr int NY = NT / NX;                        // row lanes
+    constexpr int BPT = (NMAX / 2 + NX - 1) / NX;      // column pairs per thread
+    const int tx = tid % NX, ty = tid / NX;
+    const int nn = (n + 1) & ~1, np = nn / 2;
+    for (int i = ty; i < nn; i += NY)
+      for (int j = tx; j < nn; j += NX) {
+        Q[i * LD + j] = (i == j && i < n) ? 1.f : 0.f;
+        if (i >= n || j >= n) G[i * LD + j] = 0.f;
+      }
     __syncthreads();
 
     // ---- cyclic Jacobi, parallel (tournament) ordering ---------------------
-    const int nn = (n + 1) & ~1;
+    // One round rotates nn/2 disjoint pairs at once: G <- J^T G J and Q <- Q J
+    // with J the product of the round's rotations.  Each 2x2 block of G
+    // (rows of pair a, columns of pair b) is updated in one step,
+    // R_a^T G_ab R_b, so a round needs one barrier after the rotations and one
+    // after the update.
     int sweeps = 0;  // sweeps that rotated (for the operation count)
     for (int sweep = 0; sweep < 24; ++sweep) {
       float off = 0.f, dg = 0.f;
-      for (int e = tid; e < n * n; e += NT) {
-        const int i = e / n, j = e % n;
-        const float v = G[i * LD + j];
-        if (i == j) dg += v * v; else off += v * v;
-      }
+      for (int i = ty; i < n; i += NY)
+        for (int j = tx; j < n; j += NX) {
+          const float v = G[i * LD + j];
+          if (i == j) dg += v * v; else off += v * v;
+        }
       off = block_sum(off, red);
       dg = block_sum(dg, red);
-      // fp32 cannot take the off-diagonal energy much below (n eps)^2 of the
-      // diagonal; stop once it is under 1e-12 of it (inside the build's
-      // accuracy bars: sigma 1e-3 relative, reconstruction 5e-3)
+      // fp32 rotations leave off-diagonal energy near 1e-13 of the diagonal's;
+      // stop once it is under 1e-12 of it (inside the build's accuracy bars:
+      // sigma 1e-3 relative, reconstruction 5e-3)
       if (!(off > 1e-12f * dg)) break;
       ++sweeps;
       for (int rd = 0; rd < nn - 1; ++rd) {
-        __syncthreads();
-        for (int kk = tid; kk < nn / 2; kk += NT) {
+        if (tid < np) {
           int p, q;
-          jacobi_pair(nn, rd, kk, p, q);
+          jacobi_pair(nn, rd, tid, p, q);
           float c = 1.f, s = 0.f;
           if (q < n) {
             const float apq = G[p * LD + q];
             if (apq != 0.f) {
-              const float theta = (G[q * LD + q] - G[p * LD + p]) / (2.f * apq);
+              // tan of the rotation angle, smaller root (Golub & Van Loan);
+              // rsqrt keeps c^2 + s^2 = 1 to a few ulp, which is all the
+              // orthogonality of Q needs
+              const float theta = __fdividef(G[q * LD + q] - G[p * LD + p], 2.f * apq);
               float t;
               if (fabsf(theta) > 1e18f) {
-                t = 0.5f / theta;
+                t = __fdividef(0.5f, theta);
               } else {
-                t = 1.f / (fabsf(theta) + sqrtf(theta * theta + 1.f));
+                const float u = fmaf(theta, theta, 1.f);
+                t = __fdividef(1.f, fabsf(theta) + u * rsqrtf(u));
                 if (theta < 0.f) t = -t;
               }
-              c = 1.f / sqrtf(t * t + 1.f);
+              c = rsqrtf(fmaf(t, t, 1.f));
               s = t * c;
             }
           }
-          cs[kk] = c;
-          sn[kk] = s;
-          pp[kk] = p;
-          qq[kk] = q;
+          cs[tid] = c;
+          sn[tid] = s;
+          pp[tid] = p;
+          qq[tid] = q;
         }
         __syncthreads();
-        // rows: (J^T A)
-        for (int e = tid; e < (nn / 2) * n; e += NT) {
-          const int kk = e / n, j = e % n;
-          const int p = pp[kk], q = qq[kk];
-          if (q >= n) continue;
-          const float c = cs[kk], s = sn[kk];
-          const float gp = G[p * LD + j], gq = G[q * LD + j];
-          G[p * LD + j] = c * gp - s * gq;
-          G[q * LD + j] = s * gp + c * gq;
+        int pb[BPT], qb[BPT];
+        float cb[BPT], sb[BPT];
+#pragma unroll
+        for (int t = 0; t < BPT; ++t) {
+          const int b = tx + t * NX;
+          const bool ok = b < np;
+          pb[t] = ok ? pp[b] : 0;
+          qb[t] = ok ? qq[b] : 0;
+          cb[t] = ok ? cs[b] : 1.f;
+          sb[t] = ok ? sn[b] : 0.f;
+        }
+        for (int a = ty; a < np; a += NY) {
+          const int pa = pp[a], qa = qq[a];
+          const float ca = cs[a], sa = sn[a];
+#pragma unroll
+          for (int t = 0; t < BPT; ++t) {
+            if (tx + t * NX >= np) break;
+            float* gp = G + pa * LD;
+            float* gq = G + qa * LD;
+            const float x = gp[pb[t]], y = gp[qb[t]], z = gq[pb[t]], w = gq[qb[t]];
+            const float x1 = ca * x - sa * z, y1 = ca * y - sa * w;
+            const float z1 = sa * x + ca * z, w1 = sa * y + ca * w;
+            gp[pb[t]] = cb[t] * x1 - sb[t] * y1;
+            gp[qb[t]] = sb[t] * x1 + cb[t] * y1;
+            gq[pb[t]] = cb[t] * z1 - sb[t] * w1;
+            gq[qb[t]] = sb[t] * z1 + cb[t] * w1;
+          }
+        }
+        for (int i = ty; i < n; i += NY) {
+          float* qi = Q + i * LD;
+#pragma unroll
+          for (int t = 0; t < BPT; ++t) {
+            if (tx + t * NX >= np) break;
+            const float vp = qi[pb[t]], vq = qi[qb[t]];
+            qi[pb[t]] = cb[t] * vp - sb[t] * vq;
+            qi[qb[t]] = sb[t] * vp + cb[t] * vq;
+          }
         }
         __syncthreads();
-        // columns: (A J) and the eigenvectors (Q J)
-        for (int e = tid; e < (nn / 2) * n; e += NT) {
-          const int kk = e / n, i = e % n;
-          const int p = pp[kk], q = qq[kk];
-          if (q >= n) continue;
-          const float c = cs[kk], s = sn[kk];
-          const float gp = G[i * LD + p], gq = G[i * LD + q];
-          G[i * LD + p] = c * gp - s * gq;
-          G[i * LD + q] = s * gp + c * gq;
-          const float vp = Q[i * LD + p], vq = Q[i * LD + q];
-          Q[i * LD + p] = c * vp - s * vq;
-          Q[i * LD + q] = s * vp + c * vq;
-        }
       }
-      __syncthreads();
     }
     __syncthreads();
     if (tid == 0 && P.flops != nullptr) {
       // fp32 operations of this body (an fma counts 2): the Gram matrix, every
       // sweep's norms and rotations of G's rows and columns and of the
-      // eigenvectors (3 per updated element), and the projection onto the
-      // other side for the r kept components
+      // eigenvectors (3 per element and rotation), and the projection onto
+      // the other side for the r kept components
       const unsigned long long nq = (unsigned long long)n;
       const unsigned long long gram =
           LARGE ? 128ull * 129ull * (unsigned long long)bl : nq * (nq + 1ull) * 128ull;
@@ -321,14 +354,14 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
         __syncthreads();
         if (lane == 0) {
           red[wid] = best;
-          reinterpret_cast<int*>(red)[16 + wid] = bidx;
+          reinterpret_cast<int*>(red)[32 + wid] = bidx;
         }
         __syncthreads();
         best = red[0];
-        bidx = reinterpret_cast<int*>(red)[16];
+        bidx = reinterpret_cast<int*>(red)[32];
         for (int w = 1; w < NT / 32; ++w) {
           const float ob = red[w];
-          const int oi = reinterpret_cast<int*>(red)[16 + w];
+          const int oi = reinterpret_cast<int*>(red)[32 + w];
           if (ob > best || (ob == best && oi < bidx)) {
             best = ob;
             bidx = oi;
@@ -339,9 +372,9 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       __syncthreads();
 #pragma unroll
       for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t)
-        if (tid + t * NT == bidx) red[8] = v[t];
+        if (tid + t * NT == bidx) red[64] = v[t];
       __syncthreads();
-      const float sgn = red[8] < 0.f ? -1.f : 1.f;
+      const float sgn = red[64] < 0.f ? -1.f : 1.f;
 #pragma unroll
       for (int t = 0; t < (kHeadDim + NT - 1) / NT; ++t) {
         const int d = tid + t * NT;
@@ -398,7 +431,7 @@ cudaError_t launch_svd(const BuildParams& P, int cls, int sms, cudaStream_t stre
 // One persistent launch per size class (the class lists come from plan_kernel).
 cudaError_t launch_svd_all(const BuildParams& P, int sms, cudaStream_t stream) {
   cudaError_t e = launch_svd<32, 64, false>(P, 0, sms, stream);
-  if (e == cudaSuccess) e = launch_svd<64, 128, false>(P, 1, sms, stream);
+  if (e == cudaSuccess) e = launch_svd<64, 256, false>(P, 1, sms, stream);
   if (e == cudaSuccess) e = launch_svd<128, 1024, false>(P, 2, sms, stream);
   if (e == cudaSuccess) e = launch_svd<128, 512, true>(P, 3, sms, stream);
   return e;

@@ -49,6 +49,14 @@ def ulp_bf16(x):
     return 2.0 ** (e - 7)
 
 
+def assert_sign_convention(Vt):
+    """Each stored basis row's largest-magnitude entry is positive (a tie in
+    bf16 between a positive and a negative entry is allowed)."""
+    Vt = np.asarray(Vt, np.float64)
+    if Vt.size:
+        assert np.all(Vt.max(axis=1) >= -Vt.min(axis=1)), "sign convention"
+
+
 def oracle_build(w, inp):
     K, V = inp["K"].float().numpy(), inp["V"].float().numpy()
     return oracle.build_layer(K, V, inp["H"], inp["W_r"].numpy(), inp["gates"],
@@ -81,6 +89,7 @@ def check_build(w, inp, out):
                     if len(sr) == 0:
                         continue
                     worst["sigma"] = max(worst["sigma"], np.max(np.abs(sg - sr) / sr))
+                    assert_sign_convention(getattr(Fg, "Vt" + side))
                     Rg = oracle.reconstruct(getattr(Fg, "U" + side), sg, getattr(Fg, "g" + side),
                                             getattr(Fg, "Vt" + side))
                     Rr = oracle.reconstruct(getattr(Fr, "U" + side), sr, getattr(Fr, "g" + side),
@@ -210,6 +219,7 @@ def test_build_128k_every_head_sampled_spans(sk):
                 if fr.rank == 0:
                     continue
                 worst["sigma"] = max(worst["sigma"], float(np.max(np.abs(sg - fr.sigma) / fr.sigma)))
+                assert_sign_convention(getattr(F, "Vt" + side))
                 Rg = oracle.reconstruct(getattr(F, "U" + side), sg, getattr(F, "g" + side),
                                         getattr(F, "Vt" + side))
                 Rr = oracle.reconstruct(fr.U, fr.sigma, fr.gate, fr.Vt)
