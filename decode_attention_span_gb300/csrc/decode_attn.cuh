@@ -58,7 +58,6 @@ constexpr int kStaticPages = 1;               // full-resolution pages each CTA 
 constexpr int kPoolClaim = 1;                 // pages per claim from the group's pool
 constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
 constexpr int kPrologueItems = 2;             // items per warp issued before the query
-constexpr int kWrSliceBytes = 8 * kHeadDim * 4;  // W_r rows of one warp (4 KB)
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffArena = 0;
@@ -77,7 +76,6 @@ static_assert(kSmemBytes - kOffQfrag >= 16 * 1024 + 1024, "over-read margin");
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 enum ItemType : int {
-  IT_WR = 8,     // rows 8w .. 8w + 7 of W_r for warp w (consumed before routing)
   IT_ROUTE = 1,  // routing summaries of kRouteSpans spans (consumed before the barrier)
   IT_FULL = 2,   // kFullRows full-resolution rows (K and V), the CTA's own or from the pool
   IT_SUM = 3,    // kRows summary rows (K and V) of unexpanded spans

@@ -3,8 +3,9 @@
 //
 // Per warp: an arena of kArenaGran granules used as a ring (items are placed
 // contiguously, wrapping to the arena start when one does not fit at the
-// end), up to kMaxItems items in flight (kSlots before routing: the routing
-// weights and up to two routing pages), each with its own mbarrier.  The
+// end), up to kMaxItems items in flight (before routing: up to two routing
+// pages and the first own pages, kPrologueItems in all), each with its own
+// mbarrier.  The
 // warp issues and consumes its items itself, in order, so no handover
 // between warps is needed; the only CTA-wide synchronisation is the routing
 // barrier (every span of the CTA routed, the record list final) and the
@@ -306,27 +307,15 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
 }
 
 template <int KS>
-__device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const DecodeParams& P) {
+__device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
+                                           const float4 (&wr)[8]) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const Ctx& C = ms->ctx;
   const int G = P.G;
 
-  // ---- prologue: routing weights, routing pages and the first own pages
-  // (no q needed; the caller allows W_r to be read before the wait) --------
-  // rows 8w .. 8w + 7 of W_r (4 KB) land as this warp's first item
-  if (P.fused && lane == 0) {
-    WarpQ& Q = ms->wq[w];
-    const int start = arena_place(Q, kWrSliceBytes);
-    Item it{};
-    it.type = IT_WR;
-    it.boff = kOffArena + w * kArenaBytes + (start % kArenaGran) * kGran;
-    it.end = start + kWrSliceBytes / kGran;
-    arm_item(ms, w, Q.ni % kSlots, it, kWrSliceBytes);
-    bulk_g2s_hint(smem + it.boff, P.W_r + (size_t(C.c) * kRouteDim + 8 * w) * kHeadDim,
-                  kWrSliceBytes, &ms->bar[w][Q.ni % kSlots], policy_evict_last());
-    Q.head = it.end;
-    ++Q.ni;
-  }
+  // ---- prologue: routing pages and the first own pages (no q needed; the
+  // routing weights `wr` were requested at kernel entry) ---------------------
+  const int wr_r = lane >> 2, wr_dq = lane & 3;
   if (lane == 0) {
     for (int p = w; p < C.n_rp; p += kWarps) issue_route_page(smem, ms, P, p);
   }
@@ -374,30 +363,24 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   __syncthreads();
 
   if (P.fused) {
-    // y = W_r q, rows 8w .. 8w + 7 of this warp, from the slice in its arena:
-    // lane (r = lane / 4, dq = lane % 4) sums the head-dim chunks (16 bytes)
-    // c = dq + 4 m, m = 0..7, in the rotated order m = (i + r) mod 8, so that
-    // at each step i the 32 lanes read 32 different chunks (no bank conflicts
-    // on W_r rows 512 bytes apart, nor on q)
+    // y = W_r q, rows 8w .. 8w + 7 of this warp, from the registers: at step
+    // i lane (r, dq) multiplies chunk dq + 4 i of its row with the same chunk
+    // of each head's query, which the 8 lanes of equal dq read together (one
+    // broadcast shared-memory wavefront per read)
     float* ys = reinterpret_cast<float*>(smem + kOffY);
-    const int nd = ms->wq[w].nd;
-    const bool wr_ok =
-        mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1), P.wait_ns);
-    if (!wr_ok && lane == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
-    const Item wit = ms->desc[w][nd % kSlots];
-    const float* wrs = reinterpret_cast<const float*>(smem + wit.boff);
-    const int r = lane >> 2, dq = lane & 3;
     float acc[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) acc[h] = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int c = dq + 4 * ((i + r) & 7);
-      const float4 wv = *reinterpret_cast<const float4*>(wrs + r * kHeadDim + 4 * c);
+      const int c = wr_dq + 4 * i;
+      const float4 wv = wr[i];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 4 * c);
-        acc[h] = fmaf(wv.w, qv.w, fmaf(wv.z, qv.z, fmaf(wv.y, qv.y, fmaf(wv.x, qv.x, acc[h]))));
+        if (h < G) {
+          const float4 qv = *reinterpret_cast<const float4*>(qf + h * kHeadDim + 4 * c);
+          acc[h] = fmaf(wv.w, qv.w, fmaf(wv.z, qv.z, fmaf(wv.y, qv.y, fmaf(wv.x, qv.x, acc[h]))));
+        }
       }
     }
 #pragma unroll
@@ -405,15 +388,9 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
       acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
       acc[h] += __shfl_xor_sync(kFull, acc[h], 2);
     }
-    if (dq == 0) {
+    if (wr_dq == 0) {
 #pragma unroll
-      for (int h = 0; h < 8; ++h) ys[h * kRouteDim + 8 * w + r] = acc[h];
-    }
-    if (wr_ok) {
-      retire_item(ms, nd, wit.end);
-    } else {
-      __syncwarp();
-      if (lane == 0) ms->wq[w].ok = 0;
+      for (int h = 0; h < 8; ++h) ys[h * kRouteDim + 8 * w + wr_r] = acc[h];
     }
     __syncthreads();
 #pragma unroll
@@ -701,6 +678,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   SmemMisc* ms = reinterpret_cast<SmemMisc*>(smem + kOffMisc);
+  // fused mode: lane (r = lane / 4, dq = lane % 4) of warp w keeps the
+  // 16-byte chunks c = dq + 4 i (i = 0..7) of W_r row 8w + r in registers
+  // for the projection y = W_r q.  They are requested first, so their round
+  // trip overlaps the set-up below and the wait for the query (the caller
+  // allows W_r to be read before that wait).
+  float4 wr[8];
+  if (P.fused) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const float4* wrow = reinterpret_cast<const float4*>(
+        P.W_r + (size_t(blockIdx.y) * kRouteDim + 8 * w + (lane >> 2)) * kHeadDim);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wr[i] = ldg_nc_early(wrow + (lane & 3) + 4 * i);
+  }
   if (threadIdx.x < kWarps) {
     WarpQ& Q = ms->wq[threadIdx.x];
     Q = WarpQ{};
@@ -736,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   pdl_launch_dependents();
-  run_decode<KS>(smem, ms, P);
+  run_decode<KS>(smem, ms, P, wr);
 }
 
 }  // namespace sekv
