@@ -29,7 +29,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // Circle-method pairing: round r of a tournament among nn (even) players;
-// pair k in [0, nn/2).
+// pair k in [0, nn/2).  The pair is left unordered (a Jacobi rotation is
+// the same for (p, q) and (q, p)): for k >= 1, p = r + k and q = r - k
+// (mod nn - 1) run through consecutive indices as k does, so the threads of
+// a warp, one pair each, touch 32 different shared-memory banks.
 __device__ __forceinline__ void jacobi_pair(int nn, int r, int k, int& p, int& q) {
   const int m = nn - 1;
   if (k == 0) {
@@ -38,11 +41,6 @@ __device__ __forceinline__ void jacobi_pair(int nn, int r, int k, int& p, int& q
   } else {
     p = (r + k) % m;
     q = (r - k + m) % m;
-  }
-  if (p > q) {
-    const int t = p;
-    p = q;
-    q = t;
   }
 }
 
@@ -102,11 +100,14 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
         if (j < i) continue;
         const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(Ms + i * kHeadDim);
         const __nv_bfloat162* c = reinterpret_cast<const __nv_bfloat162*>(Ms + j * kHeadDim);
+        // the threads of a warp hold different j: starting each row at pair
+        // (d + j) mod 64 spreads their reads of rows j over the banks (rows
+        // 256 bytes apart all start in bank 0)
         float acc = 0.f;
 #pragma unroll 8
         for (int d = 0; d < kHeadDim / 2; ++d) {
-          const float2 x = __bfloat1622float2(a[(d + i) & 63]);
-          const float2 y = __bfloat1622float2(c[(d + i) & 63]);
+          const float2 x = __bfloat1622float2(a[(d + j) & 63]);
+          const float2 y = __bfloat1622float2(c[(d + j) & 63]);
           acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
         }
         G[i * LD + j] = acc;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
           int p, q;
           jacobi_pair(nn, rd, tid, p, q);
           float c = 1.f, s = 0.f;
-          if (q < n) {
+          if (p < n && q < n) {
             const float apq = G[p * LD + q];
             if (apq != 0.f) {
               // tan of the rotation angle, smaller root (Golub & Van Loan);
