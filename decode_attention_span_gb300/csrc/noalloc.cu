@@ -18,22 +18,47 @@ constexpr size_t kNoAllocScratchBytes = SEKV_NOALLOC_SCRATCH_BYTES;
 // only a stand-in; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 std::mutex g_mu;
 void* g_scratch_ptr[64] = {};
+CUcontext g_scratch_ctx[64] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
+// Device address of the scratch array on the current device.  It is looked
+// up with the device current and cached per device together with the
+// context it was found in: after a device reset (a new primary context, the
+// module loaded again) the next call looks it up afresh instead of handing a
+// stale address to the kernel.
 sekv_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SEKV_ERR_CUDA;
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (get_ctx == nullptr) return SEKV_ERR_CUDA;
+  CUcontext ctx = nullptr;  // null until the runtime has made the primary context current
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return SEKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (ctx == nullptr || g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return SEKV_ERR_CUDA;
     }
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SEKV_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return SEKV_OK;
@@ -81,4 +106,12 @@ extern "C" sekv_status sekv_decode_step_noalloc(const sekv_config* cfg,
   P.n_expanded_out = n_expanded;
   P.scale_log2 = scale * kLog2e;
   return launch_decode(P, L, cfg, stream, false);
+}
+
+extern "C" sekv_status sekv_noalloc_status(cudaStream_t stream, int32_t* code, int32_t* detail) {
+  void* scratch = nullptr;
+  sekv_status st = scratch_address(&scratch);
+  if (st != SEKV_OK) return st;
+  // the status word is the first 8 bytes of the array (as of a workspace)
+  return sekv_workspace_status(scratch, stream, code, detail);
 }

@@ -30,7 +30,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 # every symbol include/sekv.h declares
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
-           "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_build_spans",
+           "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_noalloc_status",
+           "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
            "sekv_fetch_bases_cached", "sekv_build_flops",
            "sekv_status_string", "sekv_last_launch_count")
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
         L.sekv_decode_step_noalloc.argtypes = [ctypes.POINTER(SekvConfig),
                                                ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp,
                                                _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]
+        L.sekv_noalloc_status.restype = _c_i32
+        L.sekv_noalloc_status.argtypes = [_c_vp, ctypes.POINTER(_c_i32), ctypes.POINTER(_c_i32)]
         L.sekv_build_spans.restype = _c_i32
         L.sekv_build_spans.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_sz,
@@ -340,6 +343,14 @@ def decode_step_noalloc(cfg: Config, cache: LayerCache, q, W_r, theta, scale: fl
                                           _ptr(lse), _ptr(expanded), _ptr(n_expanded),
                                           _stream(stream)))
     return out, lse, expanded, n_expanded
+
+
+def noalloc_status(stream=None):
+    """(code, detail) of the no-alloc scratch array's status word on the
+    current device (sekv_noalloc_status): synchronises, reads and clears it."""
+    code, detail = _c_i32(0), _c_i32(0)
+    lib().sekv_noalloc_status(_stream(stream), ctypes.byref(code), ctypes.byref(detail))
+    return code.value, detail.value
 
 
 def fetch_bases(cfg: Config, cache: LayerCache, expanded, n_expanded, staging, per_group: int,

@@ -357,14 +357,17 @@ sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cac
  *     (e.g. batch 1 x 8 KV heads x 4 160 spans needs about 2 MiB); larger
  *     shapes return SEKV_ERR_CAPACITY before anything is launched.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
+ *     per device and context, with that device current); make that first
+ *     call before any stream capture.  After a device reset (cudaDeviceReset)
+ *     the next call looks the address up again, so it too must come before
+ *     any capture.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents; every call clears the counters it needs.  Calls that
  *     overlap on the GPU (other streams, other threads) race on it and give
  *     wrong results: serialise them.
- *   - Errors the GPU detects are not reported by this call (the status word
- *     lives in the shared array); diagnose with sekv_decode_step.
+ *   - Errors the GPU detects are not reported by this call; the status word
+ *     lives in the shared array, and sekv_noalloc_status reads it (after the
+ *     call's work has finished, before the next call clears it).
  * Arguments, layouts and results are those of sekv_decode_step; flags in
  * cfg are ignored (no overlap with the preceding kernel).
  */
@@ -373,6 +376,14 @@ sekv_status sekv_decode_step_noalloc(const sekv_config* cfg, const sekv_layer_ca
                                      const void* q, const float* W_r, const float* theta,
                                      float scale, float* out, float* lse, int32_t* expanded,
                                      int32_t* n_expanded, cudaStream_t stream);
+
+/* The status word of the no-alloc scratch array on the current device (no
+ * counterpart on the pages either): synchronises `stream`, then reads and
+ * clears it like sekv_workspace_status -- *code 0 and SEKV_OK when the GPU
+ * found nothing, else the device error code and its detail, and
+ * SEKV_ERR_TIMEOUT or SEKV_ERR_DEVICE.  Read it after a
+ * sekv_decode_step_noalloc call on that stream and before the next one. */
+sekv_status sekv_noalloc_status(cudaStream_t stream, int32_t* code, int32_t* detail);
 
 /* Outputs of sekv_build_spans: one layer of the cache (layouts as in
  * sekv_layer_cache; every array with its full capacity) plus the device

@@ -57,6 +57,7 @@ def test_noalloc_matches_decode_step_twice(sk, name, over):
         out, lse, lst, cnt = sk.decode_step_noalloc(cfg, cache, q, W, theta, SCALE,
                                                     want_list=True)
         torch.cuda.synchronize()
+        assert sk.sekv.noalloc_status() == (0, 0)
         _close(out, ref, f"{name} call {call}")
         assert torch.allclose(lse, ref_lse, atol=1e-3)
         assert torch.equal(cnt, ref_cnt)
