@@ -30,6 +30,7 @@ from .sekv_oracle import (  # noqa: F401
     routing_summary,
     attention_summary,
     span_svd,
+    build_span,
     build_layer,
     route,
     route_logits,

@@ -244,6 +244,25 @@ class LayerCache:
         return int(len(self.body_len[b]))
 
 
+def build_span(Kb, Vb, Hb, W_r_c, gates_k, gates_v, rank_cap: int):
+    """Stored representations of one span with a non-empty body: (routing
+    summary, summary key, summary value, SpanFactors), each rounded to its
+    storage format.
+
+    [DE] Methodik 2 / [ZH] 方法论 2: the GPU copy (routing summary) and the CPU
+    copy (gated SVD basis) of the span, plus the summary key/value that an
+    unexpanded span contributes to attention ([DE] Methodik 3).
+    """
+    s_row = f32_round(routing_summary(Kb, Hb, W_r_c))
+    km, vm = attention_summary(Kb, Vb)
+    fk = span_svd(Kb, gates_k, rank_cap)
+    fv = span_svd(Vb, gates_v, rank_cap)
+    F = SpanFactors(UK=bf16_round(fk.U), sK=f32_round(fk.sigma), gK=f32_round(fk.gate),
+                    VtK=bf16_round(fk.Vt), UV=bf16_round(fv.U), sV=f32_round(fv.sigma),
+                    gV=f32_round(fv.gate), VtV=bf16_round(fv.Vt))
+    return s_row, bf16_round(km), bf16_round(vm), F
+
+
 def build_layer(K, V, H, W_r, gates, *, n_sink: int, n_recent: int, tau: float,
                 len_min: int, len_max: int, rank_cap: int) -> LayerCache:
     """Prefill cache build of one layer: segmentation, summaries, SVD bases.
@@ -280,18 +299,10 @@ def build_layer(K, V, H, W_r, gates, *, n_sink: int, n_recent: int, tau: float,
                 if hi <= lo:
                     f_row.append(None)
                     continue
-                Kb, Vb = K[b, c, lo:hi], V[b, c, lo:hi]
-                s_rows[k] = f32_round(routing_summary(Kb, H[b][lo:hi], W_r[c]))
-                km, vm = attention_summary(Kb, Vb)
-                k_rows[k] = bf16_round(km)
-                v_rows[k] = bf16_round(vm)
-                fk = span_svd(Kb, gates[b][c][0][k], rank_cap)
-                fv = span_svd(Vb, gates[b][c][1][k], rank_cap)
-                f_row.append(SpanFactors(
-                    UK=bf16_round(fk.U), sK=f32_round(fk.sigma),
-                    gK=f32_round(fk.gate), VtK=bf16_round(fk.Vt),
-                    UV=bf16_round(fv.U), sV=f32_round(fv.sigma),
-                    gV=f32_round(fv.gate), VtV=bf16_round(fv.Vt)))
+                s_rows[k], k_rows[k], v_rows[k], F = build_span(
+                    K[b, c, lo:hi], V[b, c, lo:hi], H[b][lo:hi], W_r[c],
+                    gates[b][c][0][k], gates[b][c][1][k], rank_cap)
+                f_row.append(F)
             sr.append(s_rows)
             ks.append(k_rows)
             vs.append(v_rows)
