@@ -20,6 +20,7 @@ from .sekv import (  # noqa: F401
     BasisCache,
     build_spans,
     build_flops,
+    Maintainer,
     alloc_cache,
     record_size,
     last_launch_count,

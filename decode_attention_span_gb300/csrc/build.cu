@@ -182,10 +182,11 @@ __global__ void __launch_bounds__(256) summary_kernel(const BuildParams P) {
   __shared__ float kh[8][kHeadDim];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = g / P.Hkv, c = g % P.Hkv;
-  const int k = blockIdx.x * 8 + wid;
+  // decode-time maintenance: warp 0 of each group's CTA, span only_k[b]
+  const int k = P.only_k != nullptr ? (wid == 0 ? P.only_k[b] : -1) : blockIdx.x * 8 + wid;
   const size_t gs = size_t(g) * P.max_spans;
-  const int n_sp = P.n_spans[b];
-  if (k >= P.max_spans) return;
+  if (k < 0 || k >= P.max_spans) return;
+  const int n_sp = P.only_k != nullptr ? k + 1 : P.n_spans[b];
   const int bl = k < n_sp ? P.body_len[size_t(b) * P.max_spans + k] : 0;
   float4 ks = make_float4(0.f, 0.f, 0.f, 0.f), vs = ks, hs = ks;
   if (bl > 0) {

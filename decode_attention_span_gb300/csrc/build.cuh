@@ -43,9 +43,58 @@ struct BuildParams {
   int32_t* counters;       // [0..3] class counts, [4..7] class cursors, [8] plan CTAs done
   int32_t* cls_list;       // [4][B*Hkv*max_spans*2]
   int64_t cls_cap;
+  // decode-time maintenance: summaries of span only_k[b] of each sequence
+  // (-1: none) instead of every span; null in the prefill build
+  const int32_t* only_k;
   int B, Hkv, T, n_sink, n_recent, max_spans, rank_cap, len_min, len_max;
   float tau;
 };
+
+// Decode-time maintenance of one layer's cache (sekv_append_token): the new
+// token joins the tail of the full-resolution rows; the token leaving the
+// recent window continues the segmentation walk; a span it closes is built by
+// the build's summary and SVD kernels (run in place on the full rows: K = the
+// full rows of each group, T = their capacity, H = the tail surprisal by row).
+struct MaintParams {
+  const __nv_bfloat16* k_new;  // [B][Hkv][128]
+  const __nv_bfloat16* v_new;
+  const float* h_new;          // [B]
+  const float* gates;          // [B][Hkv][2][max_spans][rank_cap]
+  int32_t* n_spans;
+  int32_t* n_tail;
+  int32_t* body_len;
+  __nv_bfloat16* k_full;
+  __nv_bfloat16* v_full;
+  float* s_route;
+  __nv_bfloat16* k_sum;
+  __nv_bfloat16* v_sum;
+  int64_t* rec_off;
+  int32_t* rec_rank;
+  int64_t store_capacity;
+  // maintenance state (caller-owned, kept across calls)
+  int32_t* s_open;                 // [B] the open span's anchor position, -1: none
+  unsigned long long* store_used;  // bytes of the store in use (records go after)
+  int32_t* pend;                   // [B][8] this call's decision, for the commit
+  int32_t* only_k;                 // [B] the span this call closes, -1: none
+  float* tail_h;                   // [B][cap] surprisal of the token in each full row
+  // build workspace
+  int32_t* status;
+  int32_t* starts;
+  int64_t* rel_off;
+  int64_t* gbase;
+  int32_t* counters;
+  int32_t* cls_list;
+  int64_t cls_cap;
+  int B, Hkv, T, cap, n_sink, n_recent, max_spans, rank_cap, len_min, len_max;
+  float tau;
+};
+
+__global__ void maint_init_rows_kernel(const MaintParams M, const __nv_bfloat16* K,
+                                       const __nv_bfloat16* V, const float* H);
+__global__ void maint_init_commit_kernel(const MaintParams M);
+__global__ void maint_used_kernel(const MaintParams M);
+__global__ void maint_plan_kernel(const MaintParams M);
+__global__ void maint_commit_kernel(const MaintParams M);
 
 __global__ void seg_kernel(const BuildParams P);
 __global__ void plan_kernel(const BuildParams P);

@@ -104,6 +104,7 @@ struct RecEntry {  // one expanded span of the CTA, 16 bytes
 struct DecodeParams {
   CUtensorMap tm_kfull, tm_vfull, tm_ksum, tm_vsum, tm_sroute;
   const int32_t* n_spans;
+  const int32_t* n_tail;   // [B] full-resolution rows after the anchors, or null: n_recent
   const int32_t* body_len;
   const int64_t* rec_off;
   const int32_t* rec_rank;

@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     C.gs = (long long)C.g * P.max_spans;
     C.bs = (long long)C.b * P.max_spans;
     C.n_sp = P.n_spans[C.b];
-    C.n_full = P.n_sink + C.n_sp + P.n_recent;
+    C.n_full = P.n_sink + C.n_sp + (P.n_tail != nullptr ? P.n_tail[C.b] : P.n_recent);
     span_range(C.j, P.cg, C.n_sp, C.k0, C.k1);
     C.n_fp = (C.n_full + kFullRows - 1) / kFullRows;
     C.own0 = kStaticPages * C.j;

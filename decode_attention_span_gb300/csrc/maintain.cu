@@ -1,0 +1,282 @@
+// Decode-time maintenance of one layer's span cache (sekv_maint_init,
+// sekv_append_token).
+//
+// SeKV, technical summary (gist.science, German page / Chinese page), and the
+// lay explainer of the same pages: the GPU keeps the very last part of the
+// text at full resolution (explainer, part 2 / 两层记忆); high-surprisal
+// tokens are span boundaries and a span is the run of tokens between two
+// neighbouring anchors (Methodik 1 / 方法论 1); each span is kept as a routing
+// summary and a gated SVD basis (Methodik 2 / 方法论 2).  During decode the
+// new token joins the recent window, the token leaving the window continues
+// the segmentation walk, and a span is built once the next anchor closes it;
+// until then the open span -- anchor and body -- stays at full resolution in
+// the tail of the full rows, in front of the recent window.
+//
+// Row layout of one group (sequence b, KV head c), capacity `cap` rows:
+//   [0, n_sink)                 sinks
+//   [n_sink, n_sink + n_spans)  anchors of the closed spans
+//   [n_sink + n_spans, + n_tail) the tail: the open span's anchor and body,
+//                               then the recent window (oldest first)
+// A span closing at ordinal k = n_spans keeps its anchor at row n_sink + k;
+// its body rows leave the tail, which moves up over them.
+#include "build.cuh"
+
+namespace sekv {
+
+namespace {
+
+constexpr int kRowChunks = kHeadDim * 2 / 16;  // 16-byte chunks per row
+
+__device__ __forceinline__ int gate_rank_m(const float* g, int R) {
+  int r = 0;
+  while (r < R && g[r] > 0.5f) ++r;
+  return r;
+}
+
+// Move rows [from, from + n) of one group's K and V rows to [to, to + n),
+// to < from (overlap allowed): chunks of rows in increasing order, each read
+// whole into registers before any of it is written, so a chunk never
+// overwrites rows a later chunk still has to read.
+__device__ void move_rows_down(__nv_bfloat16* Kg, __nv_bfloat16* Vg, int from, int to, int n) {
+  constexpr int kPer = 4;  // 16-byte chunks per thread and array per step
+  const int step = blockDim.x * kPer;  // chunks per step
+  int4* K4 = reinterpret_cast<int4*>(Kg);
+  int4* V4 = reinterpret_cast<int4*>(Vg);
+  const int total = n * kRowChunks;
+  for (int c0 = 0; c0 < total; c0 += step) {
+    int4 kv[kPer], vv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = c0 + threadIdx.x + i * blockDim.x;
+      if (e < total) {
+        kv[i] = K4[size_t(from) * kRowChunks + e];
+        vv[i] = V4[size_t(from) * kRowChunks + e];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = c0 + threadIdx.x + i * blockDim.x;
+      if (e < total) {
+        K4[size_t(to) * kRowChunks + e] = kv[i];
+        V4[size_t(to) * kRowChunks + e] = vv[i];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// init, from a prefill build of a prefix of length T: the build closed its
+// last span at the end of the middle region; that span is open again (its
+// anchor and body return to full resolution from K, V).  grid (Hkv, B).
+// pend[b] = {n_spans after, n_tail, s_open}.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) maint_init_rows_kernel(const MaintParams M,
+                                                              const __nv_bfloat16* K,
+                                                              const __nv_bfloat16* V,
+                                                              const float* H) {
+  __shared__ int red[8];
+  const int c = blockIdx.x, b = blockIdx.y, g = b * M.Hkv + c, tid = threadIdx.x;
+  const int n_sp = M.n_spans[b];
+  int s = -1;  // the open anchor
+  if (n_sp > 0) {
+    int acc = 0;
+    for (int k = tid; k < n_sp - 1; k += blockDim.x) acc += M.body_len[size_t(b) * M.max_spans + k] + 1;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    __syncthreads();
+    acc = 0;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) acc += red[w];
+    s = M.n_sink + acc;
+  }
+  const int n_closed = n_sp > 0 ? n_sp - 1 : 0;
+  const int start = M.n_sink + n_closed;
+  const int src0 = s >= 0 ? s : M.T - M.n_recent;  // first token of the tail
+  const int n_tail = M.T - src0;
+  if (start + n_tail > M.cap) {
+    if (tid == 0) set_device_error(M.status, DEV_STAGING_FULL, b);
+    return;
+  }
+  const int4* Ks = reinterpret_cast<const int4*>(K + (size_t(g) * M.T + src0) * kHeadDim);
+  const int4* Vs = reinterpret_cast<const int4*>(V + (size_t(g) * M.T + src0) * kHeadDim);
+  int4* Kd = reinterpret_cast<int4*>(M.k_full + (size_t(g) * M.cap + start) * kHeadDim);
+  int4* Vd = reinterpret_cast<int4*>(M.v_full + (size_t(g) * M.cap + start) * kHeadDim);
+  for (int e = tid; e < n_tail * kRowChunks; e += blockDim.x) {
+    Kd[e] = Ks[e];
+    Vd[e] = Vs[e];
+  }
+  if (c == 0) {
+    for (int i = tid; i < n_tail; i += blockDim.x)
+      M.tail_h[size_t(b) * M.cap + start + i] = H[size_t(b) * M.T + src0 + i];
+    if (tid == 0) {
+      int32_t* pd = M.pend + size_t(b) * 8;
+      pd[0] = n_closed;
+      pd[1] = n_tail;
+      pd[2] = s;
+    }
+  }
+}
+
+// grid (B): the per-sequence counters, once every group's rows are in place.
+__global__ void maint_init_commit_kernel(const MaintParams M) {
+  const int b = blockIdx.x;
+  if (threadIdx.x != 0) return;
+  const int32_t* pd = M.pend + size_t(b) * 8;
+  M.n_spans[b] = pd[0];
+  M.n_tail[b] = pd[1];
+  M.s_open[b] = pd[2];
+}
+
+// grid (B*Hkv): the end of the records in the store (their maximum end).
+__global__ void __launch_bounds__(256) maint_used_kernel(const MaintParams M) {
+  const int g = blockIdx.x, b = g / M.Hkv;
+  const int n_sp = M.n_spans[b];
+  unsigned long long mx = 0;
+  for (int k = threadIdx.x; k < n_sp; k += blockDim.x) {
+    const size_t gk = size_t(g) * M.max_spans + k;
+    const int bl = M.body_len[size_t(b) * M.max_spans + k];
+    const int rk = M.rec_rank[gk] & 0xffff, rv = (M.rec_rank[gk] >> 16) & 0xffff;
+    if (bl > 0) {
+      const unsigned long long e = (unsigned long long)M.rec_off[gk] + record_bytes(bl, rk, rv);
+      mx = e > mx ? e : mx;
+    }
+  }
+  if (mx) atomicMax(M.store_used, mx);
+}
+
+// ---------------------------------------------------------------------------
+// one append, step 1 (grid (Hkv, B)): the new token's row at the end of the
+// tail; the segmentation decision for the token leaving the recent window
+// (t = T - n_recent); for a span this closes (ordinal k = n_spans): its ranks
+// from the gates, its record's place at the end of the store, its SVD work
+// items, and the empty-body case written out.  pend[b] = {closes, k, body,
+// n_tail after, s_open after}.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) maint_plan_kernel(const MaintParams M) {
+  const int c = blockIdx.x, b = blockIdx.y, g = b * M.Hkv + c, tid = threadIdx.x;
+  const int n_sp = M.n_spans[b], n_tail = M.n_tail[b], s = M.s_open[b];
+  const int row0 = M.n_sink + n_sp;  // the tail's first row
+  const int r_new = row0 + n_tail;
+  if (r_new >= M.cap || n_sp >= M.max_spans) {
+    if (tid == 0) set_device_error(M.status, DEV_STAGING_FULL, b);
+    if (c == 0 && tid == 0) {
+      int32_t* pd = M.pend + size_t(b) * 8;
+      pd[0] = -1;  // nothing to commit
+      M.only_k[b] = -1;
+    }
+    return;
+  }
+  // the new token's key and value
+  if (tid < 2 * 16) {
+    const int4* src = reinterpret_cast<const int4*>((tid < 16 ? M.k_new : M.v_new) +
+                                                    size_t(g) * kHeadDim);
+    int4* dst = reinterpret_cast<int4*>((tid < 16 ? M.k_full : M.v_full) +
+                                        (size_t(g) * M.cap + r_new) * kHeadDim);
+    dst[tid & 15] = src[tid & 15];
+  }
+  const int t = M.T - M.n_recent;
+  int closes = 0, s_new = s, n = 0;
+  if (t >= M.n_sink) {
+    if (s < 0) {
+      s_new = t;  // the first middle token opens span 0
+    } else {
+      n = t - s;
+      const float h = M.tail_h[size_t(b) * M.cap + row0 + n];
+      if ((h > M.tau && n >= M.len_min) || n == M.len_max) {
+        closes = 1;
+        s_new = t;
+      }
+    }
+  }
+  const int k = n_sp, bl = n - 1;
+  if (closes && tid == 0) {
+    const size_t gk = size_t(g) * M.max_spans + k;
+    int rk = 0, rv = 0;
+    if (bl > 0) {
+      const int R = bl < M.rank_cap ? bl : M.rank_cap;
+      const float* gkp = M.gates + ((size_t(b) * M.Hkv + c) * 2 * M.max_spans + k) * M.rank_cap;
+      rk = gate_rank_m(gkp, R);
+      rv = gate_rank_m(gkp + size_t(M.max_spans) * M.rank_cap, R);
+      const long long size = record_bytes(bl, rk, rv);
+      const unsigned long long off = atomicAdd(M.store_used, (unsigned long long)size);
+      if ((long long)off + size > M.store_capacity)
+        set_device_error(M.status, DEV_STAGING_FULL, int((off + size) >> 20));
+      M.rel_off[gk] = (long long)off;
+      const int cls = bl <= 32 ? 0 : bl <= 64 ? 1 : bl <= 128 ? 2 : 3;
+      const int pos = atomicAdd(&M.counters[cls], 2);
+      if (pos + 1 < M.cls_cap) {
+        int32_t* lst = M.cls_list + size_t(cls) * M.cls_cap;
+        lst[pos] = int32_t(gk * 2);
+        lst[pos + 1] = int32_t(gk * 2 + 1);
+      }
+    }
+    M.rec_rank[gk] = rk | (rv << 16);
+    M.gbase[g] = 0;
+    if (c == 0) {
+      M.starts[size_t(b) * M.max_spans + k] = row0;  // the anchor's row
+      M.body_len[size_t(b) * M.max_spans + k] = bl;
+    }
+  }
+  if (c == 0 && tid == 0) {
+    M.tail_h[size_t(b) * M.cap + r_new] = M.h_new[b];
+    int32_t* pd = M.pend + size_t(b) * 8;
+    pd[0] = closes;
+    pd[1] = k;
+    pd[2] = bl;
+    pd[3] = closes ? n_tail + 1 - n : n_tail + 1;
+    pd[4] = s_new;
+    M.only_k[b] = closes ? k : -1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// one append, last step (grid (Hkv, B)), after the closed span's summaries and
+// basis are built: its body rows leave the tail (the rows after them move up),
+// then the per-sequence counters.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) maint_commit_kernel(const MaintParams M) {
+  const int c = blockIdx.x, b = blockIdx.y, g = b * M.Hkv + c;
+  const int32_t* pd = M.pend + size_t(b) * 8;
+  const int closes = pd[0];
+  if (closes < 0) return;
+  const int k = pd[1], bl = pd[2], n_tail_new = pd[3], s_new = pd[4];
+  if (closes) {
+    // the tail after the anchor: tokens t .. T (n_tail_new rows), behind the
+    // bl body rows that leave it
+    const int anchor = M.n_sink + k;
+    const int from = anchor + 1 + bl, to = anchor + 1, cnt = n_tail_new;
+    if (bl > 0 && cnt > 0) {
+      move_rows_down(M.k_full + size_t(g) * M.cap * kHeadDim,
+                     M.v_full + size_t(g) * M.cap * kHeadDim, from, to, cnt);
+      if (c == 0) {
+        float* th = M.tail_h + size_t(b) * M.cap;
+        float v[4];
+        for (int i0 = 0; i0 < cnt; i0 += 4 * blockDim.x) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = i0 + threadIdx.x + j * blockDim.x;
+            v[j] = i < cnt ? th[from + i] : 0.f;
+          }
+          __syncthreads();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = i0 + threadIdx.x + j * blockDim.x;
+            if (i < cnt) th[to + i] = v[j];
+          }
+          __syncthreads();
+        }
+      }
+    }
+  }
+  if (c == 0 && threadIdx.x == 0) {
+    if (closes) M.n_spans[b] = k + 1;
+    M.n_tail[b] = n_tail_new;
+    M.s_open[b] = s_new;
+  }
+}
+
+}  // namespace sekv

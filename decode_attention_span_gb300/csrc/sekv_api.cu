@@ -246,6 +246,7 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   if (!ok) return SEKV_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(ws);
   P.n_spans = cache->n_spans;
+  P.n_tail = cache->n_tail;
   P.body_len = cache->body_len;
   P.rec_off = cache->rec_off;
   P.rec_rank = cache->rec_rank;

@@ -33,7 +33,8 @@ EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_noalloc_status",
            "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
-           "sekv_fetch_bases_cached", "sekv_build_flops",
+           "sekv_fetch_bases_cached", "sekv_build_flops", "sekv_maint_state_size",
+           "sekv_maint_init", "sekv_append_token",
            "sekv_status_string", "sekv_last_launch_count")
 
 
@@ -59,7 +60,8 @@ class SekvCacheOut(ctypes.Structure):
 class SekvLayerCache(ctypes.Structure):
     _fields_ = [("n_spans", _c_vp), ("body_len", _c_vp), ("k_full", _c_vp), ("v_full", _c_vp),
                 ("s_route", _c_vp), ("k_sum", _c_vp), ("v_sum", _c_vp), ("rec_off", _c_vp),
-                ("rec_rank", _c_vp), ("store", _c_vp), ("store_on_host", _c_i32)]
+                ("rec_rank", _c_vp), ("store", _c_vp), ("store_on_host", _c_i32),
+                ("n_tail", _c_vp)]
 
 
 _LIB = None
@@ -95,6 +97,16 @@ def lib() -> ctypes.CDLL:
                                        _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]
         L.sekv_build_flops.restype = _c_i32
         L.sekv_build_flops.argtypes = [_c_vp, _c_vp, ctypes.POINTER(_c_i64)]
+        L.sekv_maint_state_size.restype = _c_sz
+        L.sekv_maint_state_size.argtypes = [ctypes.POINTER(SekvConfig)]
+        L.sekv_maint_init.restype = _c_i32
+        L.sekv_maint_init.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
+                                      ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp, _c_sz, _c_vp,
+                                      _c_sz, _c_vp]
+        L.sekv_append_token.restype = _c_i32
+        L.sekv_append_token.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
+                                        _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp,
+                                        _c_sz, _c_vp, _c_sz, _c_vp]
         L.sekv_basis_cache_bytes.restype = _c_sz
         L.sekv_basis_cache_bytes.argtypes = [ctypes.POINTER(SekvConfig), _c_i32]
         L.sekv_basis_cache_init.restype = _c_i32
@@ -206,7 +218,12 @@ class LayerCache:
         _need(st, "store", torch.uint8, cuda=not store_on_host)
         if store_on_host and not st.is_pinned():
             raise ValueError("store: host tier must be pinned memory")
-        self._c = SekvLayerCache(*[_ptr(self.t[k]) for k in CACHE_FIELDS], int(store_on_host))
+        n_tail = tensors.get("n_tail")
+        if n_tail is not None:
+            _need(n_tail, "n_tail", torch.int32)
+            self.t["n_tail"] = n_tail
+        self._c = SekvLayerCache(*[_ptr(self.t[k]) for k in CACHE_FIELDS], int(store_on_host),
+                                 _ptr(n_tail))
 
     @property
     def c(self) -> SekvLayerCache:
@@ -462,6 +479,44 @@ def build_flops(ws: Workspace, stream=None) -> int:
     v = _c_i64(0)
     _check("sekv_build_flops", lib().sekv_build_flops(ws.ptr(), _stream(stream), ctypes.byref(v)))
     return v.value
+
+
+class Maintainer:
+    """Decode-time maintenance of one layer's cache (sekv_maint_init,
+    sekv_append_token): `out` is the dict of sekv_build_spans' output tensors;
+    this object adds the per-sequence tail lengths (``n_tail``) and the state
+    buffer, and keeps the sequence length.  ``layer_cache()`` gives the
+    LayerCache (with n_tail) that the decode calls read."""
+
+    def __init__(self, cfg: Config, out: Dict[str, torch.Tensor], K, V, H, ctx_len: int,
+                 ws: Workspace, stream=None):
+        self.cfg, self.out, self.ws, self.T = cfg, out, ws, int(ctx_len)
+        dev = out["k_full"].device
+        c = cfg.c()
+        n = int(lib().sekv_maint_state_size(ctypes.byref(c)))
+        self.state = torch.zeros(n, dtype=torch.uint8, device=dev)
+        self.n_tail = torch.zeros(cfg.batch, dtype=torch.int32, device=dev)
+        self._o = SekvCacheOut(*[_ptr(out[k]) for k in CACHE_FIELDS], out["store"].numel())
+        _need(K, "K", torch.bfloat16); _need(V, "V", torch.bfloat16); _need(H, "H", torch.float32)
+        _check("sekv_maint_init",
+               lib().sekv_maint_init(ctypes.byref(c), self.T, _ptr(K), _ptr(V), _ptr(H),
+                                     ctypes.byref(self._o), _ptr(self.n_tail), _ptr(self.state),
+                                     self.state.numel(), ws.ptr(), ws.nbytes, _stream(stream)))
+
+    def append(self, k_new, v_new, h_new, W_r, gates, stream=None):
+        _need(k_new, "k_new", torch.bfloat16); _need(v_new, "v_new", torch.bfloat16)
+        _need(h_new, "h_new", torch.float32); _need(W_r, "W_r", torch.float32)
+        _need(gates, "gates", torch.float32)
+        c = self.cfg.c()
+        _check("sekv_append_token",
+               lib().sekv_append_token(ctypes.byref(c), self.T, _ptr(k_new), _ptr(v_new),
+                                       _ptr(h_new), _ptr(W_r), _ptr(gates), ctypes.byref(self._o),
+                                       _ptr(self.n_tail), _ptr(self.state), self.state.numel(),
+                                       self.ws.ptr(), self.ws.nbytes, _stream(stream)))
+        self.T += 1
+
+    def layer_cache(self) -> LayerCache:
+        return LayerCache({**{k: self.out[k] for k in CACHE_FIELDS}, "n_tail": self.n_tail})
 
 
 def default_scale() -> float:

@@ -147,6 +147,13 @@ typedef struct sekv_layer_cache {
   const int32_t* rec_rank;
   const void* store;
   int32_t store_on_host;
+  /* Optional (NULL: n_recent for every sequence).  int32 [B]: the number of
+   * full-resolution rows after the anchors of sequence b.  A cache kept up to
+   * date during decode (sekv_append_token) holds the open span -- its anchor
+   * and body, not yet closed by a next anchor -- at full resolution in front
+   * of the recent window, so its tail is n_recent plus the open span's
+   * length; all rows still fit the n_full_cap rows of each group. */
+  const int32_t* n_tail;
 } sekv_layer_cache;
 
 /* Which call a workspace is sized for. */
@@ -435,6 +442,54 @@ sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len, const void
  * last read -- Gram matrices, the Jacobi sweeps actually run, projections --
  * then clear the count.  For reporting the build's arithmetic rate. */
 sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, int64_t* flops);
+
+/*
+ * Decode-time maintenance of one layer's cache.  The pages describe the cache
+ * built at prefill and the zoom-in during decode, not how the cache follows
+ * the tokens that decoding appends; these calls take this reading of them:
+ * the GPU keeps the very last part of the text at full resolution ([DE]
+ * explainer part 2 / [ZH] 两层记忆), so each new token joins the recent
+ * window; the token leaving the window continues the segmentation walk of
+ * Methodik 1 (it opens a span iff (H_t > tau and the open span's length >=
+ * len_min) or that length == len_max); a span is the run of tokens between
+ * two neighbouring anchors, so it is built (routing summary, summary
+ * key/value, gated SVD basis: Methodik 2) once the next anchor closes it.
+ * Until then the open span -- anchor and body -- stays at full resolution at
+ * the head of the tail (sekv_layer_cache.n_tail).  After every append the
+ * cache equals the prefill build of the same prefix whose recent window is
+ * taken to start at the open span's anchor.
+ *
+ * The maintained cache is a sekv_cache_out of the prefill build plus
+ * n_tail (int32 [B], caller-owned) and a state buffer of
+ * sekv_maint_state_size bytes (caller-owned, kept between calls; it holds the
+ * open anchors, the surprisal of the tail tokens and the end of the records in
+ * `store`).  Records of closing spans are appended after the last record in
+ * `store`.  The workspace is a build workspace (SEKV_CALL_BUILD); device
+ * errors go to its status word (code 3: no room left -- rows, spans or store
+ * -- with the sequence or the MiB needed as detail).  All sequences of the
+ * batch have the same length ctx_len (the length before the call).
+ */
+size_t sekv_maint_state_size(const sekv_config* cfg);
+
+/* Starts maintenance of a cache that sekv_build_spans built from K, V, H of
+ * length ctx_len (same arguments): the build's last span, which the end of
+ * the middle region closed, is open again -- its anchor and body return to
+ * full resolution from K and V, and n_tail and the state are set. */
+sekv_status sekv_maint_init(const sekv_config* cfg, int64_t ctx_len, const void* K,
+                            const void* V, const float* H, const sekv_cache_out* out,
+                            int32_t* n_tail, void* state, size_t state_bytes, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/* Appends one token to every sequence (ctx_len -> ctx_len + 1): k_new, v_new
+ * bf16 [B][Hkv][128] (16-byte aligned), h_new f32 [B] its surprisal; W_r and
+ * gates as sekv_build_spans (gates indexed by span ordinal).  The cache (out,
+ * n_tail) is updated in place on `stream`; read it with a sekv_layer_cache
+ * that carries n_tail. */
+sekv_status sekv_append_token(const sekv_config* cfg, int64_t ctx_len, const void* k_new,
+                              const void* v_new, const float* h_new, const float* W_r,
+                              const float* gates, const sekv_cache_out* out, int32_t* n_tail,
+                              void* state, size_t state_bytes, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Human-readable name of a status. */
 const char* sekv_status_string(sekv_status status);

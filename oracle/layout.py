@@ -170,8 +170,10 @@ def unpack_layer(arrs: Dict[str, np.ndarray], n_sink: int, n_recent: int,
     """Logical cache from ABI arrays.  ``groups``: optional set of (b, c) to
     decode fully; the others get empty per-head lists (for sampled checks).
     ``records=False`` leaves every span's factors as None (routing needs no
-    basis records; it saves unpacking them)."""
+    basis records; it saves unpacking them).  An ``n_tail`` array in
+    ``arrs`` gives each sequence's rows after the anchors (else n_recent)."""
     n_spans = np.asarray(arrs["n_spans"])
+    n_tail = arrs.get("n_tail")
     B = n_spans.shape[0]
     Hkv = arrs["k_full"].shape[1]
     store = np.asarray(arrs["store"], np.uint8)
@@ -181,7 +183,7 @@ def unpack_layer(arrs: Dict[str, np.ndarray], n_sink: int, n_recent: int,
         ns = int(n_spans[b])
         body = np.asarray(arrs["body_len"][b, :ns], np.int64)
         out.body_len.append(body)
-        nf = n_sink + ns + n_recent
+        nf = n_sink + ns + (n_recent if n_tail is None else int(n_tail[b]))
         kf, vf, sr, ks, vs, fac = [], [], [], [], [], []
         for c in range(Hkv):
             if groups is not None and (b, c) not in groups:
