@@ -55,9 +55,10 @@ def parse():
     ap.add_argument("--traffic-workload", default="llama3_8b_128k")
     ap.add_argument("--traffic-scale", type=float, default=1.0)
     ap.add_argument("--traffic-command", default="")
-    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv"],
+    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv", "append"],
                     help="decode: the headline decode step; build: the prefill cache build; "
-                         "fullkv: the same decode step over a full-KV cache (comparator)")
+                         "fullkv: the same decode step over a full-KV cache (comparator); "
+                         "append: decode-time cache maintenance, one token per step")
     return ap.parse_args()
 
 
@@ -792,6 +793,121 @@ def fp32_peak_tflops(dev) -> dict:
             "nominal": props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12}
 
 
+def run_append_bench(args, ws_n, rank, local):
+    """Decode-time cache maintenance at 128K (Mistral-7B shape, one layer): the
+    prefill build of the first 131,072 - 1,024 tokens, then one appended token
+    per step (sekv_append_token): the token joins the tail, the token leaving
+    the recent window continues the segmentation walk, and about one step in
+    32 closes a span of every KV head, which is then built (summaries and the
+    gated SVD of both sides) and leaves full resolution."""
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (append) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.get_config("mistral_7b_build_128k")
+    n_app = 1024
+    T0 = w.ctx - n_app
+    n_sp = len(gen.sequence_spans(w, 0))
+    ms = (n_sp + w.len_max + 63) // 64 * 64
+    inp = gen.build_inputs(w, 0, device="cpu", max_spans=ms)
+    K, V = inp["K"].to(dev), inp["V"].to(dev)
+    H = torch.from_numpy(inp["H"]).to(dev)
+    W = inp["W_r"].to(dev)
+    gates = torch.from_numpy(inp["gates"]).to(dev)
+    cfg = sk.Config(w.batch, w.n_q_heads, w.n_kv_heads, w.n_sink, w.n_recent, ms, w.rank_cap,
+                    w.len_min, w.len_max, w.tau)
+    ws = sk.Workspace(cfg, which=sk.sekv.SEKV_CALL_BUILD, ctx_len=w.ctx)
+    out = sk.alloc_cache(cfg, 1 << 30, dev)
+    K0, V0, H0 = K[:, :, :T0].contiguous(), V[:, :, :T0].contiguous(), H[:, :T0].contiguous()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        sk.build_spans(cfg, K0, V0, H0, W, gates, out, ws, stream=stream)
+        mt = sk.Maintainer(cfg, out, K0, V0, H0, T0, ws, stream=stream)
+    del K0, V0
+    kv = [(K[:, :, t].contiguous(), V[:, :, t].contiguous(), H[:, t].contiguous())
+          for t in range(T0, w.ctx)]
+    # the decode loop's view: the model writes each new token's key, value and
+    # surprisal into fixed buffers, and one CUDA graph appends it
+    kbuf, vbuf, hbuf = (torch.empty_like(x) for x in kv[0])
+
+    def load(i):
+        kbuf.copy_(kv[i][0])
+        vbuf.copy_(kv[i][1])
+        hbuf.copy_(kv[i][2])
+
+    warm = max(args.warmup, 3)
+    steps = min(args.steps, (n_app - warm) // 2)
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            load(i)
+            mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
+    ws.raise_on_error()
+    sk.build_flops(ws)
+    spans0 = int(out["n_spans"][0])
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(warm, warm + steps):
+            load(i)
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    barrier(ws_n)
+    ws.raise_on_error()
+    closed = int(out["n_spans"][0]) - spans0
+    flops = sk.build_flops(ws)
+    # the same appends launched eagerly, for comparison
+    ee0 = torch.cuda.Event(enable_timing=True)
+    ee1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ee0.record(stream)
+        for i in range(warm + steps, warm + 2 * steps):
+            load(i)
+            mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
+        ee1.record(stream)
+    torch.cuda.synchronize()
+    ws.raise_on_error()
+    eager_us = ee0.elapsed_time(ee1) * 1e3 / steps
+    ms_total = max_over_ranks(e0.elapsed_time(e1), ws_n)
+    us = ms_total * 1e3 / steps
+    if rank != 0:
+        return
+    fp32 = fp32_peak_tflops(dev)
+    alu = flops / (ms_total / 1e3) / 1e12
+    line = {"metric": "decode-time cache maintenance: us per appended token (one 128K layer, "
+                      "8 KV heads)",
+            "value": us, "unit": "us/token", "n_gpus": ws_n, "steps": steps, "warmup": warm,
+            "ms_per_step": ms_total / steps, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, fp32 compute", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "ctx_before": T0 + warm,
+                       "kv_heads": w.n_kv_heads, "rank_cap": w.rank_cap,
+                       "spans_closed": closed, "closes_per_token": closed / steps,
+                       "launches_per_append": 8,
+                       "graph": "one CUDA graph per append (inputs copied into fixed buffers "
+                                "first, inside the timed region)",
+                       "eager_us_per_token": eager_us},
+            "roofline": {"bound": "alu", "achieved": alu, "peak": fp32["measured"],
+                         "unit": "TFLOP/s", "frac": alu / fp32["measured"], "traffic": None,
+                         "peak_kind": "measured fp32 (cuBLAS SGEMM, TF32 off)",
+                         "flops_per_token": flops / steps,
+                         "note": "latency-bound: each append is 8 short launches; the SVD "
+                                 "arithmetic of the spans that close is all the work"},
+            "clocks": ck, "gpu_launches": 8 * steps}
+    print(json.dumps(line), flush=True)
+
+
 def run_build_bench(args, ws_n, rank, local):
     """Prefill cache build at 128K (Mistral-7B shape): segmentation, summaries
     and the batched gated span SVD of every span, one layer per call.  Two
@@ -946,6 +1062,8 @@ def main():
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm (the oracle) "
                               "is timed on the decode path only"}), flush=True)
         return
+    if args.path == "append":
+        return run_append_bench(args, ws_n, rank, local)
     if args.path == "build":
         run_build_bench(args, ws_n, rank, local)
         return

@@ -72,6 +72,7 @@ struct MaintParams {
   int32_t* rec_rank;
   int64_t store_capacity;
   // maintenance state (caller-owned, kept across calls)
+  int32_t* seq_len;                // [B] sequence lengths
   int32_t* s_open;                 // [B] the open span's anchor position, -1: none
   unsigned long long* store_used;  // bytes of the store in use (records go after)
   int32_t* pend;                   // [B][8] this call's decision, for the commit
@@ -85,7 +86,7 @@ struct MaintParams {
   int32_t* counters;
   int32_t* cls_list;
   int64_t cls_cap;
-  int B, Hkv, T, cap, n_sink, n_recent, max_spans, rank_cap, len_min, len_max;
+  int B, Hkv, T, cap, n_sink, n_recent, max_spans, rank_cap, len_min, len_max;  // T: init only
   float tau;
 };
 

@@ -143,7 +143,7 @@ extern "C" sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, in
 namespace {
 
 struct MaintState {
-  size_t s_open, store_used, pend, only_k, tail_h, total;
+  size_t seq_len, s_open, store_used, pend, only_k, tail_h, total;
 };
 
 int64_t full_cap(const sekv_config* cfg) {
@@ -154,6 +154,7 @@ MaintState maint_state(const sekv_config* cfg) {
   MaintState S{};
   const size_t B = cfg->batch;
   size_t off = 0;
+  S.seq_len = off;    off += align256(B * 4);
   S.s_open = off;     off += align256(B * 4);
   S.store_used = off; off += align256(8);
   S.pend = off;       off += align256(B * 32);
@@ -200,6 +201,7 @@ MaintParams maint_params(const sekv_config* cfg, int64_t ctx_len, const sekv_cac
   M.rec_off = out->rec_off;
   M.rec_rank = out->rec_rank;
   M.store_capacity = out->store_capacity;
+  M.seq_len = reinterpret_cast<int32_t*>(st + S.seq_len);
   M.s_open = reinterpret_cast<int32_t*>(st + S.s_open);
   M.store_used = reinterpret_cast<unsigned long long*>(st + S.store_used);
   M.pend = reinterpret_cast<int32_t*>(st + S.pend);
@@ -254,14 +256,15 @@ extern "C" sekv_status sekv_maint_init(const sekv_config* cfg, int64_t ctx_len, 
   return SEKV_OK;
 }
 
-extern "C" sekv_status sekv_append_token(const sekv_config* cfg, int64_t ctx_len,
-                                         const void* k_new, const void* v_new,
+extern "C" sekv_status sekv_append_token(const sekv_config* cfg, const void* k_new,
+                                         const void* v_new,
                                          const float* h_new, const float* W_r,
                                          const float* gates, const sekv_cache_out* out,
                                          int32_t* n_tail, void* state, size_t state_bytes,
                                          void* workspace, size_t workspace_bytes,
                                          cudaStream_t stream) {
   reset_launches();
+  const int64_t ctx_len = int64_t(cfg ? cfg->n_sink : 0) + (cfg ? cfg->n_recent : 0);  // checks only
   if (!maint_args_ok(cfg, ctx_len, out, n_tail, state, state_bytes, workspace, workspace_bytes))
     return SEKV_ERR_INVALID;
   if (!k_new || !v_new || !h_new || !W_r || !gates || !al16(k_new) || !al16(v_new) ||

@@ -129,6 +129,7 @@ __global__ void maint_init_commit_kernel(const MaintParams M) {
   M.n_spans[b] = pd[0];
   M.n_tail[b] = pd[1];
   M.s_open[b] = pd[2];
+  M.seq_len[b] = M.T;
 }
 
 // grid (B*Hkv): the end of the records in the store (their maximum end).
@@ -151,14 +152,14 @@ __global__ void __launch_bounds__(256) maint_used_kernel(const MaintParams M) {
 // ---------------------------------------------------------------------------
 // one append, step 1 (grid (Hkv, B)): the new token's row at the end of the
 // tail; the segmentation decision for the token leaving the recent window
-// (t = T - n_recent); for a span this closes (ordinal k = n_spans): its ranks
+// (t = T - n_recent, T the sequence's length before the append); for a span this closes (ordinal k = n_spans): its ranks
 // from the gates, its record's place at the end of the store, its SVD work
 // items, and the empty-body case written out.  pend[b] = {closes, k, body,
 // n_tail after, s_open after}.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) maint_plan_kernel(const MaintParams M) {
   const int c = blockIdx.x, b = blockIdx.y, g = b * M.Hkv + c, tid = threadIdx.x;
-  const int n_sp = M.n_spans[b], n_tail = M.n_tail[b], s = M.s_open[b];
+  const int n_sp = M.n_spans[b], n_tail = M.n_tail[b], s = M.s_open[b], T = M.seq_len[b];
   const int row0 = M.n_sink + n_sp;  // the tail's first row
   const int r_new = row0 + n_tail;
   if (r_new >= M.cap || n_sp >= M.max_spans) {
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(256) maint_plan_kernel(const MaintParams M) {
                                         (size_t(g) * M.cap + r_new) * kHeadDim);
     dst[tid & 15] = src[tid & 15];
   }
-  const int t = M.T - M.n_recent;
+  const int t = T - M.n_recent;
   int closes = 0, s_new = s, n = 0;
   if (t >= M.n_sink) {
     if (s < 0) {
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(256) maint_commit_kernel(const MaintParams M) 
     if (closes) M.n_spans[b] = k + 1;
     M.n_tail[b] = n_tail_new;
     M.s_open[b] = s_new;
+    M.seq_len[b] += 1;
   }
 }
 

@@ -104,7 +104,7 @@ def lib() -> ctypes.CDLL:
                                       ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp, _c_sz, _c_vp,
                                       _c_sz, _c_vp]
         L.sekv_append_token.restype = _c_i32
-        L.sekv_append_token.argtypes = [ctypes.POINTER(SekvConfig), _c_i64, _c_vp, _c_vp, _c_vp,
+        L.sekv_append_token.argtypes = [ctypes.POINTER(SekvConfig), _c_vp, _c_vp, _c_vp,
                                         _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp,
                                         _c_sz, _c_vp, _c_sz, _c_vp]
         L.sekv_basis_cache_bytes.restype = _c_sz
@@ -504,12 +504,14 @@ class Maintainer:
                                      self.state.numel(), ws.ptr(), ws.nbytes, _stream(stream)))
 
     def append(self, k_new, v_new, h_new, W_r, gates, stream=None):
+        """sekv_append_token: one token per sequence (lengths advance on the
+        device; `T` here mirrors them for the caller)."""
         _need(k_new, "k_new", torch.bfloat16); _need(v_new, "v_new", torch.bfloat16)
         _need(h_new, "h_new", torch.float32); _need(W_r, "W_r", torch.float32)
         _need(gates, "gates", torch.float32)
         c = self.cfg.c()
         _check("sekv_append_token",
-               lib().sekv_append_token(ctypes.byref(c), self.T, _ptr(k_new), _ptr(v_new),
+               lib().sekv_append_token(ctypes.byref(c), _ptr(k_new), _ptr(v_new),
                                        _ptr(h_new), _ptr(W_r), _ptr(gates), ctypes.byref(self._o),
                                        _ptr(self.n_tail), _ptr(self.state), self.state.numel(),
                                        self.ws.ptr(), self.ws.nbytes, _stream(stream)))

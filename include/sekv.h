@@ -467,7 +467,7 @@ sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, int64_t* flop
  * `store`.  The workspace is a build workspace (SEKV_CALL_BUILD); device
  * errors go to its status word (code 3: no room left -- rows, spans or store
  * -- with the sequence or the MiB needed as detail).  All sequences of the
- * batch have the same length ctx_len (the length before the call).
+ * batch start from the same length (sekv_maint_init's ctx_len).
  */
 size_t sekv_maint_state_size(const sekv_config* cfg);
 
@@ -480,12 +480,14 @@ sekv_status sekv_maint_init(const sekv_config* cfg, int64_t ctx_len, const void*
                             int32_t* n_tail, void* state, size_t state_bytes, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
-/* Appends one token to every sequence (ctx_len -> ctx_len + 1): k_new, v_new
- * bf16 [B][Hkv][128] (16-byte aligned), h_new f32 [B] its surprisal; W_r and
- * gates as sekv_build_spans (gates indexed by span ordinal).  The cache (out,
- * n_tail) is updated in place on `stream`; read it with a sekv_layer_cache
- * that carries n_tail. */
-sekv_status sekv_append_token(const sekv_config* cfg, int64_t ctx_len, const void* k_new,
+/* Appends one token to every sequence: k_new, v_new bf16 [B][Hkv][128]
+ * (16-byte aligned), h_new f32 [B] its surprisal; W_r and gates as
+ * sekv_build_spans (gates indexed by span ordinal).  The sequence lengths live
+ * in the state (set by sekv_maint_init, advanced by each call), so a decode
+ * loop can capture this call in a CUDA graph.  The cache (out, n_tail) is
+ * updated in place on `stream`; read it with a sekv_layer_cache that carries
+ * n_tail. */
+sekv_status sekv_append_token(const sekv_config* cfg, const void* k_new,
                               const void* v_new, const float* h_new, const float* W_r,
                               const float* gates, const sekv_cache_out* out, int32_t* n_tail,
                               void* state, size_t state_bytes, void* workspace,

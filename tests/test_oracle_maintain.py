@@ -5,9 +5,10 @@ Two independent checks:
 * a hand-worked sequence (tests/golden/maintenance_worked.txt) fixes the
   positions: when a span opens and closes, which rows stay at full
   resolution, and in what order;
-* after every appended token, the maintained cache equals the batch build of
-  the same prefix with the recent window taken from the open span's anchor
-  (``closed_build``), array by array and factor by factor.  The batch side
+* after every appended token (and every flush of the closed spans waiting to
+  be built), the maintained cache equals the batch build of the same prefix
+  with the recent window taken from the anchor of the first span not yet
+  built (``closed_build``), array by array and factor by factor.  The batch side
   walks the whole prefix and builds every span from the raw K/V; the
   maintained side only ever sees one token at a time.
 """
@@ -120,3 +121,27 @@ def test_maintenance_from_an_empty_middle_region():
     kw = dict(n_sink=3, n_recent=6, tau=2.8, len_min=3, len_max=12, rank_cap=3)
     closes = _run_equal_to_closed_build(12, B=1, Hkv=1, T0=9, T1=60, **kw)
     assert closes >= 3
+
+
+def test_deferred_builds_equal_the_batch_build_with_a_longer_tail():
+    """Closed spans wait in the tail until a flush: after every append the
+    cache equals the batch build whose full-resolution tail starts at the
+    first span not yet built; flushes at irregular intervals build them all."""
+    kw = dict(n_sink=2, n_recent=5, tau=2.2, len_min=1, len_max=7, rank_cap=4)
+    rng = np.random.default_rng(13)
+    B, Hkv, T0, T1 = 2, 2, 20, 90
+    K, V, H, W, gates = _rand_inputs(rng, B, Hkv, T1, kw["rank_cap"], 512)
+    st = maintain.init_state(K[:, :, :T0], V[:, :, :T0], H[:, :T0], W, gates, **kw)
+    flush_at = set(int(x) for x in rng.choice(np.arange(T0 + 1, T1 + 1), 9, replace=False))
+    most_pending = 0
+    for T in range(T0 + 1, T1 + 1):
+        maintain.append_token(st, K[:, :, T - 1], V[:, :, T - 1], H[:, T - 1], build=False)
+        most_pending = max(most_pending, max(len(p) for p in st.pending))
+        if T in flush_at:
+            maintain.flush(st, W, gates)
+            assert all(not p for p in st.pending)
+        built = [st.caches[b].n_spans(0) for b in range(B)]
+        ref = maintain.closed_build(K[:, :, :T], V[:, :, :T], H[:, :T], W, gates, n_built=built, **kw)
+        for b in range(B):
+            _same_cache(st.caches[b], ref[b])
+    assert most_pending >= 3
