@@ -796,17 +796,19 @@ def fp32_peak_tflops(dev) -> dict:
 def run_append_bench(args, ws_n, rank, local):
     """Decode-time cache maintenance at 128K (Mistral-7B shape, one layer): the
     prefill build of the first 131,072 - 1,024 tokens, then one appended token
-    per step (sekv_append_token): the token joins the tail, the token leaving
-    the recent window continues the segmentation walk, and about one step in
-    32 closes a span of every KV head, which is then built (summaries and the
-    gated SVD of both sides) and leaves full resolution."""
+    per step (sekv_append_token: the token joins the tail, the token leaving
+    the recent window continues the segmentation walk; about one step in 32
+    closes a span of every KV head) and a flush (sekv_maint_flush: the closed
+    spans' summaries and gated SVD bases, their body rows leave full
+    resolution) every FLUSH_EVERY steps.  Appends and flushes are CUDA graphs
+    over fixed input buffers, as in a decode loop."""
     import decode_attention_span_gb300 as sk
     if not torch.cuda.is_available():
         raise SystemExit("bench.py (append) needs a CUDA device")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.get_config("mistral_7b_build_128k")
-    n_app = 1024
+    n_app, every = 1024, 64
     T0 = w.ctx - n_app
     n_sp = len(gen.sequence_spans(w, 0))
     ms = (n_sp + w.len_max + 63) // 64 * 64
@@ -827,84 +829,90 @@ def run_append_bench(args, ws_n, rank, local):
     del K0, V0
     kv = [(K[:, :, t].contiguous(), V[:, :, t].contiguous(), H[:, t].contiguous())
           for t in range(T0, w.ctx)]
-    # the decode loop's view: the model writes each new token's key, value and
-    # surprisal into fixed buffers, and one CUDA graph appends it
-    kbuf, vbuf, hbuf = (torch.empty_like(x) for x in kv[0])
-
-    def load(i):
-        kbuf.copy_(kv[i][0])
-        vbuf.copy_(kv[i][1])
-        hbuf.copy_(kv[i][2])
-
+    # the appends of each chunk of tokens, and the flush that closes the chunk,
+    # captured as one CUDA graph (each token's inputs at their own address, as
+    # a decode loop's projection would write them); the timed region replays
+    # the chunks' graphs back to back
     warm = max(args.warmup, 3)
-    steps = min(args.steps, (n_app - warm) // 2)
     with torch.cuda.stream(stream):
         for i in range(warm):
-            load(i)
-            mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
+            mt.append(*kv[i], stream=stream)
+        mt.flush(W, gates, stream=stream)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
+
+    def chunk_graph(i0, n, flush_every):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            for i in range(i0, i0 + n):
+                mt.append(*kv[i], stream=stream)
+                if flush_every and (i - i0 + 1) % flush_every == 0:
+                    mt.flush(W, gates, stream=stream)
+        return gph
+
+    def timed(graphs):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        s0 = int(out["n_spans"][0])
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for gph in graphs:
+                gph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), int(out["n_spans"][0]) - s0
+
+    steps = min(args.steps, 512)
+    steps -= steps % every
+    main = [chunk_graph(warm + i0, every, every) for i0 in range(0, steps, every)]
+    i = warm + steps
+    g_app = chunk_graph(i, 32, 0)            # 32 appends alone (their spans wait)
+    g_fl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fl, stream=stream):
+        mt.flush(W, gates, stream=stream)   # the flush of those 32 appends
+    g_imm = chunk_graph(i + 32, 128, 1)     # a flush after every append
     ws.raise_on_error()
     sk.build_flops(ws)
-    spans0 = int(out["n_spans"][0])
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(ws_n)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(warm, warm + steps):
-            load(i)
-            graph.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
+    ms_total, closed = timed(main)
     ck = clocks.stop()
     barrier(ws_n)
     ws.raise_on_error()
-    closed = int(out["n_spans"][0]) - spans0
     flops = sk.build_flops(ws)
-    # the same appends launched eagerly, for comparison
-    ee0 = torch.cuda.Event(enable_timing=True)
-    ee1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ee0.record(stream)
-        for i in range(warm + steps, warm + 2 * steps):
-            load(i)
-            mt.append(kbuf, vbuf, hbuf, W, gates, stream=stream)
-        ee1.record(stream)
-    torch.cuda.synchronize()
+    ms_total = max_over_ranks(ms_total, ws_n)
+    ms_app, _ = timed([g_app])
+    ms_fl1, _ = timed([g_fl])
+    ms_imm, closed_imm = timed([g_imm])
     ws.raise_on_error()
-    eager_us = ee0.elapsed_time(ee1) * 1e3 / steps
-    ms_total = max_over_ranks(e0.elapsed_time(e1), ws_n)
     us = ms_total * 1e3 / steps
     if rank != 0:
         return
     fp32 = fp32_peak_tflops(dev)
     alu = flops / (ms_total / 1e3) / 1e12
     line = {"metric": "decode-time cache maintenance: us per appended token (one 128K layer, "
-                      "8 KV heads)",
+                      "8 KV heads, a flush every 64 tokens)",
             "value": us, "unit": "us/token", "n_gpus": ws_n, "steps": steps, "warmup": warm,
             "ms_per_step": ms_total / steps, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 in, fp32 compute", "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "ctx_before": T0 + warm,
                        "kv_heads": w.n_kv_heads, "rank_cap": w.rank_cap,
-                       "spans_closed": closed, "closes_per_token": closed / steps,
-                       "launches_per_append": 8,
-                       "graph": "one CUDA graph per append (inputs copied into fixed buffers "
-                                "first, inside the timed region)",
-                       "eager_us_per_token": eager_us},
+                       "flush_every": every, "spans_built": closed,
+                       "graph": "each chunk of 64 appends and its flush captured as one CUDA "
+                                "graph; the chunks' graphs replayed back to back"},
+            "append_us": ms_app * 1e3 / 32,
+            "flush_us_after_32_appends": ms_fl1 * 1e3,
+            "flush_after_every_append_us_per_token": ms_imm * 1e3 / 128,
+            "spans_built_flushing_every_append": closed_imm,
             "roofline": {"bound": "alu", "achieved": alu, "peak": fp32["measured"],
                          "unit": "TFLOP/s", "frac": alu / fp32["measured"], "traffic": None,
                          "peak_kind": "measured fp32 (cuBLAS SGEMM, TF32 off)",
                          "flops_per_token": flops / steps,
-                         "note": "latency-bound: each append is 8 short launches; the SVD "
-                                 "arithmetic of the spans that close is all the work"},
-            "clocks": ck, "gpu_launches": 8 * steps}
+                         "note": "latency-bound: a flush is a few short launches and one wave of "
+                                 "span SVDs (16 per span: 8 KV heads x keys and values)"},
+            "clocks": ck, "gpu_launches": steps + 9 * (steps // every)}
     print(json.dumps(line), flush=True)
 
 

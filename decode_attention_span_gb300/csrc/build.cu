@@ -182,8 +182,9 @@ __global__ void __launch_bounds__(256) summary_kernel(const BuildParams P) {
   __shared__ float kh[8][kHeadDim];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = g / P.Hkv, c = g % P.Hkv;
-  // decode-time maintenance: warp 0 of each group's CTA, span only_k[b]
-  const int k = P.only_k != nullptr ? (wid == 0 ? P.only_k[b] : -1) : blockIdx.x * 8 + wid;
+  // decode-time maintenance: spans only_k[b] .. only_k[b] + only_n[b] - 1
+  const int j = blockIdx.x * 8 + wid;
+  const int k = P.only_k != nullptr ? (j < P.only_n[b] ? P.only_k[b] + j : -1) : j;
   const size_t gs = size_t(g) * P.max_spans;
   if (k < 0 || k >= P.max_spans) return;
   const int n_sp = P.only_k != nullptr ? k + 1 : P.n_spans[b];

@@ -43,9 +43,11 @@ struct BuildParams {
   int32_t* counters;       // [0..3] class counts, [4..7] class cursors, [8] plan CTAs done
   int32_t* cls_list;       // [4][B*Hkv*max_spans*2]
   int64_t cls_cap;
-  // decode-time maintenance: summaries of span only_k[b] of each sequence
-  // (-1: none) instead of every span; null in the prefill build
+  // decode-time maintenance: summaries of spans only_k[b] .. only_k[b] +
+  // only_n[b] - 1 of each sequence instead of every span; null in the
+  // prefill build
   const int32_t* only_k;
+  const int32_t* only_n;
   int B, Hkv, T, n_sink, n_recent, max_spans, rank_cap, len_min, len_max;
   float tau;
 };
@@ -74,9 +76,13 @@ struct MaintParams {
   // maintenance state (caller-owned, kept across calls)
   int32_t* seq_len;                // [B] sequence lengths
   int32_t* s_open;                 // [B] the open span's anchor position, -1: none
+  int32_t* n_pend;                 // [B] closed spans not yet built (head of the tail)
+  int32_t* pend_rows;              // [B] their rows (anchors and bodies)
+  int32_t* pend_len;               // [B][kMaxPending] their lengths, in order
   unsigned long long* store_used;  // bytes of the store in use (records go after)
-  int32_t* pend;                   // [B][8] this call's decision, for the commit
-  int32_t* only_k;                 // [B] the span this call closes, -1: none
+  int32_t* pend;                   // [B][8] init: the values to commit
+  int32_t* only_k;                 // [B] first ordinal a flush builds
+  int32_t* only_n;                 // [B] how many it builds
   float* tail_h;                   // [B][cap] surprisal of the token in each full row
   // build workspace
   int32_t* status;
@@ -94,8 +100,13 @@ __global__ void maint_init_rows_kernel(const MaintParams M, const __nv_bfloat16*
                                        const __nv_bfloat16* V, const float* H);
 __global__ void maint_init_commit_kernel(const MaintParams M);
 __global__ void maint_used_kernel(const MaintParams M);
-__global__ void maint_plan_kernel(const MaintParams M);
-__global__ void maint_commit_kernel(const MaintParams M);
+__global__ void maint_append_kernel(const MaintParams M);
+__global__ void maint_flush_plan_kernel(const MaintParams M);
+__global__ void maint_flush_move_kernel(const MaintParams M);
+__global__ void maint_flush_commit_kernel(const MaintParams M);
+
+// closed spans a sequence can hold unbuilt (a flush is needed before more)
+constexpr int kMaxPending = 128;
 
 __global__ void seg_kernel(const BuildParams P);
 __global__ void plan_kernel(const BuildParams P);

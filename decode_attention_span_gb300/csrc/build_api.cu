@@ -95,6 +95,7 @@ extern "C" sekv_status sekv_build_spans(const sekv_config* cfg, int64_t ctx_len,
   P.cls_list = reinterpret_cast<int32_t*>(w + L.cls_list);
   P.cls_cap = L.cls_cap;
   P.only_k = nullptr;
+  P.only_n = nullptr;
   P.B = cfg->batch;
   P.Hkv = cfg->n_kv_heads;
   P.T = int(ctx_len);
@@ -143,7 +144,8 @@ extern "C" sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, in
 namespace {
 
 struct MaintState {
-  size_t seq_len, s_open, store_used, pend, only_k, tail_h, total;
+  size_t seq_len, s_open, n_pend, pend_rows, pend_len, store_used, pend, only_k, only_n, tail_h,
+      total;
 };
 
 int64_t full_cap(const sekv_config* cfg) {
@@ -156,9 +158,13 @@ MaintState maint_state(const sekv_config* cfg) {
   size_t off = 0;
   S.seq_len = off;    off += align256(B * 4);
   S.s_open = off;     off += align256(B * 4);
+  S.n_pend = off;     off += align256(B * 4);
+  S.pend_rows = off;  off += align256(B * 4);
+  S.pend_len = off;   off += align256(B * kMaxPending * 4);
   S.store_used = off; off += align256(8);
   S.pend = off;       off += align256(B * 32);
   S.only_k = off;     off += align256(B * 4);
+  S.only_n = off;     off += align256(B * 4);
   S.tail_h = off;     off += align256(B * size_t(full_cap(cfg)) * 4);
   S.total = off;
   return S;
@@ -203,6 +209,10 @@ MaintParams maint_params(const sekv_config* cfg, int64_t ctx_len, const sekv_cac
   M.store_capacity = out->store_capacity;
   M.seq_len = reinterpret_cast<int32_t*>(st + S.seq_len);
   M.s_open = reinterpret_cast<int32_t*>(st + S.s_open);
+  M.n_pend = reinterpret_cast<int32_t*>(st + S.n_pend);
+  M.pend_rows = reinterpret_cast<int32_t*>(st + S.pend_rows);
+  M.pend_len = reinterpret_cast<int32_t*>(st + S.pend_len);
+  M.only_n = reinterpret_cast<int32_t*>(st + S.only_n);
   M.store_used = reinterpret_cast<unsigned long long*>(st + S.store_used);
   M.pend = reinterpret_cast<int32_t*>(st + S.pend);
   M.only_k = reinterpret_cast<int32_t*>(st + S.only_k);
@@ -257,32 +267,46 @@ extern "C" sekv_status sekv_maint_init(const sekv_config* cfg, int64_t ctx_len, 
 }
 
 extern "C" sekv_status sekv_append_token(const sekv_config* cfg, const void* k_new,
-                                         const void* v_new,
-                                         const float* h_new, const float* W_r,
-                                         const float* gates, const sekv_cache_out* out,
-                                         int32_t* n_tail, void* state, size_t state_bytes,
-                                         void* workspace, size_t workspace_bytes,
-                                         cudaStream_t stream) {
+                                         const void* v_new, const float* h_new,
+                                         const sekv_cache_out* out, int32_t* n_tail, void* state,
+                                         size_t state_bytes, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream) {
   reset_launches();
   const int64_t ctx_len = int64_t(cfg ? cfg->n_sink : 0) + (cfg ? cfg->n_recent : 0);  // checks only
   if (!maint_args_ok(cfg, ctx_len, out, n_tail, state, state_bytes, workspace, workspace_bytes))
     return SEKV_ERR_INVALID;
-  if (!k_new || !v_new || !h_new || !W_r || !gates || !al16(k_new) || !al16(v_new) ||
-      !al16(W_r) || (reinterpret_cast<uintptr_t>(gates) & 3))
-    return SEKV_ERR_INVALID;
-  const int sms = device_sm_count();
-  if (sms <= 0) return SEKV_ERR_CUDA;
+  if (!k_new || !v_new || !h_new || !al16(k_new) || !al16(v_new)) return SEKV_ERR_INVALID;
   MaintParams M = maint_params(cfg, ctx_len, out, n_tail, state, workspace);
   M.k_new = static_cast<const __nv_bfloat16*>(k_new);
   M.v_new = static_cast<const __nv_bfloat16*>(v_new);
   M.h_new = h_new;
+  maint_append_kernel<<<cfg->batch, 256, 0, stream>>>(M);
+  if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
+  count_launch(1);
+  return SEKV_OK;
+}
+
+extern "C" sekv_status sekv_maint_flush(const sekv_config* cfg, const float* W_r,
+                                        const float* gates, const sekv_cache_out* out,
+                                        int32_t* n_tail, void* state, size_t state_bytes,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+  reset_launches();
+  const int64_t ctx_len = int64_t(cfg ? cfg->n_sink : 0) + (cfg ? cfg->n_recent : 0);  // checks only
+  if (!maint_args_ok(cfg, ctx_len, out, n_tail, state, state_bytes, workspace, workspace_bytes))
+    return SEKV_ERR_INVALID;
+  if (!W_r || !gates || !al16(W_r) || (reinterpret_cast<uintptr_t>(gates) & 3))
+    return SEKV_ERR_INVALID;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SEKV_ERR_CUDA;
+  MaintParams M = maint_params(cfg, ctx_len, out, n_tail, state, workspace);
   M.gates = gates;
   const BuildWs L = build_ws(cfg);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   if (cudaMemsetAsync(w + L.counters, 0, 16 * 4, stream) != cudaSuccess) return SEKV_ERR_CUDA;
   const dim3 grid(cfg->n_kv_heads, cfg->batch);
-  maint_plan_kernel<<<grid, 256, 0, stream>>>(M);
-  // the closed span's summaries and basis: the build's kernels, in place on
+  maint_flush_plan_kernel<<<grid, kMaxPending, 0, stream>>>(M);
+  // the waiting spans' summaries and bases: the build's kernels, in place on
   // the full rows (K = the rows of each group, T = their capacity, H = the
   // surprisal by row)
   BuildParams P{};
@@ -312,6 +336,7 @@ extern "C" sekv_status sekv_append_token(const sekv_config* cfg, const void* k_n
   P.cls_list = M.cls_list;
   P.cls_cap = M.cls_cap;
   P.only_k = M.only_k;
+  P.only_n = M.only_n;
   P.B = M.B;
   P.Hkv = M.Hkv;
   P.T = M.cap;
@@ -322,11 +347,12 @@ extern "C" sekv_status sekv_append_token(const sekv_config* cfg, const void* k_n
   P.len_min = M.len_min;
   P.len_max = M.len_max;
   P.tau = M.tau;
-  summary_kernel<<<dim3(1, cfg->batch * cfg->n_kv_heads), 256, 0, stream>>>(P);
+  summary_kernel<<<dim3(kMaxPending / 8, cfg->batch * cfg->n_kv_heads), 256, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
   if (launch_svd_all(P, sms, stream) != cudaSuccess) return SEKV_ERR_CUDA;
-  maint_commit_kernel<<<grid, 256, 0, stream>>>(M);
+  maint_flush_move_kernel<<<grid, 256, 0, stream>>>(M);
+  maint_flush_commit_kernel<<<cfg->batch, 32, 0, stream>>>(M);
   if (cudaGetLastError() != cudaSuccess) return SEKV_ERR_CUDA;
-  count_launch(8);
+  count_launch(9);
   return SEKV_OK;
 }

@@ -34,7 +34,7 @@ EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
            "sekv_fetch_bases_cached", "sekv_build_flops", "sekv_maint_state_size",
-           "sekv_maint_init", "sekv_append_token",
+           "sekv_maint_init", "sekv_append_token", "sekv_maint_flush",
            "sekv_status_string", "sekv_last_launch_count")
 
 
@@ -105,8 +105,12 @@ def lib() -> ctypes.CDLL:
                                       _c_sz, _c_vp]
         L.sekv_append_token.restype = _c_i32
         L.sekv_append_token.argtypes = [ctypes.POINTER(SekvConfig), _c_vp, _c_vp, _c_vp,
-                                        _c_vp, _c_vp, ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp,
-                                        _c_sz, _c_vp, _c_sz, _c_vp]
+                                        ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp, _c_sz, _c_vp,
+                                        _c_sz, _c_vp]
+        L.sekv_maint_flush.restype = _c_i32
+        L.sekv_maint_flush.argtypes = [ctypes.POINTER(SekvConfig), _c_vp, _c_vp,
+                                       ctypes.POINTER(SekvCacheOut), _c_vp, _c_vp, _c_sz, _c_vp,
+                                       _c_sz, _c_vp]
         L.sekv_basis_cache_bytes.restype = _c_sz
         L.sekv_basis_cache_bytes.argtypes = [ctypes.POINTER(SekvConfig), _c_i32]
         L.sekv_basis_cache_init.restype = _c_i32
@@ -503,19 +507,29 @@ class Maintainer:
                                      ctypes.byref(self._o), _ptr(self.n_tail), _ptr(self.state),
                                      self.state.numel(), ws.ptr(), ws.nbytes, _stream(stream)))
 
-    def append(self, k_new, v_new, h_new, W_r, gates, stream=None):
+    def append(self, k_new, v_new, h_new, stream=None):
         """sekv_append_token: one token per sequence (lengths advance on the
-        device; `T` here mirrors them for the caller)."""
+        device; `T` here mirrors them for the caller).  Spans it closes wait
+        at full resolution until `flush`."""
         _need(k_new, "k_new", torch.bfloat16); _need(v_new, "v_new", torch.bfloat16)
-        _need(h_new, "h_new", torch.float32); _need(W_r, "W_r", torch.float32)
-        _need(gates, "gates", torch.float32)
+        _need(h_new, "h_new", torch.float32)
         c = self.cfg.c()
         _check("sekv_append_token",
-               lib().sekv_append_token(ctypes.byref(c), _ptr(k_new), _ptr(v_new),
-                                       _ptr(h_new), _ptr(W_r), _ptr(gates), ctypes.byref(self._o),
-                                       _ptr(self.n_tail), _ptr(self.state), self.state.numel(),
-                                       self.ws.ptr(), self.ws.nbytes, _stream(stream)))
+               lib().sekv_append_token(ctypes.byref(c), _ptr(k_new), _ptr(v_new), _ptr(h_new),
+                                       ctypes.byref(self._o), _ptr(self.n_tail), _ptr(self.state),
+                                       self.state.numel(), self.ws.ptr(), self.ws.nbytes,
+                                       _stream(stream)))
         self.T += 1
+
+    def flush(self, W_r, gates, stream=None):
+        """sekv_maint_flush: builds every closed span still waiting."""
+        _need(W_r, "W_r", torch.float32); _need(gates, "gates", torch.float32)
+        c = self.cfg.c()
+        _check("sekv_maint_flush",
+               lib().sekv_maint_flush(ctypes.byref(c), _ptr(W_r), _ptr(gates),
+                                      ctypes.byref(self._o), _ptr(self.n_tail), _ptr(self.state),
+                                      self.state.numel(), self.ws.ptr(), self.ws.nbytes,
+                                      _stream(stream)))
 
     def layer_cache(self) -> LayerCache:
         return LayerCache({**{k: self.out[k] for k in CACHE_FIELDS}, "n_tail": self.n_tail})

@@ -452,12 +452,13 @@ sekv_status sekv_build_flops(void* workspace, cudaStream_t stream, int64_t* flop
  * window; the token leaving the window continues the segmentation walk of
  * Methodik 1 (it opens a span iff (H_t > tau and the open span's length >=
  * len_min) or that length == len_max); a span is the run of tokens between
- * two neighbouring anchors, so it is built (routing summary, summary
+ * two neighbouring anchors, so it can be built (routing summary, summary
  * key/value, gated SVD basis: Methodik 2) once the next anchor closes it.
- * Until then the open span -- anchor and body -- stays at full resolution at
- * the head of the tail (sekv_layer_cache.n_tail).  After every append the
- * cache equals the prefill build of the same prefix whose recent window is
- * taken to start at the open span's anchor.
+ * Closed spans wait, with the open span -- anchor and body -- at full
+ * resolution at the head of the tail (sekv_layer_cache.n_tail) until
+ * sekv_maint_flush builds them.  After every append or flush the cache
+ * equals the prefill build of the same prefix whose recent window is taken
+ * to start at the anchor of the first span not yet built.
  *
  * The maintained cache is a sekv_cache_out of the prefill build plus
  * n_tail (int32 [B], caller-owned) and a state buffer of
@@ -481,17 +482,31 @@ sekv_status sekv_maint_init(const sekv_config* cfg, int64_t ctx_len, const void*
                             size_t workspace_bytes, cudaStream_t stream);
 
 /* Appends one token to every sequence: k_new, v_new bf16 [B][Hkv][128]
- * (16-byte aligned), h_new f32 [B] its surprisal; W_r and gates as
- * sekv_build_spans (gates indexed by span ordinal).  The sequence lengths live
- * in the state (set by sekv_maint_init, advanced by each call), so a decode
- * loop can capture this call in a CUDA graph.  The cache (out, n_tail) is
- * updated in place on `stream`; read it with a sekv_layer_cache that carries
- * n_tail. */
-sekv_status sekv_append_token(const sekv_config* cfg, const void* k_new,
-                              const void* v_new, const float* h_new, const float* W_r,
-                              const float* gates, const sekv_cache_out* out, int32_t* n_tail,
+ * (16-byte aligned), h_new f32 [B] its surprisal.  The token joins the tail;
+ * the token leaving the recent window continues the segmentation walk, and a
+ * span this closes waits in the tail (at full resolution) until
+ * sekv_maint_flush builds it.  At most 128 closed spans per sequence may wait
+ * (then flush first: an append that would close one more sets device error
+ * code 3 and does not close it).  The sequence lengths live in the state
+ * (set by sekv_maint_init, advanced by each call), so a decode loop can
+ * capture this call in a CUDA graph.  The cache (out, n_tail) is updated in
+ * place on `stream`; read it with a sekv_layer_cache that carries n_tail. */
+sekv_status sekv_append_token(const sekv_config* cfg, const void* k_new, const void* v_new,
+                              const float* h_new, const sekv_cache_out* out, int32_t* n_tail,
                               void* state, size_t state_bytes, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
+
+/* Builds every closed span waiting in the tails (Methodik 2: routing summary,
+ * summary key/value, gated SVD basis, with W_r and gates as sekv_build_spans,
+ * gates indexed by span ordinal) as the next span ordinals of each sequence;
+ * their body rows leave full resolution.  Flushing after every append builds
+ * each span as soon as it closes; flushing every few tokens batches the
+ * builds (the cache between flushes holds the waiting spans at full
+ * resolution, which is the same prefill build with a longer tail). */
+sekv_status sekv_maint_flush(const sekv_config* cfg, const float* W_r, const float* gates,
+                             const sekv_cache_out* out, int32_t* n_tail, void* state,
+                             size_t state_bytes, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
 
 /* Human-readable name of a status. */
 const char* sekv_status_string(sekv_status status);

@@ -1,9 +1,9 @@
 """GPU parity of decode-time cache maintenance (sekv_maint_init,
-sekv_append_token) against the oracle's reading (oracle/maintain.py): after
-the appends, the maintained cache equals the batch build of the same prefix
-with the recent window taken from each sequence's open span's anchor; and a
-decode step over the maintained cache equals the oracle's decode over that
-build."""
+sekv_append_token, sekv_maint_flush) against the oracle's reading
+(oracle/maintain.py): after the appends and flushes, the maintained cache
+equals the batch build of the same prefix with the recent window taken from
+the anchor of each sequence's first span not yet built; and a decode step
+over the maintained cache equals the oracle's decode over that build."""
 import numpy as np
 import pytest
 import torch
@@ -73,14 +73,19 @@ def compare(got, ref, Hkv):
     return worst
 
 
-@pytest.mark.parametrize("over,T0,n_app", [
-    # 2 sequences, 2 KV heads; bodies up to 63 tokens, ranks up to 32
-    (dict(ctx=2600, n_kv_heads=2, n_q_heads=8, batch=2, len_max=64), 2200, 400),
+@pytest.mark.parametrize("over,T0,n_app,every", [
+    # 2 sequences, 2 KV heads; bodies up to 63 tokens, ranks up to 32; every
+    # closed span built at once
+    (dict(ctx=2600, n_kv_heads=2, n_q_heads=8, batch=2, len_max=64), 2200, 400, 1),
+    # the same with builds batched: a flush every 37 appends, the last
+    # appends left waiting (the decode reads them at full resolution)
+    (dict(ctx=2600, n_kv_heads=2, n_q_heads=8, batch=2, len_max=64), 2200, 400, 37),
     # len_min 1 (one-token spans: empty bodies), bodies past 128 tokens (the
     # 128 x 128 side of the SVD), forced boundaries at len_max 160
-    (dict(ctx=1800, n_kv_heads=1, n_q_heads=4, batch=1, tau=6.1, len_min=1, len_max=160), 1000, 800),
+    (dict(ctx=1800, n_kv_heads=1, n_q_heads=4, batch=1, tau=6.1, len_min=1, len_max=160), 1000,
+     800, 5),
 ])
-def test_append_matches_closed_build_and_decodes(sk, over, T0, n_app):
+def test_append_matches_closed_build_and_decodes(sk, over, T0, n_app, every):
     w = synth.get_config("mistral_7b_build_128k", layers=1, **over)
     T1 = T0 + n_app
     assert T1 == w.ctx
@@ -100,16 +105,20 @@ def test_append_matches_closed_build_and_decodes(sk, over, T0, n_app):
     sk.build_spans(cfg, K0, V0, H0, W, gates, out, ws)
     mt = sk.Maintainer(cfg, out, K0, V0, H0, T0, ws)
     n0 = out["n_spans"].clone()
-    for t in range(T0, T1):
-        mt.append(K[:, :, t].contiguous(), V[:, :, t].contiguous(), H[:, t].contiguous(), W, gates)
+    for i, t in enumerate(range(T0, T1)):
+        mt.append(K[:, :, t].contiguous(), V[:, :, t].contiguous(), H[:, t].contiguous())
+        if (i + 1) % every == 0:
+            mt.flush(W, gates)
     torch.cuda.synchronize()
     assert ws.status() == (0, 0)
-    assert int((out["n_spans"] - n0).min()) >= 5  # several spans closed per sequence
+    assert int((out["n_spans"] - n0).min()) >= 5  # several spans built per sequence
+    built = [int(x) for x in out["n_spans"].cpu()]
 
     kw = dict(n_sink=w.n_sink, n_recent=w.n_recent, tau=w.tau, len_min=w.len_min,
               len_max=w.len_max, rank_cap=w.rank_cap)
     Kn, Vn = inp["K"].float().numpy(), inp["V"].float().numpy()
-    ref = merged(maintain.closed_build(Kn, Vn, inp["H"], inp["W_r"].numpy(), inp["gates"], **kw))
+    ref = merged(maintain.closed_build(Kn, Vn, inp["H"], inp["W_r"].numpy(), inp["gates"],
+                                       n_built=built, **kw))
     arrs = gen.abi_to_numpy({**out, "n_tail": mt.n_tail})
     got = layout.unpack_layer(arrs, w.n_sink, w.n_recent)
     print(compare(got, ref, w.n_kv_heads))
