@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
       gat[j] = j < r ? gin[j] : 0.f;
     }
     for (int e = tid; e < bl * (rs - r); e += NT)  // zero padding columns of U
-      Ud[size_t(e / (rs - r)) * rs + r + e % (rs - r)] = __float2bfloat16_rn(0.f);
+      Ud[size_t(e / (rs - r)) * rs + u_col(e / (rs - r), r + e % (rs - r), rs)] =
+          __float2bfloat16_rn(0.f);
     for (int j = 0; j < r; ++j) {
       const int col = ord[j];
       const float sj = sqrtf(fmaxf(G[col * LD + col], 0.f));
@@ -386,7 +387,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
         }
       }
       if (!LARGE) {
-        for (int i = tid; i < bl; i += NT) Ud[size_t(i) * rs + j] = __float2bfloat16_rn(sgn * Q[i * LD + col]);
+        for (int i = tid; i < bl; i += NT)
+          Ud[size_t(i) * rs + u_col(i, j, rs)] = __float2bfloat16_rn(sgn * Q[i * LD + col]);
       }
     }
     if (LARGE && r > 0) {
@@ -406,7 +408,8 @@ __global__ void __launch_bounds__(NT) svd_kernel(const BuildParams P, int cls) {
           float acc = 0.f;
           for (int d = 0; d < kHeadDim; ++d)
             acc = fmaf(__bfloat162float(Ms[i * kHeadDim + d]), Vs[j * kHeadDim + d], acc);
-          Ud[size_t(r0 + i) * rs + j] = __float2bfloat16_rn(sj > 1e-30f ? acc / sj : 0.f);
+          Ud[size_t(r0 + i) * rs + u_col(r0 + i, j, rs)] =
+              __float2bfloat16_rn(sj > 1e-30f ? acc / sj : 0.f);
         }
       }
     }

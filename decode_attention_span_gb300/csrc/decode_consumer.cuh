@@ -290,7 +290,8 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
 }
 
 // Body tokens [0, n) of this page; U_K rows at uk, U_V rows at uv (row
-// strides r8(rK), r8(rV) bf16), one pass of 16-token tiles with lazy
+// strides r8(rK), r8(rV) bf16, chunks swizzled by u_swz: a page starts at a
+// token that is a multiple of 16), one pass of 16-token tiles with lazy
 // re-basing.  Rows or ranks past the valid ones read neighbouring shared
 // memory and are masked, never multiplied.
 template <int KS>
@@ -300,6 +301,7 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
   (void)rV;
   const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   const int sk = 2 * r8(rK), sv = 2 * r8(rV);  // row strides in bytes
+  const int wk = r8(rK) >> 3, wv = r8(rV) >> 3;  // 16-byte chunks per row (swizzled)
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
   X.had = true;
 #pragma unroll 1
@@ -309,7 +311,7 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a0, a1, a2, a3, m0, m1;
-      ldsm_x4(uku + tq * sk + (16 * ks + 8 * (mi >> 1)) * 2, a0, a1, a2, a3);
+      ldsm_x4(uku + tq * sk + (((2 * ks + (mi >> 1)) ^ u_swz(tq, wk)) << 4), a0, a1, a2, a3);
       pair_masks(16 * ks, rK, m0, m1);
       a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
       mma16816(s, a0, a1, a2, a3, X.ch[ks][0], X.ch[ks][1]);
@@ -334,7 +336,7 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
 #pragma unroll
     for (int t = 0; t < KS; ++t) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(uvu + tv * sv + (16 * t + 8 * (mi & 1)) * 2, a0, a1, a2, a3);
+      ldsm_x4_t(uvu + tv * sv + (((2 * t + (mi & 1)) ^ u_swz(tv, wv)) << 4), a0, a1, a2, a3);
       a0 &= t0; a1 &= t0; a2 &= t1; a3 &= t1;
       mma16816(X.w[t], a0, a1, a2, a3, b0, b1);
     }

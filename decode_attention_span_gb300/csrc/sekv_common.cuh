@@ -266,6 +266,22 @@ __device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int chunk16) 
 
 __host__ __device__ inline int r4(int r) { return (r + 3) & ~3; }
 __host__ __device__ inline int r8(int r) { return (r + 7) & ~7; }
+
+// U rows of a basis record hold W = r8(r) / 8 sixteen-byte chunks; chunk c of
+// token row t is stored at chunk position c ^ u_swz(t, W).  With g the largest
+// power of two dividing W, rows t and t + 8/g start in the same bank group;
+// the XOR with bits of t above log2(8/g) (below g) moves them apart, so the 8
+// rows an ldmatrix reads hit 8 different bank groups.  It stays below W and
+// depends on t mod 8 only.
+__host__ __device__ inline int u_swz(int t, int W) {
+  const int g = W & -W;
+  const int s = 3 - ((g > 1) + (g > 2) + (g > 4));
+  return (t >> s) & (g - 1);
+}
+// element offset of column j of row t in a U block with row stride rs = r8(r)
+__host__ __device__ inline int u_col(int t, int j, int rs) {
+  return (((j >> 3) ^ u_swz(t, rs >> 3)) << 3) | (j & 7);
+}
 __host__ __device__ inline int64_t pad16(int64_t n) { return (n + 15) & ~int64_t(15); }
 
 // Basis record layout (see sekv.h): byte offsets of its parts.

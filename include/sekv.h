@@ -132,7 +132,10 @@ typedef struct sekv_config {
  * Vt rows are stored swizzled: row j's 128 values form sixteen 16-byte
  * chunks (chunk c = columns 8c..8c+7), and chunk c is stored at chunk
  * position c ^ (j & 7) of the row (so that eight consecutive rows read the
- * same columns from eight different shared-memory banks).
+ * same columns from eight different shared-memory banks).  U rows likewise:
+ * token row t of a U block has W = r8(r) / 8 chunks, and chunk c is stored at
+ * chunk position c ^ m(t), m(t) = (t >> (3 - log2 g)) & (g - 1) with g the
+ * largest power of two dividing W (m = 0 for odd W; t & 7 for W = 8).
  * Record size = the sum of the right-hand column (sekv_record_size).
  */
 typedef struct sekv_layer_cache {

@@ -46,6 +46,29 @@ def swizzle_vt(vt: np.ndarray) -> np.ndarray:
     return out
 
 
+def u_swz(t: int, W: int) -> int:
+    """Chunk permutation key of U row t (W sixteen-byte chunks per row): with g
+    the largest power of two dividing W, bits of t above log2(8/g), below g."""
+    g = W & -W
+    s = 3 - ((g > 1) + (g > 2) + (g > 4))
+    return (t >> s) & (g - 1)
+
+
+def swizzle_u(u: np.ndarray) -> np.ndarray:
+    """Chunk permutation of U rows (its own inverse): for token row t of a U
+    block with W = u.shape[1] / 8 chunks per row, chunk c goes to chunk
+    position c ^ u_swz(t, W)."""
+    b, w8 = u.shape
+    W = w8 // 8
+    out = np.empty_like(u)
+    for t in range(b):
+        m = u_swz(t, W)
+        for c in range(W):
+            p = c ^ m
+            out[t, 8 * p:8 * p + 8] = u[t, 8 * c:8 * c + 8]
+    return out
+
+
 def bf16_bits(x) -> np.ndarray:
     """uint16 patterns of values that are already bfloat16-representable."""
     x = np.asarray(x, np.float64)
@@ -83,8 +106,8 @@ def pack_record(F: SpanFactors) -> bytes:
     put(swizzle_vt(bf16_bits(F.VtK).reshape(rK, HEAD_DIM)).reshape(-1), 256 * rK)
     uk = np.zeros((b, _r8(rK)), np.uint16); uk[:, :rK] = bf16_bits(F.UK)
     uv = np.zeros((b, _r8(rV)), np.uint16); uv[:, :rV] = bf16_bits(F.UV)
-    put(uk.reshape(-1), 2 * b * _r8(rK))
-    put(uv.reshape(-1), 2 * b * _r8(rV))
+    put(swizzle_u(uk).reshape(-1), 2 * b * _r8(rK))
+    put(swizzle_u(uv).reshape(-1), 2 * b * _r8(rV))
     sv = np.zeros(_r4(rV), np.float32); sv[:rV] = F.sV
     gv = np.zeros(_r4(rV), np.float32); gv[:rV] = F.gV
     put(sv, 4 * _r4(rV)); put(gv, 4 * _r4(rV))
@@ -110,8 +133,10 @@ def unpack_record(buf: np.ndarray, off: int, b_expected: Optional[int] = None) -
     sK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
     gK = take(4 * rK, 4 * _r4(rK), np.float32).astype(np.float64)
     VtK = swizzle_vt(bits_bf16(take(256 * rK, 256 * rK, np.uint16)).reshape(rK, HEAD_DIM))
-    UK = bits_bf16(take(2 * b * _r8(rK), 2 * b * _r8(rK), np.uint16)).reshape(b, _r8(rK))[:, :rK]
-    UV = bits_bf16(take(2 * b * _r8(rV), 2 * b * _r8(rV), np.uint16)).reshape(b, _r8(rV))[:, :rV]
+    UK = bits_bf16(swizzle_u(take(2 * b * _r8(rK), 2 * b * _r8(rK), np.uint16)
+                             .reshape(b, _r8(rK))))[:, :rK]
+    UV = bits_bf16(swizzle_u(take(2 * b * _r8(rV), 2 * b * _r8(rV), np.uint16)
+                             .reshape(b, _r8(rV))))[:, :rV]
     sV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
     gV = take(4 * rV, 4 * _r4(rV), np.float32).astype(np.float64)
     VtV = swizzle_vt(bits_bf16(take(256 * rV, 256 * rV, np.uint16)).reshape(rV, HEAD_DIM))

@@ -407,7 +407,15 @@ def decode_cache(cfg: WorkloadConfig, layer: int, device="cpu",
         start = torch.cumsum(n_el, 0) - n_el
         e = torch.arange(int(n_el.sum().item()), device=device) - start[rec_i]
         row, colp = e // pad[rec_i], e % pad[rec_i]
-        idx = base_bytes[rec_i] // 2 + row * r8(r_)[rec_i] + r_[rec_i] + colp
+        # the padding columns are in the row's last 16-byte chunk, which the
+        # record layout stores at chunk position (W - 1) ^ u_swz(row, W)
+        W = r8(r_)[rec_i] // 8
+        g = W & -W
+        sh = 3 - ((g > 1).long() + (g > 2).long() + (g > 4).long())
+        key = (row >> sh) & (g - 1)
+        col = r_[rec_i] + colp
+        phys = (((col >> 3) ^ key) << 3) | (col & 7)
+        idx = base_bytes[rec_i] // 2 + row * r8(r_)[rec_i] + phys
         bf[idx] = 0
 
     zero_u_padding(uk_off, b_r, rK_r)
