@@ -13,6 +13,7 @@ from .sekv import (  # noqa: F401
     route,
     decode_attention,
     decode_step,
+    decode_step_multi,
     decode_step_noalloc,
     fetch_bases,
     fetch_bases_copy,

@@ -66,7 +66,8 @@ constexpr int kOffQf = kOffQfrag + 2048;                 // query as f32 [8][128
 constexpr int kOffY = kOffQf + 4096;                     // y = W_r q, f32 [8][64] (2 KB)
 constexpr int kOffBias = kOffY + 2048;                   // summary bias per span (2 KB)
 constexpr int kOffEntries = kOffBias + kSpanCap * 4;     // expanded records (8 KB)
-constexpr int kOffMisc = kOffEntries + kSpanCap * 16;
+constexpr int kOffCmask = kOffEntries + kSpanCap * 16;   // multi-query: columns expanding each span
+constexpr int kOffMisc = kOffCmask + kSpanCap;
 constexpr int kMiscBytes = 4096;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -93,11 +94,12 @@ struct Item {      // one landed (or landing) work item of a warp, 32 bytes
   int boff;        // byte offset of the item's data from the CTA's arena base
   int end;         // the warp's arena granule counter at the item's end
   int uv;          // IT_UT: byte offset of the U_V rows from the item's data
+  int cm;          // records: the query columns that expand the span (bit per column)
 };
 
 struct RecEntry {  // one expanded span of the CTA, 16 bytes
   int off_lo, off_hi;  // byte offset of its record from `store`
-  int body;
+  int body;            // |S| | (columns expanding the span) << 16
   int rank;            // rK | rV << 16
 };
 
@@ -124,7 +126,10 @@ struct DecodeParams {
   int32_t* cta_n;                // [g][cg] expanded spans per CTA (fused, list output)
   int32_t* cta_list;             // [g][max_spans] them, ascending within each CTA's share
   float* partials;               // [g][cg] of 16 + G*128 floats (m[8], l[8], o[G][128])
+  // G: query columns of a group, mma N -- the group's heads, or (multi-query
+  // decode) nq query tokens x hpg heads; column h is token h / hpg, head h % hpg
   int B, Hq, Hkv, G, n_sink, n_recent, max_spans, cg;
+  int nq, hpg;
   float scale_log2;
   int fused;
   int rank_lim;                  // largest record rank the kernel instance handles (16 KS)

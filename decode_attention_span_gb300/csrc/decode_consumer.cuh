@@ -151,7 +151,7 @@ __device__ __forceinline__ void pair_masks(int base, int count, uint32_t& m0, ui
 //   S^T (16 keys x 8 heads) = K (16 x 128) q^T, then O^T += V^T P^T.
 __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
                                                const float* bias_row, float scale_log2,
-                                               int half) {
+                                               int half, const uint8_t* cmask_row = nullptr) {
   const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   const int krow = (lane & 7) + 8 * (mi & 1);
@@ -178,6 +178,16 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
   s[1] = v0 ? fmaf(s0[1] + s1[1], scale_log2, bias0) : kNegInf;
   s[2] = v1 ? fmaf(s0[2] + s1[2], scale_log2, bias1) : kNegInf;
   s[3] = v1 ? fmaf(s0[3] + s1[3], scale_log2, bias1) : kNegInf;
+  if (cmask_row != nullptr) {
+    // multi-query decode: a summary row is not seen by the columns (query
+    // tokens) that expand its span
+    const int c0 = 2 * (lane & 3);
+    const unsigned m0 = v0 ? cmask_row[g] : 0u, m1 = v1 ? cmask_row[g + 8] : 0u;
+    if ((m0 >> c0) & 1u) s[0] = kNegInf;
+    if ((m0 >> (c0 + 1)) & 1u) s[1] = kNegInf;
+    if ((m1 >> c0) & 1u) s[2] = kNegInf;
+    if ((m1 >> (c0 + 1)) & 1u) s[3] = kNegInf;
+  }
   rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
   uint32_t b0, b1;
   probs_to_b(A, s, b0, b1);
@@ -201,10 +211,10 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
 // eight lanes read eight different bank groups; the y reads are broadcasts.
 // Returns whether some head h of the group has z > theta_h for this lane's
 // span (rows past the page's spans are computed and ignored by the caller).
-__device__ __forceinline__ bool route32(const uint8_t* page, const float* ys, const float* theta,
-                                        int G) {
+__device__ __forceinline__ unsigned route32(const uint8_t* page, const float* ys,
+                                            const float* theta, int G) {
   const int lane = threadIdx.x & 31, sw = lane & 7;
-  bool hit = false;
+  unsigned hit = 0u;  // bit h: column h's logit passes its threshold
 #pragma unroll 1
   for (int h0 = 0; h0 < G; h0 += 4) {
     float z[4] = {0.f, 0.f, 0.f, 0.f};
@@ -220,7 +230,7 @@ __device__ __forceinline__ bool route32(const uint8_t* page, const float* ys, co
     }
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh)
-      if (h0 + hh < G) hit |= z[hh] > theta[h0 + hh];
+      if (h0 + hh < G && z[hh] > theta[h0 + hh]) hit |= 1u << (h0 + hh);
   }
   return hit;
 }
@@ -296,7 +306,8 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
 // memory and are masked, never multiplied.
 template <int KS>
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* uk,
-                                           const uint8_t* uv, int n, int rK, int rV) {
+                                           const uint8_t* uv, int n, int rK, int rV,
+                                           unsigned cm) {
   if (n <= 0) return;
   (void)rV;
   const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
@@ -319,6 +330,10 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
     }
     if (rb + g >= n) s[0] = s[1] = kNegInf;
     if (rb + g + 8 >= n) s[2] = s[3] = kNegInf;
+    // multi-query decode: only the columns (query tokens) that expand the
+    // span see its tokens
+    if (!((cm >> (2 * (lane & 3))) & 1u)) s[0] = s[2] = kNegInf;
+    if (!((cm >> (2 * (lane & 3) + 1)) & 1u)) s[1] = s[3] = kNegInf;
     const float2 alpha = rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
     if (alpha.x != 1.f || alpha.y != 1.f) {
 #pragma unroll

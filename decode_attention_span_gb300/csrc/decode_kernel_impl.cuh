@@ -81,7 +81,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
           Q.pk = 2;
           Q.pidx = e;
           Q.ppart = 0;
-          Q.pnp = record_parts(en.body, rK, rV);
+          Q.pnp = record_parts(en.body & 0xffff, rK, rV);
         } else {
           Q.rec_out = 1;
         }
@@ -125,11 +125,12 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
         bytes = full ? kFullPageBytes : kRowPageBytes;
       } else {
         const RecEntry en = ents[Q.pidx];
-        const int b = en.body, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
+        const int b = en.body & 0xffff, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
         const RecordLayout L = record_layout(b, rK, rV);
         roff = (int64_t(uint32_t(en.off_lo)) | (int64_t(en.off_hi) << 32));
         it.rk = rK;
         it.rv = rV;
+        it.cm = en.body >> 16;
         if (Q.pnp == 1) {
           it.type = IT_REC;
           it.n = b;
@@ -200,7 +201,8 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
                      P.scale_log2, kFullHalf);
   } else if (it.type == IT_SUM) {
     consume_rows16(A, bu, bu + 2 * kRowHalf, it.n, bias + (it.a - ms->ctx.k0), P.scale_log2,
-                   kRowHalf);
+                   kRowHalf,
+                   P.nq > 1 ? smem + kOffCmask + (it.a - ms->ctx.k0) : nullptr);
   } else {
     int off_key = -1, off_uk = 0, off_uv = 0, off_val = -1, n = 0;
     if (it.type == IT_REC) {
@@ -219,7 +221,7 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
       off_val = 0;
     }
     if (off_key >= 0) exp_key<KS>(A, X, base + off_key, it.rk, P.scale_log2);
-    if (n > 0) exp_tokens<KS>(A, X, base + off_uk, base + off_uv, n, it.rk, it.rv);
+    if (n > 0) exp_tokens<KS>(A, X, base + off_uk, base + off_uv, n, it.rk, it.rv, unsigned(it.cm));
     if (off_val >= 0) exp_value<KS>(A, X, base + off_val, it.rv);
   }
   return it.end;
@@ -266,22 +268,32 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   RecEntry* ents = reinterpret_cast<RecEntry*>(smem + kOffEntries);
   const int nd = ms->wq[w].nd;
   const int k0 = ms->ctx.k0, k1 = ms->ctx.k1;
-  bool hit = false, landed = false;
+  unsigned cols = 0u;  // the query columns whose gate logit passes their threshold
+  bool landed = false;
   int end = 0;
   if (ms->wq[w].ok) {
     landed = mbar_wait_parked(&ms->bar[w][nd % kSlots], uint32_t((nd / kSlots) & 1), P.wait_ns);
     if (landed) {
       const Item it = ms->desc[w][nd % kSlots];
       end = it.end;
-      hit = route32(smem + it.boff, ys, ms->theta, P.G);
+      cols = route32(smem + it.boff, ys, ms->theta, P.G);
     } else if (lane == 0) {
       set_device_error(P.status, DEV_WAIT_TIMEOUT, 5);
     }
   }
+  // a query token expands the span if any of its heads does (the union over
+  // the group); its columns then see the reconstructed tokens and not the
+  // summary
+  const unsigned tok = (1u << P.hpg) - 1u, all = (1u << P.G) - 1u;
+  unsigned cm = 0u;
+  for (int i = 0; i < P.nq; ++i)
+    if ((cols >> (i * P.hpg)) & tok) cm |= tok << (i * P.hpg);
   const int k = k0 + kRouteSpans * p + lane;
   const bool valid = k < k1;
-  const bool ex = valid && body > 0 && hit;
-  if (valid) bias[k - k0] = (body > 0 && !ex) ? log2f(float(body)) : kNegInf;
+  if (!(valid && body > 0)) cm = 0u;
+  const bool ex = cm != 0u;
+  if (valid) bias[k - k0] = (body > 0 && cm != all) ? log2f(float(body)) : kNegInf;
+  if (valid && P.nq > 1) smem[kOffCmask + (k - k0)] = uint8_t(cm);
   const uint32_t bal = __ballot_sync(kFull, ex);
   int base = 0;
   if (lane == 0) {
@@ -293,7 +305,7 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
     RecEntry en;
     en.off_lo = int(uint32_t(off));
     en.off_hi = int(off >> 32);
-    en.body = body;
+    en.body = body | int(cm << 16);
     en.rank = rank;
     ents[base + __popc(bal & ((1u << lane) - 1u))] = en;
   }
@@ -343,12 +355,14 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     // them as f32 for the routing projection and as the bf16 pairs of the
     // query's mma A fragments (rows 0..7 = heads, grouped by 32 dims: pair
     // (h, 32 i + 8 k + 2 j) is component k of lane 4 h + j's fragment i).
+    // (column h: query token h / hpg, head h % hpg; q is [B][nq][Hq][128])
     const int h = tid >> 5, d = 4 * (tid & 31);
     uint2 u = make_uint2(0u, 0u);
     if (h < G)
-      u = *reinterpret_cast<const uint2*>(P.q + (size_t(C.b) * P.Hq + size_t(C.c) * G + h) *
-                                                    kHeadDim + d);
-    const float th = (P.fused && tid < G) ? P.theta[C.c * G + tid] : 0.f;
+      u = *reinterpret_cast<const uint2*>(
+          P.q + ((size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg) *
+                    kHeadDim + d);
+    const float th = (P.fused && tid < G) ? P.theta[C.c * P.hpg + tid % P.hpg] : 0.f;
     const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     *reinterpret_cast<float4*>(qf + h * kHeadDim + d) = make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -431,7 +445,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
           RecEntry en;
           en.off_lo = int(uint32_t(off));
           en.off_hi = int(off >> 32);
-          en.body = body;
+          en.body = body | int(((1u << P.G) - 1u) << 16);  // every column
           en.rank = rank;
           ents[atomicAdd(&ms->n_rec, 1)] = en;
         }
@@ -636,7 +650,8 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     const int h = hsel + 2 * i;
     if (h < G) {
       const float L = MLa[8 + h];
-      const size_t row = size_t(C.b) * P.Hq + size_t(C.c) * G + h;
+      const size_t row =
+          (size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg;
       P.out[row * kHeadDim + d] = L > 0.f ? Oh[i] / L : 0.f;
       if (d == 0 && P.lse != nullptr) P.lse[row] = L > 0.f ? (MLa[h] + log2f(L)) * kLn2 : kNegInf;
     }

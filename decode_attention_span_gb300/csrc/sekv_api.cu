@@ -259,6 +259,8 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.Hq = cfg->n_q_heads;
   P.Hkv = cfg->n_kv_heads;
   P.G = cfg->n_q_heads / cfg->n_kv_heads;
+  P.nq = 1;
+  P.hpg = P.G;
   P.n_sink = cfg->n_sink;
   P.n_recent = cfg->n_recent;
   P.max_spans = cfg->max_spans;
@@ -307,14 +309,17 @@ sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_
 
 }  // namespace sekv
 
-extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
-                                        const void* q, const float* W_r, const float* theta,
-                                        float scale, float* out, float* lse, int32_t* expanded,
-                                        int32_t* n_expanded, void* workspace,
-                                        size_t workspace_bytes, cudaStream_t stream) {
+namespace {
+sekv_status decode_step_impl(const sekv_config* cfg, const sekv_layer_cache* cache,
+                             const void* q, int n_q, const float* W_r, const float* theta,
+                             float scale, float* out, float* lse, int32_t* expanded,
+                             int32_t* n_expanded, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
   reset_launches();
   sekv_status why;
   if (!config_ok(cfg, &why)) return why;
+  const int hpg = cfg->n_q_heads / cfg->n_kv_heads;
+  if (n_q < 1 || n_q * hpg > 8) return SEKV_ERR_UNSUPPORTED;
   sekv_status st = check_cache(cfg, cache, true);
   if (st != SEKV_OK) return st;
   if (!q || !W_r || !theta || !out || !workspace || !cache->s_route) return SEKV_ERR_INVALID;
@@ -328,6 +333,8 @@ extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer
   memset(&P, 0, sizeof(P));
   st = fill_decode_params(cfg, cache, L, workspace, P, true);
   if (st != SEKV_OK) return st;
+  P.nq = n_q;
+  P.G = n_q * hpg;
   P.store = static_cast<const uint8_t*>(cache->store);
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.W_r = W_r;
@@ -338,6 +345,27 @@ extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer
   P.n_expanded_out = n_expanded;
   P.scale_log2 = scale * kLog2e;
   return launch_decode(P, L, cfg, stream, (cfg->flags & SEKV_FLAG_OVERLAP_PREVIOUS) != 0);
+}
+}  // namespace
+
+extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                        const void* q, const float* W_r, const float* theta,
+                                        float scale, float* out, float* lse, int32_t* expanded,
+                                        int32_t* n_expanded, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  return decode_step_impl(cfg, cache, q, 1, W_r, theta, scale, out, lse, expanded, n_expanded,
+                          workspace, workspace_bytes, stream);
+}
+
+extern "C" sekv_status sekv_decode_step_multi(const sekv_config* cfg,
+                                              const sekv_layer_cache* cache, const void* q,
+                                              int32_t n_q, const float* W_r, const float* theta,
+                                              float scale, float* out, float* lse,
+                                              int32_t* expanded, int32_t* n_expanded,
+                                              void* workspace, size_t workspace_bytes,
+                                              cudaStream_t stream) {
+  return decode_step_impl(cfg, cache, q, n_q, W_r, theta, scale, out, lse, expanded, n_expanded,
+                          workspace, workspace_bytes, stream);
 }
 
 extern "C" sekv_status sekv_decode_attention(const sekv_config* cfg,

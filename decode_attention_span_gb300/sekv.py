@@ -30,7 +30,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 # every symbol include/sekv.h declares
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
-           "sekv_decode_step", "sekv_decode_step_noalloc", "sekv_noalloc_status",
+           "sekv_decode_step", "sekv_decode_step_multi", "sekv_decode_step_noalloc",
+           "sekv_noalloc_status",
            "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
            "sekv_fetch_bases_cached", "sekv_build_flops", "sekv_maint_state_size",
@@ -134,6 +135,11 @@ def lib() -> ctypes.CDLL:
         L.sekv_decode_step.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_sz, _c_vp]
+        L.sekv_decode_step_multi.restype = _c_i32
+        L.sekv_decode_step_multi.argtypes = [ctypes.POINTER(SekvConfig),
+                                             ctypes.POINTER(SekvLayerCache), _c_vp, _c_i32,
+                                             _c_vp, _c_vp, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
+                                             _c_vp, _c_sz, _c_vp]
         L.sekv_decode_step_noalloc.restype = _c_i32
         L.sekv_decode_step_noalloc.argtypes = [ctypes.POINTER(SekvConfig),
                                                ctypes.POINTER(SekvLayerCache), _c_vp, _c_vp,
@@ -332,6 +338,33 @@ def decode_step(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float, ws:
                                   _ptr(theta), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(expanded), _ptr(n_expanded), ws.ptr(), ws.nbytes,
                                   _stream(stream)))
+    return out, lse, expanded, n_expanded
+
+
+def decode_step_multi(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float,
+                      ws: Workspace, out=None, lse=None, want_list: bool = False, stream=None):
+    """sekv_decode_step_multi: q [B][n_q][Hq][128] bf16, n_q query tokens per
+    sequence over the same cache; returns out [B][n_q][Hq][128], lse, and the
+    union expansion list and counts when want_list."""
+    _need(q, "q", torch.bfloat16); _need(W_r, "W_r", torch.float32)
+    _need(theta, "theta", torch.float32)
+    B, n_q = q.shape[0], q.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty(B, n_q, cfg.n_q_heads, 128, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(B, n_q, cfg.n_q_heads, dtype=torch.float32, device=dev)
+    NG = cfg.batch * cfg.n_kv_heads
+    expanded = n_expanded = None
+    if want_list:
+        expanded = torch.zeros(NG * cfg.max_spans, dtype=torch.int32, device=dev)
+        n_expanded = torch.zeros(NG, dtype=torch.int32, device=dev)
+    c = cfg.c()
+    _check("sekv_decode_step_multi",
+           lib().sekv_decode_step_multi(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q), n_q,
+                                        _ptr(W_r), _ptr(theta), float(scale), _ptr(out),
+                                        _ptr(lse), _ptr(expanded), _ptr(n_expanded), ws.ptr(),
+                                        ws.nbytes, _stream(stream)))
     return out, lse, expanded, n_expanded
 
 

@@ -352,6 +352,28 @@ sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cac
                              cudaStream_t stream);
 
 /*
+ * sekv_decode_step_multi -- sekv_decode_step for n_q query tokens per
+ * sequence over the same cache (for example the draft tokens of speculative
+ * decoding, or queries that share one prefix).  Each query token routes and
+ * attends on its own, as [DE]/[ZH] Methodik 3 describe for one query: its
+ * expansion set is the union over its GQA group's heads, its expanded spans
+ * contribute their reconstructed tokens and its other spans their summaries.
+ * The tokens share one pass over the cache: the union of their expansion
+ * sets is loaded once, and each (token, head) pair is one column of the
+ * kernel's tensor-core tiles, so n_q * (n_q_heads / n_kv_heads) <= 8 (else
+ * SEKV_ERR_UNSUPPORTED).
+ *   q    bf16 [B][n_q][Hq][128];  out f32 [B][n_q][Hq][128];  lse f32
+ *        [B][n_q][Hq] (nullable); theta, W_r, workspace and the optional
+ *        expansion list (the union over the tokens) as sekv_decode_step.
+ * n_q = 1 is sekv_decode_step.
+ */
+sekv_status sekv_decode_step_multi(const sekv_config* cfg, const sekv_layer_cache* cache,
+                                   const void* q, int32_t n_q, const float* W_r,
+                                   const float* theta, float scale, float* out, float* lse,
+                                   int32_t* expanded, int32_t* n_expanded, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * sekv_decode_step_noalloc -- sekv_decode_step without a caller workspace.
  * The SeKV pages have no counterpart for this call; it exists for callers
  * that cannot allocate device memory and have no spare buffer to lend: for
