@@ -55,10 +55,11 @@ def parse():
     ap.add_argument("--traffic-workload", default="llama3_8b_128k")
     ap.add_argument("--traffic-scale", type=float, default=1.0)
     ap.add_argument("--traffic-command", default="")
-    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv", "append"],
+    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv", "append", "multi"],
                     help="decode: the headline decode step; build: the prefill cache build; "
                          "fullkv: the same decode step over a full-KV cache (comparator); "
-                         "append: decode-time cache maintenance, one token per step")
+                         "append: decode-time cache maintenance, one token per step; "
+                         "multi: two query tokens per sequence in one pass")
     return ap.parse_args()
 
 
@@ -1000,6 +1001,90 @@ def run_build_bench(args, ws_n, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_multi_bench(args, ws_n, rank, local):
+    """Multi-query decode at 128K (Llama-3-8B shape): two query tokens per
+    sequence over the same cache (sekv_decode_step_multi: each token routes
+    and attends on its own; the union of their expansion sets is loaded once
+    and each (token, head) pair is a column of the tensor-core tiles), 32
+    layers in one CUDA graph.  Reported as query tokens/s, with the one-query
+    step of the same run beside it."""
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (multi) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.get_config(args.config, **({"layers": args.layers} if args.layers else {}))
+    nq = 2
+    cfg, ws, layers = build_workload(sk, w, dev, w.layers)
+    B, Hkv, ms = cfg.batch, cfg.n_kv_heads, cfg.max_spans
+    for l, L in enumerate(layers):
+        g = gen._gen(w.seed * 4099 + 17 * l + 3, dev)
+        q2 = gen.query(g, w.batch, w.n_q_heads, dev)
+        L["qm"] = torch.stack([L["q"], q2], 1).contiguous()
+        L["outm"] = torch.empty(w.batch, nq, w.n_q_heads, 128, device=dev)
+        L["lsem"] = torch.empty(w.batch, nq, w.n_q_heads, device=dev)
+        sets = []
+        for i in range(nq):
+            lst, cnt, _ = sk.route(cfg, L["cache"], L["qm"][:, i].contiguous(), L["W"], L["theta"], ws)
+            lst, cnt = lst.view(B * Hkv, ms).cpu().numpy(), cnt.cpu().numpy()
+            sets.append([set(lst[gi, :cnt[gi]].tolist()) for gi in range(B * Hkv)])
+        union = [sorted(set().union(*[st[gi] for st in sets])) for gi in range(B * Hkv)]
+        both = sum(len(set.intersection(*[st[gi] for st in sets])) for gi in range(B * Hkv))
+        ulst = torch.zeros(B * Hkv, ms, dtype=torch.int32)
+        ucnt = torch.zeros(B * Hkv, dtype=torch.int32)
+        for gi, u in enumerate(union):
+            ulst[gi, :len(u)] = torch.tensor(u, dtype=torch.int32)
+            ucnt[gi] = len(u)
+        # the union's factors, and the summaries of every span that some token
+        # does not expand (expanded by all tokens: no summary)
+        L["bytes_m"] = (algorithmic_bytes(L["t"], ulst.to(dev), ucnt.to(dev), cfg)
+                        + 512 * (int(ucnt.sum()) - both))
+        L["union_frac"] = int(ucnt.sum()) / max(L["n_nonempty"], 1)
+    scale = sk.default_scale()
+
+    def step_m():
+        for L in layers:
+            sk.decode_step_multi(cfg, L["cache"], L["qm"], L["W"], L["theta"], scale, ws,
+                                 out=L["outm"], lse=L["lsem"])
+
+    def step_1():
+        for L in layers:
+            sk.decode_step(cfg, L["cache"], L["q"], L["W"], L["theta"], scale, ws,
+                           out=L["out"], lse=L["lse"])
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    ms_m, ck = time_graph(step_m, args.steps, args.warmup, torch.cuda.Stream(), ws_n, clocks)
+    ms_1, _ = time_graph(step_1, args.steps, args.warmup, torch.cuda.Stream(), ws_n, None)
+    ws.raise_on_error()
+    ms_m = max_over_ranks(ms_m, ws_n)
+    ms_1 = max_over_ranks(ms_1, ws_n)
+    if rank != 0:
+        return
+    per_launch = ms_m / 1e3 / args.steps / len(layers)
+    nbytes = sum(L["bytes_m"] for L in layers) / len(layers)
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / per_launch / 1e9
+    line = {"metric": "multi-query decode: query tokens/s at 128K ctx (2 tokens per sequence "
+                      "over one cache, one pass)",
+            "value": whole_job_rate(args.steps, ms_m, ws_n) * nq * w.batch, "unit": "tokens/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_m / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "layers": len(layers), "batch": w.batch,
+                       "ctx": w.ctx, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                       "query_tokens": nq, "columns": nq * w.n_q_heads // w.n_kv_heads,
+                       "union_expand_frac": float(np.mean([L["union_frac"] for L in layers])),
+                       "graph": "one CUDA graph per step, programmatic dependent launch"},
+            "one_query_ms_per_step": ms_1 / args.steps,
+            "one_query_tokens_per_s": whole_job_rate(args.steps, ms_1, ws_n) * w.batch,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "sekv::decode_kernel", "bytes_per_launch": nbytes,
+                         "avg_launch_us": per_launch * 1e6},
+            "clocks": ck, "gpu_launches": args.steps * len(layers)}
+    print(json.dumps(line), flush=True)
+
+
 def run_fullkv_bench(args, ws_n, rank, local):
     """Full-KV comparator at the headline shape: the same decode step over a
     cache with no spans, every one of the 128K context tokens a full-resolution
@@ -1072,6 +1157,8 @@ def main():
         return
     if args.path == "append":
         return run_append_bench(args, ws_n, rank, local)
+    if args.path == "multi":
+        return run_multi_bench(args, ws_n, rank, local)
     if args.path == "build":
         run_build_bench(args, ws_n, rank, local)
         return
