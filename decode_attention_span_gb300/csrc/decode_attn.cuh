@@ -89,12 +89,11 @@ enum ItemType : int {
 struct Item {      // one landed (or landing) work item of a warp, 32 bytes
   int type;
   int n;           // rows / spans / tokens of a U tile / body of a record
-  int a;           // first row / first span / first token of a U tile
+  int a;           // first row / first span; records: the query columns that expand the span
   int rk, rv;      // record ranks
   int boff;        // byte offset of the item's data from the CTA's arena base
   int end;         // the warp's arena granule counter at the item's end
   int uv;          // IT_UT: byte offset of the U_V rows from the item's data
-  int cm;          // records: the query columns that expand the span (bit per column)
 };
 
 struct RecEntry {  // one expanded span of the CTA, 16 bytes
@@ -136,14 +135,17 @@ struct DecodeParams {
   unsigned long long wait_ns;    // limit of a parked wait for an item (SEKV_FLAG_SHORT_WAITS: 0)
 };
 
-template <int KS>
+// KS: rank k-steps of 16 (ranks up to 16 KS); MQ: multi-query decode (query
+// columns of several tokens, per-token expansion masks), a separate instance
+// so that the one-token step carries none of its masking
+template <int KS, bool MQ>
 __global__ void decode_kernel(const __grid_constant__ DecodeParams P);
 
 // Host-side handles of the decode kernel instances (ranks up to 16 KS).
-const void* decode_kernel_fn_ks1();
-const void* decode_kernel_fn_ks2();
-const void* decode_kernel_fn_ks3();
-const void* decode_kernel_fn_ks4();
+const void* decode_kernel_fn_ks1(bool mq);
+const void* decode_kernel_fn_ks2(bool mq);
+const void* decode_kernel_fn_ks3(bool mq);
+const void* decode_kernel_fn_ks4(bool mq);
 
 // Span share [k0, k1) of CTA j of cg.  Boundaries are rounded up to
 // multiples of 8 so that every per-span array slice starts 16-byte aligned.

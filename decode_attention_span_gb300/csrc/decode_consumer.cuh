@@ -149,9 +149,10 @@ __device__ __forceinline__ void pair_masks(int base, int count, uint32_t& m0, ui
 // the logit bias of the page's spans (log2|S|, or -inf for a span that does
 // not enter as a summary); nullptr for full rows.  Rows >= n are masked.
 //   S^T (16 keys x 8 heads) = K (16 x 128) q^T, then O^T += V^T P^T.
+template <bool MQ>
 __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
                                                const float* bias_row, float scale_log2,
-                                               int half, const uint8_t* cmask_row = nullptr) {
+                                               int half, const uint8_t* cmask_row) {
   const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   const int krow = (lane & 7) + 8 * (mi & 1);
@@ -178,7 +179,7 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
   s[1] = v0 ? fmaf(s0[1] + s1[1], scale_log2, bias0) : kNegInf;
   s[2] = v1 ? fmaf(s0[2] + s1[2], scale_log2, bias1) : kNegInf;
   s[3] = v1 ? fmaf(s0[3] + s1[3], scale_log2, bias1) : kNegInf;
-  if (cmask_row != nullptr) {
+  if (MQ) {
     // multi-query decode: a summary row is not seen by the columns (query
     // tokens) that expand its span
     const int c0 = 2 * (lane & 3);
@@ -304,7 +305,7 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
 // token that is a multiple of 16), one pass of 16-token tiles with lazy
 // re-basing.  Rows or ranks past the valid ones read neighbouring shared
 // memory and are masked, never multiplied.
-template <int KS>
+template <int KS, bool MQ>
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* uk,
                                            const uint8_t* uv, int n, int rK, int rV,
                                            unsigned cm) {
@@ -332,8 +333,10 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
     if (rb + g + 8 >= n) s[2] = s[3] = kNegInf;
     // multi-query decode: only the columns (query tokens) that expand the
     // span see its tokens
-    if (!((cm >> (2 * (lane & 3))) & 1u)) s[0] = s[2] = kNegInf;
-    if (!((cm >> (2 * (lane & 3) + 1)) & 1u)) s[1] = s[3] = kNegInf;
+    if (MQ) {
+      if (!((cm >> (2 * (lane & 3))) & 1u)) s[0] = s[2] = kNegInf;
+      if (!((cm >> (2 * (lane & 3) + 1)) & 1u)) s[1] = s[3] = kNegInf;
+    }
     const float2 alpha = rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
     if (alpha.x != 1.f || alpha.y != 1.f) {
 #pragma unroll

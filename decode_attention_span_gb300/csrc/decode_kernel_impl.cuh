@@ -130,7 +130,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
         roff = (int64_t(uint32_t(en.off_lo)) | (int64_t(en.off_hi) << 32));
         it.rk = rK;
         it.rv = rV;
-        it.cm = en.body >> 16;
+        it.a = en.body >> 16;  // the query columns that expand the span
         if (Q.pnp == 1) {
           it.type = IT_REC;
           it.n = b;
@@ -142,7 +142,6 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
           const int rows = split_rows(rK, rV);
           const int i0 = (Q.ppart - 1) * rows;
           it.type = IT_UT;
-          it.a = i0;
           it.n = (b - i0) < rows ? (b - i0) : rows;
           it.uv = 2 * it.n * r8(rK);
           s0 = L.uk + 2 * int64_t(i0) * r8(rK);
@@ -185,7 +184,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
 }
 
 // Consume the warp's item nd (landed); returns its end in the arena.
-template <int KS>
+template <int KS, bool MQ>
 __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
                                             const DecodeParams& P, int nd, WarpAcc& A,
                                             ExpAcc<KS>& X) {
@@ -197,12 +196,11 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
   if (it.type == IT_FULL) {
     // two 16-row tiles (the second one only if the page has rows there)
     for (int t0 = 0; t0 < it.n; t0 += kRows)
-      consume_rows16(A, bu + t0 * 128, bu + 2 * kFullHalf + t0 * 128, it.n - t0, nullptr,
-                     P.scale_log2, kFullHalf);
+      consume_rows16<false>(A, bu + t0 * 128, bu + 2 * kFullHalf + t0 * 128, it.n - t0,
+                            nullptr, P.scale_log2, kFullHalf, nullptr);
   } else if (it.type == IT_SUM) {
-    consume_rows16(A, bu, bu + 2 * kRowHalf, it.n, bias + (it.a - ms->ctx.k0), P.scale_log2,
-                   kRowHalf,
-                   P.nq > 1 ? smem + kOffCmask + (it.a - ms->ctx.k0) : nullptr);
+    consume_rows16<MQ>(A, bu, bu + 2 * kRowHalf, it.n, bias + (it.a - ms->ctx.k0),
+                       P.scale_log2, kRowHalf, smem + kOffCmask + (it.a - ms->ctx.k0));
   } else {
     int off_key = -1, off_uk = 0, off_uv = 0, off_val = -1, n = 0;
     if (it.type == IT_REC) {
@@ -221,7 +219,7 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
       off_val = 0;
     }
     if (off_key >= 0) exp_key<KS>(A, X, base + off_key, it.rk, P.scale_log2);
-    if (n > 0) exp_tokens<KS>(A, X, base + off_uk, base + off_uv, n, it.rk, it.rv, unsigned(it.cm));
+    if (n > 0) exp_tokens<KS, MQ>(A, X, base + off_uk, base + off_uv, n, it.rk, it.rv, unsigned(it.a));
     if (off_val >= 0) exp_value<KS>(A, X, base + off_val, it.rv);
   }
   return it.end;
@@ -260,6 +258,7 @@ __device__ __forceinline__ void issue_route_page(uint8_t* smem, SmemMisc* ms,
 
 // Routing page p of this CTA (fused mode), landed as the warp's next item:
 // expansion decisions for its spans, their summary biases and record entries.
+template <bool MQ>
 __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
                                            int p, int body, int rank, long long off) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -284,16 +283,20 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   // a query token expands the span if any of its heads does (the union over
   // the group); its columns then see the reconstructed tokens and not the
   // summary
-  const unsigned tok = (1u << P.hpg) - 1u, all = (1u << P.G) - 1u;
-  unsigned cm = 0u;
-  for (int i = 0; i < P.nq; ++i)
-    if ((cols >> (i * P.hpg)) & tok) cm |= tok << (i * P.hpg);
+  const unsigned all = (1u << P.G) - 1u;
+  unsigned cm = cols != 0u ? all : 0u;  // one token: every column or none
+  if (MQ) {
+    const unsigned tok = (1u << P.hpg) - 1u;
+    cm = 0u;
+    for (int i = 0; i < P.nq; ++i)
+      if ((cols >> (i * P.hpg)) & tok) cm |= tok << (i * P.hpg);
+  }
   const int k = k0 + kRouteSpans * p + lane;
   const bool valid = k < k1;
   if (!(valid && body > 0)) cm = 0u;
   const bool ex = cm != 0u;
   if (valid) bias[k - k0] = (body > 0 && cm != all) ? log2f(float(body)) : kNegInf;
-  if (valid && P.nq > 1) smem[kOffCmask + (k - k0)] = uint8_t(cm);
+  if (MQ && valid) smem[kOffCmask + (k - k0)] = uint8_t(cm);
   const uint32_t bal = __ballot_sync(kFull, ex);
   int base = 0;
   if (lane == 0) {
@@ -318,7 +321,7 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   __syncwarp();
 }
 
-template <int KS>
+template <int KS, bool MQ>
 __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const DecodeParams& P,
                                            const float4 (&wr)[8]) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -358,11 +361,10 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     // (column h: query token h / hpg, head h % hpg; q is [B][nq][Hq][128])
     const int h = tid >> 5, d = 4 * (tid & 31);
     uint2 u = make_uint2(0u, 0u);
-    if (h < G)
-      u = *reinterpret_cast<const uint2*>(
-          P.q + ((size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg) *
-                    kHeadDim + d);
-    const float th = (P.fused && tid < G) ? P.theta[C.c * P.hpg + tid % P.hpg] : 0.f;
+    const int hq = MQ ? (C.b * P.nq + h / P.hpg) * P.Hq + C.c * P.hpg + h % P.hpg
+                      : C.b * P.Hq + C.c * G + h;
+    if (h < G) u = *reinterpret_cast<const uint2*>(P.q + size_t(hq) * kHeadDim + d);
+    const float th = (P.fused && tid < G) ? P.theta[C.c * P.hpg + (MQ ? tid % P.hpg : tid)] : 0.f;
     const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     *reinterpret_cast<float4*>(qf + h * kHeadDim + d) = make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -410,7 +412,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int p = w + kWarps * i;
-      if (p < C.n_rp) route_page(smem, ms, P, p, rbody[i], rrank[i], roff[i]);
+      if (p < C.n_rp) route_page<MQ>(smem, ms, P, p, rbody[i], rrank[i], roff[i]);
     }
   } else {
     // list mode: this CTA's expanded spans from the caller's ascending list
@@ -504,7 +506,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
       __syncwarp();
       break;
     }
-    const int end = consume_item<KS>(smem, ms, P, nd, A, X);
+    const int end = consume_item<KS, MQ>(smem, ms, P, nd, A, X);
     retire_item(ms, nd, end);
   }
   // after a timeout: every issued copy lands before the arena is reused
@@ -650,8 +652,8 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     const int h = hsel + 2 * i;
     if (h < G) {
       const float L = MLa[8 + h];
-      const size_t row =
-          (size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg;
+      const size_t row = MQ ? (size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg
+                            : size_t(C.b) * P.Hq + size_t(C.c) * G + h;
       P.out[row * kHeadDim + d] = L > 0.f ? Oh[i] / L : 0.f;
       if (d == 0 && P.lse != nullptr) P.lse[row] = L > 0.f ? (MLa[h] + log2f(L)) * kLn2 : kNegInf;
     }
@@ -686,7 +688,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
 }
 
 // grid: (cg, Hkv, B); block: 8 warps, each its own producer and consumer
-template <int KS>
+template <int KS, bool MQ>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -741,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   pdl_launch_dependents();
-  run_decode<KS>(smem, ms, P, wr);
+  run_decode<KS, MQ>(smem, ms, P, wr);
 }
 
 }  // namespace sekv

@@ -3,8 +3,12 @@
 
 namespace sekv {
 
-template __global__ void decode_kernel<1>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<1, false>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<1, true>(const __grid_constant__ DecodeParams P);
 
-const void* decode_kernel_fn_ks1() { return reinterpret_cast<const void*>(&decode_kernel<1>); }
+const void* decode_kernel_fn_ks1(bool mq) {
+  return mq ? reinterpret_cast<const void*>(&decode_kernel<1, true>)
+            : reinterpret_cast<const void*>(&decode_kernel<1, false>);
+}
 
 }  // namespace sekv

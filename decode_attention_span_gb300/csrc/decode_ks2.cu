@@ -3,8 +3,12 @@
 
 namespace sekv {
 
-template __global__ void decode_kernel<2>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<2, false>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<2, true>(const __grid_constant__ DecodeParams P);
 
-const void* decode_kernel_fn_ks2() { return reinterpret_cast<const void*>(&decode_kernel<2>); }
+const void* decode_kernel_fn_ks2(bool mq) {
+  return mq ? reinterpret_cast<const void*>(&decode_kernel<2, true>)
+            : reinterpret_cast<const void*>(&decode_kernel<2, false>);
+}
 
 }  // namespace sekv

@@ -3,8 +3,12 @@
 
 namespace sekv {
 
-template __global__ void decode_kernel<3>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<3, false>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<3, true>(const __grid_constant__ DecodeParams P);
 
-const void* decode_kernel_fn_ks3() { return reinterpret_cast<const void*>(&decode_kernel<3>); }
+const void* decode_kernel_fn_ks3(bool mq) {
+  return mq ? reinterpret_cast<const void*>(&decode_kernel<3, true>)
+            : reinterpret_cast<const void*>(&decode_kernel<3, false>);
+}
 
 }  // namespace sekv

@@ -3,8 +3,12 @@
 
 namespace sekv {
 
-template __global__ void decode_kernel<4>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<4, false>(const __grid_constant__ DecodeParams P);
+template __global__ void decode_kernel<4, true>(const __grid_constant__ DecodeParams P);
 
-const void* decode_kernel_fn_ks4() { return reinterpret_cast<const void*>(&decode_kernel<4>); }
+const void* decode_kernel_fn_ks4(bool mq) {
+  return mq ? reinterpret_cast<const void*>(&decode_kernel<4, true>)
+            : reinterpret_cast<const void*>(&decode_kernel<4, false>);
+}
 
 }  // namespace sekv

@@ -278,17 +278,19 @@ int decode_ks(const sekv_config* cfg) {
 
 sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_config* cfg,
                           cudaStream_t stream, bool overlap) {
-  static const void* const fns[4] = {decode_kernel_fn_ks1(), decode_kernel_fn_ks2(),
-                                     decode_kernel_fn_ks3(), decode_kernel_fn_ks4()};
-  static std::once_flag once[4];
-  static cudaError_t attr_err[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
+  static const void* const fns[8] = {
+      decode_kernel_fn_ks1(false), decode_kernel_fn_ks2(false), decode_kernel_fn_ks3(false),
+      decode_kernel_fn_ks4(false), decode_kernel_fn_ks1(true),  decode_kernel_fn_ks2(true),
+      decode_kernel_fn_ks3(true),  decode_kernel_fn_ks4(true)};
+  static std::once_flag once[8];
+  static cudaError_t attr_err[8] = {};
   const int ks = decode_ks(cfg);
-  const void* fn = fns[ks - 1];
-  std::call_once(once[ks - 1], [&] {
-    attr_err[ks - 1] =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  const int fi = ks - 1 + (P0.nq > 1 ? 4 : 0);
+  const void* fn = fns[fi];
+  std::call_once(once[fi], [&] {
+    attr_err[fi] = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   });
-  if (attr_err[ks - 1] != cudaSuccess) return SEKV_ERR_CUDA;
+  if (attr_err[fi] != cudaSuccess) return SEKV_ERR_CUDA;
   DecodeParams P = P0;
   P.rank_lim = 16 * ks;
   cudaLaunchConfig_t lc{};
