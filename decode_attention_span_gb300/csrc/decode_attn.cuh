@@ -37,7 +37,7 @@ namespace sekv {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGran = 1024;                   // arena granule (TMA swizzle alignment)
-constexpr int kArenaGran = 24;                // arena of one warp, in granules
+constexpr int kArenaGran = 25;                // arena of one warp, in granules
 constexpr int kArenaBytes = kArenaGran * kGran;
 constexpr int kMaxItems = 2;                  // items in flight per warp (main loop)
 constexpr int kSlots = 4;                     // item slots (descriptor + mbarrier) per warp
