@@ -51,8 +51,8 @@ constexpr int kRouteSpans = 32;               // spans per routing page
 constexpr int kRoutePageBytes = kRouteSpans * 256;  // 8 KB
 constexpr int kSpanCap = 512;                 // spans of one CTA (bias cache, entries)
 constexpr int kMaxRoutePages = kSpanCap / kRouteSpans;
-constexpr int kWholeMax = 20480;              // records up to this size land whole
-constexpr int kTileMax = 12288;               // U-row tiles of larger records
+constexpr int kWholeMax = 25600;              // records up to this size land whole (a whole arena)
+constexpr int kTileMax = 24576;               // U-row tiles of larger records
 constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) group
 constexpr int kStaticPages = 1;               // full-resolution pages each CTA owns
 constexpr int kPoolClaim = 1;                 // pages per claim from the group's pool
