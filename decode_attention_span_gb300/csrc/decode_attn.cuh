@@ -199,7 +199,8 @@ struct SmemMisc {
   uint64_t cmb_bar;        // last CTA of a group: a chunk of partials landed
   unsigned int pmask[kMaxRoutePages];  // fused: expanded spans per routing page
   float theta[8];
-  int n_rec;               // expanded records of this CTA
+  int n_front;             // expanded records in parts, from the front of the entries
+  int n_back;              // the other expanded records, from the back of the entries
   int rec_next;            // record queue head
   int fixed_next;          // fixed-page queue head
   int is_last;
@@ -222,6 +223,12 @@ __host__ __device__ inline int record_parts(int b, int rK, int rV) {
   if (record_bytes(b, rK, rV) <= kWholeMax) return 1;
   const int rows = split_rows(rK, rV);
   return 2 + (b + rows - 1) / rows;
+}
+
+// Entry slot of the e-th record of a CTA's queue: the n_front records in
+// parts first (from the front of the entries), then the others (from the back).
+__host__ __device__ inline int rec_slot(int e, int n_front) {
+  return e < n_front ? e : kSpanCap - 1 - (e - n_front);
 }
 
 }  // namespace sekv

@@ -205,6 +205,65 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
   }
 }
 
+// A page of 32 full-resolution rows (two 16-row tiles, laid out as for
+// consume_rows16, the second 16 rows after the first), folded into the
+// warp's softmax state at once: the two tiles' logit products run as
+// independent chains, and the page takes at most one rescale.  Rows >= n are
+// masked.
+__device__ __forceinline__ void consume_rows32(WarpAcc& A, uint32_t kb, uint32_t vb, int n,
+                                               float scale_log2, int half) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // rows 0-15
+  float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};  // rows 16-31
+  const int krow = (lane & 7) + 8 * (mi & 1);
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {  // head dims 32 i .. 32 i + 31: k-steps 2 i, 2 i + 1
+    const uint4 qv = lds128(A.qfrag + (i * 32 + lane) * 16);
+    const uint32_t box = kb + (i >> 1) * half;
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(swz128(box, krow, 4 * (i & 1) + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s0, a0, a1, a2, a3, qv.x, qv.y);
+    ldsm_x4(swz128(box, krow + 16, 4 * (i & 1) + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(u0, a0, a1, a2, a3, qv.x, qv.y);
+    ldsm_x4(swz128(box, krow, 4 * (i & 1) + 2 + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s1, a0, a1, a2, a3, qv.z, qv.w);
+    ldsm_x4(swz128(box, krow + 16, 4 * (i & 1) + 2 + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(u1, a0, a1, a2, a3, qv.z, qv.w);
+  }
+  const bool v0 = g < n, v1 = g + 8 < n, v2 = g + 16 < n, v3 = g + 24 < n;
+  float s[4], u[4];
+  s[0] = v0 ? (s0[0] + s1[0]) * scale_log2 : kNegInf;
+  s[1] = v0 ? (s0[1] + s1[1]) * scale_log2 : kNegInf;
+  s[2] = v1 ? (s0[2] + s1[2]) * scale_log2 : kNegInf;
+  s[3] = v1 ? (s0[3] + s1[3]) * scale_log2 : kNegInf;
+  u[0] = v2 ? (u0[0] + u1[0]) * scale_log2 : kNegInf;
+  u[1] = v2 ? (u0[1] + u1[1]) * scale_log2 : kNegInf;
+  u[2] = v3 ? (u0[2] + u1[2]) * scale_log2 : kNegInf;
+  u[3] = v3 ? (u0[3] + u1[3]) * scale_log2 : kNegInf;
+  rebase_if_needed(A, fmaxf(fmaxf(s[0], s[2]), fmaxf(u[0], u[2])),
+                   fmaxf(fmaxf(s[1], s[3]), fmaxf(u[1], u[3])));
+  uint32_t b0, b1, c0, c1;
+  probs_to_b(A, s, b0, b1);
+  probs_to_b(A, u, c0, c1);
+  // value rows past n (zero fill or unrelated rows) must not reach o
+  uint32_t t0, t1, t2, t3;
+  pair_masks(0, n, t0, t1);
+  pair_masks(16, n, t2, t3);
+  const int vrow = (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+  for (int dt = 0; dt < 8; ++dt) {
+    const uint32_t vbox = vb + (dt >> 2) * half;
+    const int chunk = 2 * (dt & 3) + (mi & 1);
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(swz128(vbox, vrow, chunk), a0, a1, a2, a3);
+    a0 &= t0; a1 &= t0; a2 &= t1; a3 &= t1;
+    mma16816(A.o[dt], a0, a1, a2, a3, b0, b1);
+    ldsm_x4_t(swz128(vbox, vrow + 16, chunk), a0, a1, a2, a3);
+    a0 &= t2; a1 &= t2; a2 &= t3; a3 &= t3;
+    mma16816(A.o[dt], a0, a1, a2, a3, c0, c1);
+  }
+}
+
 // Routing logits z[span][head] = s_span . y_head of a routing page (two
 // 128B-swizzled boxes of 32 rows x 32 floats: routing dims 0-31, then 32-63)
 // in fp32 FMAs, lane l taking span l, four heads per pass (y rows past the
@@ -318,7 +377,8 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
   X.had = true;
 #pragma unroll 1
   for (int rb = 0; rb < n; rb += 16) {
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // the hi and lo products of c accumulate in separate chains
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
     const int tq = rb + (lane & 7) + 8 * (mi & 1);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -327,8 +387,10 @@ __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint
       pair_masks(16 * ks, rK, m0, m1);
       a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
       mma16816(s, a0, a1, a2, a3, X.ch[ks][0], X.ch[ks][1]);
-      mma16816(s, a0, a1, a2, a3, X.cl[ks][0], X.cl[ks][1]);
+      mma16816(sl, a0, a1, a2, a3, X.cl[ks][0], X.cl[ks][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] += sl[e];
     if (rb + g >= n) s[0] = s[1] = kNegInf;
     if (rb + g + 8 >= n) s[2] = s[3] = kNegInf;
     // multi-query decode: only the columns (query tokens) that expand the

@@ -64,7 +64,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
   if (lane == 0) {
     WarpQ Q = ms->wq[w];
     const Ctx C = ms->ctx;
-    const int n_rec = ms->n_rec;
+    const int n_front = ms->n_front, n_rec = n_front + ms->n_back;
     const int cap = routed ? kMaxItems : kPrologueItems;
     const RecEntry* ents = reinterpret_cast<const RecEntry*>(smem + kOffEntries);
     const uint64_t pol = policy_evict_first();
@@ -72,14 +72,15 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
       if (Q.pk == 0 && routed && !Q.rec_out) {
         const int e = atomicAdd(&ms->rec_next, 1);
         if (e < n_rec) {
-          const RecEntry en = ents[e];
+          const int ei = rec_slot(e, n_front);
+          const RecEntry en = ents[ei];
           const int rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
           if (rK > P.rank_lim || rV > P.rank_lim) {
             set_device_error(P.status, DEV_BAD_RANK, rK > rV ? rK : rV);
             continue;  // skipped
           }
           Q.pk = 2;
-          Q.pidx = e;
+          Q.pidx = ei;
           Q.ppart = 0;
           Q.pnp = record_parts(en.body & 0xffff, rK, rV);
         } else {
@@ -194,10 +195,7 @@ __device__ __forceinline__ int consume_item(const uint8_t* smem, SmemMisc* ms,
   const uint32_t bu = smem_u32(base);
   const float* bias = reinterpret_cast<const float*>(smem + kOffBias);
   if (it.type == IT_FULL) {
-    // two 16-row tiles (the second one only if the page has rows there)
-    for (int t0 = 0; t0 < it.n; t0 += kRows)
-      consume_rows16<false>(A, bu + t0 * 128, bu + 2 * kFullHalf + t0 * 128, it.n - t0,
-                            nullptr, P.scale_log2, kFullHalf, nullptr);
+    consume_rows32(A, bu, bu + 2 * kFullHalf, it.n, P.scale_log2, kFullHalf);
   } else if (it.type == IT_SUM) {
     consume_rows16<MQ>(A, bu, bu + 2 * kRowHalf, it.n, bias + (it.a - ms->ctx.k0),
                        P.scale_log2, kRowHalf, smem + kOffCmask + (it.a - ms->ctx.k0));
@@ -297,20 +295,27 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   const bool ex = cm != 0u;
   if (valid) bias[k - k0] = (body > 0 && cm != all) ? log2f(float(body)) : kNegInf;
   if (MQ && valid) smem[kOffCmask + (k - k0)] = uint8_t(cm);
+  // records that arrive in parts go to the front of the queue, the others to
+  // its back (longest first: a split record is one warp's serial chain)
+  const bool big = ex && record_parts(body, rank & 0xffff, (rank >> 16) & 0xffff) > 1;
   const uint32_t bal = __ballot_sync(kFull, ex);
-  int base = 0;
+  const uint32_t bbig = __ballot_sync(kFull, big), bsmall = bal & ~bbig;
+  int bf = 0, bb = 0;
   if (lane == 0) {
     ms->pmask[p] = bal;
-    base = bal ? atomicAdd(&ms->n_rec, __popc(bal)) : 0;
+    if (bbig) bf = atomicAdd(&ms->n_front, __popc(bbig));
+    if (bsmall) bb = atomicAdd(&ms->n_back, __popc(bsmall));
   }
-  base = __shfl_sync(kFull, base, 0);
+  bf = __shfl_sync(kFull, bf, 0);
+  bb = __shfl_sync(kFull, bb, 0);
   if (ex) {
     RecEntry en;
     en.off_lo = int(uint32_t(off));
     en.off_hi = int(off >> 32);
     en.body = body | int(cm << 16);
     en.rank = rank;
-    ents[base + __popc(bal & ((1u << lane) - 1u))] = en;
+    const uint32_t below = (1u << lane) - 1u;
+    ents[big ? bf + __popc(bbig & below) : kSpanCap - 1 - (bb + __popc(bsmall & below))] = en;
   }
   if (landed) {
     retire_item(ms, nd, end);
@@ -449,7 +454,10 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
           en.off_hi = int(off >> 32);
           en.body = body | int(((1u << P.G) - 1u) << 16);  // every column
           en.rank = rank;
-          ents[atomicAdd(&ms->n_rec, 1)] = en;
+          if (record_parts(body, rank & 0xffff, (rank >> 16) & 0xffff) > 1)
+            ents[atomicAdd(&ms->n_front, 1)] = en;
+          else
+            ents[kSpanCap - 1 - atomicAdd(&ms->n_back, 1)] = en;
         }
       }
     }
@@ -569,10 +577,13 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
       }
     }
   }
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int old = atomicAdd(&P.groups[C.g].done, 1);
+    // release: the CTA's partial (stored by every thread before the barrier)
+    // is visible before the count; acquire: the last CTA sees every partial
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(&P.groups[C.g].done) : "memory");
     ms->is_last = (old == P.cg - 1);
   }
   __syncthreads();
@@ -582,7 +593,6 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
   // (the partials arrive by bulk copy, kMergeChunk CTAs per copy, so the
   // merge costs one global round trip per chunk; an online log-sum-exp
   // merge runs over the chunks)
-  __threadfence();
   const int cg = P.cg;
   const float* parts = P.partials + size_t(C.g) * cg * pstride;
   const float* cbuf = reinterpret_cast<const float*>(smem);  // chunk of partials
@@ -717,7 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kSlots; ++s) mbar_init(&ms->bar[w][s], 1);
     mbar_init(&ms->cmb_bar, 1);
-    ms->n_rec = 0;
+    ms->n_front = 0;
+    ms->n_back = 0;
     ms->rec_next = 0;
     ms->fixed_next = 0;
     ms->is_last = 0;
