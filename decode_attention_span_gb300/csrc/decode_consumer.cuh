@@ -154,17 +154,29 @@ __device__ __forceinline__ void consume_rows16(WarpAcc& A, uint32_t kb, uint32_t
                                                const float* bias_row, float scale_log2,
                                                int half, const uint8_t* cmask_row) {
   const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
+  // four accumulator chains (k-steps 4 j + 0..3), added at the end
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
   const int krow = (lane & 7) + 8 * (mi & 1);
 #pragma unroll 1
-  for (int i = 0; i < 4; ++i) {  // head dims 32 i .. 32 i + 31: k-steps 2 i, 2 i + 1
+  for (int i = 0; i < 4; i += 2) {  // head dims 32 i .. 32 i + 63: the box of half i / 2
     const uint4 qv = lds128(A.qfrag + (i * 32 + lane) * 16);
+    const uint4 qw = lds128(A.qfrag + ((i + 1) * 32 + lane) * 16);
     const uint32_t box = kb + (i >> 1) * half;
     uint32_t a0, a1, a2, a3;
-    ldsm_x4(swz128(box, krow, 4 * (i & 1) + (mi >> 1)), a0, a1, a2, a3);
+    ldsm_x4(swz128(box, krow, (mi >> 1)), a0, a1, a2, a3);
     mma16816(s0, a0, a1, a2, a3, qv.x, qv.y);
-    ldsm_x4(swz128(box, krow, 4 * (i & 1) + 2 + (mi >> 1)), a0, a1, a2, a3);
+    ldsm_x4(swz128(box, krow, 2 + (mi >> 1)), a0, a1, a2, a3);
     mma16816(s1, a0, a1, a2, a3, qv.z, qv.w);
+    ldsm_x4(swz128(box, krow, 4 + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s2, a0, a1, a2, a3, qw.x, qw.y);
+    ldsm_x4(swz128(box, krow, 6 + (mi >> 1)), a0, a1, a2, a3);
+    mma16816(s3, a0, a1, a2, a3, qw.z, qw.w);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    s0[e] += s2[e];
+    s1[e] += s3[e];
   }
   float s[4];
   float bias0 = 0.f, bias1 = 0.f;
@@ -320,9 +332,13 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
   const float* sig = reinterpret_cast<const float*>(part + 16);
   const float* gat = sig + r4(rK);
   const uint32_t vt = smem_u32(part + 16 + 8 * r4(rK));
-  float cv[KS][4];
+  // two accumulator chains per rank tile (the two 16-dim halves of each
+  // 32-dim step), added at the end
+  float cv[KS][4], cw[KS][4];
 #pragma unroll
-  for (int t = 0; t < KS; ++t) cv[t][0] = cv[t][1] = cv[t][2] = cv[t][3] = 0.f;
+  for (int t = 0; t < KS; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cv[t][e] = cw[t][e] = 0.f;
   // Vt_K rows past rK read the record's next bytes; their rows of c are
   // dropped by the selects below
 #pragma unroll
@@ -331,15 +347,17 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
 #pragma unroll
     for (int t = 0; t < KS; ++t) {
       const int row = 16 * t + (lane & 7) + 8 * (mi & 1);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int chunk = 4 * i + 2 * h + (mi >> 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(vt + row * 256 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
-        mma16816(cv[t], a0, a1, a2, a3, h ? qv.z : qv.x, h ? qv.w : qv.y);
-      }
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(vt + row * 256 + (((4 * i + (mi >> 1)) ^ (row & 7)) << 4), a0, a1, a2, a3);
+      mma16816(cv[t], a0, a1, a2, a3, qv.x, qv.y);
+      ldsm_x4(vt + row * 256 + (((4 * i + 2 + (mi >> 1)) ^ (row & 7)) << 4), a0, a1, a2, a3);
+      mma16816(cw[t], a0, a1, a2, a3, qv.z, qv.w);
     }
   }
+#pragma unroll
+  for (int t = 0; t < KS; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cv[t][e] += cw[t][e];
 #pragma unroll
   for (int t = 0; t < KS; ++t) {
     const int r0 = 16 * t + g, r1 = r0 + 8;
@@ -359,68 +377,97 @@ __device__ __forceinline__ void exp_key(const WarpAcc& A, ExpAcc<KS>& X, const u
   X.had = false;
 }
 
+// NT (1 or 2) tiles of 16 body tokens from token rb on: logits U_K c (the
+// hi and lo products of c in separate chains, the tiles' chains interleaved),
+// one re-basing check over the tiles, then w^T += U_V^T P^T.  Tokens >= n
+// are masked; so are the columns (query tokens) outside cm in multi-query
+// decode.
+template <int KS, bool MQ, int NT>
+__device__ __forceinline__ void tok_tiles(WarpAcc& A, ExpAcc<KS>& X, uint32_t uku, uint32_t uvu,
+                                          int rb, int n, int rK, int sk, int sv, int wk, int wv,
+                                          unsigned cm) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
+  float s[NT][4], sl[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[j][e] = sl[j][e] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t m0, m1;
+    pair_masks(16 * ks, rK, m0, m1);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int tq = rb + 16 * j + (lane & 7) + 8 * (mi & 1);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(uku + tq * sk + (((2 * ks + (mi >> 1)) ^ u_swz(tq, wk)) << 4), a0, a1, a2, a3);
+      a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
+      mma16816(s[j], a0, a1, a2, a3, X.ch[ks][0], X.ch[ks][1]);
+      mma16816(sl[j], a0, a1, a2, a3, X.cl[ks][0], X.cl[ks][1]);
+    }
+  }
+  float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[j][e] += sl[j][e];
+    if (rb + 16 * j + g >= n) s[j][0] = s[j][1] = kNegInf;
+    if (rb + 16 * j + g + 8 >= n) s[j][2] = s[j][3] = kNegInf;
+    if (MQ) {
+      if (!((cm >> (2 * (lane & 3))) & 1u)) s[j][0] = s[j][2] = kNegInf;
+      if (!((cm >> (2 * (lane & 3) + 1)) & 1u)) s[j][1] = s[j][3] = kNegInf;
+    }
+    mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
+    mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
+  }
+  const float2 alpha = rebase_if_needed(A, mx0, mx1);
+  if (alpha.x != 1.f || alpha.y != 1.f) {
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+      X.w[t][0] *= alpha.x;
+      X.w[t][1] *= alpha.y;
+      X.w[t][2] *= alpha.x;
+      X.w[t][3] *= alpha.y;
+    }
+  }
+  uint32_t b[NT][2], tm[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    probs_to_b(A, s[j], b[j][0], b[j][1]);
+    pair_masks(rb + 16 * j, n, tm[j][0], tm[j][1]);
+  }
+#pragma unroll
+  for (int t = 0; t < KS; ++t) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int tv = rb + 16 * j + (lane & 7) + 8 * (mi >> 1);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(uvu + tv * sv + (((2 * t + (mi & 1)) ^ u_swz(tv, wv)) << 4), a0, a1, a2, a3);
+      a0 &= tm[j][0]; a1 &= tm[j][0]; a2 &= tm[j][1]; a3 &= tm[j][1];
+      mma16816(X.w[t], a0, a1, a2, a3, b[j][0], b[j][1]);
+    }
+  }
+}
+
 // Body tokens [0, n) of this page; U_K rows at uk, U_V rows at uv (row
 // strides r8(rK), r8(rV) bf16, chunks swizzled by u_swz: a page starts at a
-// token that is a multiple of 16), one pass of 16-token tiles with lazy
-// re-basing.  Rows or ranks past the valid ones read neighbouring shared
-// memory and are masked, never multiplied.
+// token that is a multiple of 16), in pairs of 16-token tiles with lazy
+// re-basing, the last tile alone if it is odd.  Rows or ranks past the valid
+// ones read neighbouring shared memory (up to 31 rows past a block's end) and
+// are masked, never multiplied.
 template <int KS, bool MQ>
 __device__ __forceinline__ void exp_tokens(WarpAcc& A, ExpAcc<KS>& X, const uint8_t* uk,
                                            const uint8_t* uv, int n, int rK, int rV,
                                            unsigned cm) {
   if (n <= 0) return;
-  (void)rV;
-  const int lane = threadIdx.x & 31, g = lane >> 2, mi = lane >> 3;
   const int sk = 2 * r8(rK), sv = 2 * r8(rV);  // row strides in bytes
   const int wk = r8(rK) >> 3, wv = r8(rV) >> 3;  // 16-byte chunks per row (swizzled)
   const uint32_t uku = smem_u32(uk), uvu = smem_u32(uv);
   X.had = true;
+  int rb = 0;
 #pragma unroll 1
-  for (int rb = 0; rb < n; rb += 16) {
-    // the hi and lo products of c accumulate in separate chains
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-    const int tq = rb + (lane & 7) + 8 * (mi & 1);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a0, a1, a2, a3, m0, m1;
-      ldsm_x4(uku + tq * sk + (((2 * ks + (mi >> 1)) ^ u_swz(tq, wk)) << 4), a0, a1, a2, a3);
-      pair_masks(16 * ks, rK, m0, m1);
-      a0 &= m0; a1 &= m0; a2 &= m1; a3 &= m1;
-      mma16816(s, a0, a1, a2, a3, X.ch[ks][0], X.ch[ks][1]);
-      mma16816(sl, a0, a1, a2, a3, X.cl[ks][0], X.cl[ks][1]);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] += sl[e];
-    if (rb + g >= n) s[0] = s[1] = kNegInf;
-    if (rb + g + 8 >= n) s[2] = s[3] = kNegInf;
-    // multi-query decode: only the columns (query tokens) that expand the
-    // span see its tokens
-    if (MQ) {
-      if (!((cm >> (2 * (lane & 3))) & 1u)) s[0] = s[2] = kNegInf;
-      if (!((cm >> (2 * (lane & 3) + 1)) & 1u)) s[1] = s[3] = kNegInf;
-    }
-    const float2 alpha = rebase_if_needed(A, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
-    if (alpha.x != 1.f || alpha.y != 1.f) {
-#pragma unroll
-      for (int t = 0; t < KS; ++t) {
-        X.w[t][0] *= alpha.x;
-        X.w[t][1] *= alpha.y;
-        X.w[t][2] *= alpha.x;
-        X.w[t][3] *= alpha.y;
-      }
-    }
-    uint32_t b0, b1, t0, t1;
-    probs_to_b(A, s, b0, b1);
-    pair_masks(rb, n, t0, t1);
-    const int tv = rb + (lane & 7) + 8 * (mi >> 1);
-#pragma unroll
-    for (int t = 0; t < KS; ++t) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(uvu + tv * sv + (((2 * t + (mi & 1)) ^ u_swz(tv, wv)) << 4), a0, a1, a2, a3);
-      a0 &= t0; a1 &= t0; a2 &= t1; a3 &= t1;
-      mma16816(X.w[t], a0, a1, a2, a3, b0, b1);
-    }
-  }
+  for (; rb + 16 < n; rb += 32) tok_tiles<KS, MQ, 2>(A, X, uku, uvu, rb, n, rK, sk, sv, wk, wv, cm);
+  if (rb < n) tok_tiles<KS, MQ, 1>(A, X, uku, uvu, rb, n, rK, sk, sv, wk, wv, cm);
 }
 
 template <int KS>
