@@ -209,6 +209,7 @@ struct SmemMisc {
 static_assert(sizeof(SmemMisc) <= kMiscBytes, "misc smem");
 
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls (~1-2 s at most)
+constexpr unsigned long long kMergeWaitNs = 2000000000ull;  // bounded wait for the partials
 
 // U rows per tile of a split record (a multiple of 16, at most 512).
 __host__ __device__ inline int split_rows(int rK, int rV) {

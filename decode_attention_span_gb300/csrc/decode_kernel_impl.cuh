@@ -613,7 +613,9 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
       bulk_g2s(smem, parts + size_t(c0) * pstride, uint32_t(nc * pstride * 4), &ms->cmb_bar);
     }
     // every thread takes every barrier of this loop, even after a timeout
-    const bool landed = mbar_wait(&ms->cmb_bar, uint32_t(ph), kWaitLimit);
+    // parked: the warps resume as the copy completes (a polling loop that
+    // backs off with sleeps can oversleep it)
+    const bool landed = mbar_wait_parked(&ms->cmb_bar, uint32_t(ph), kMergeWaitNs);
     if (!landed && tid == 0) set_device_error(P.status, DEV_WAIT_TIMEOUT, 7);
     // warp h: log-sum-exp statistics of head h over the chunk's CTAs (lane =
     // CTA), one shuffle reduction each, and every CTA's rescale factor
