@@ -59,7 +59,9 @@ def parse():
                     help="decode: the headline decode step; build: the prefill cache build; "
                          "fullkv: the same decode step over a full-KV cache (comparator); "
                          "append: decode-time cache maintenance, one token per step; "
-                         "multi: two query tokens per sequence in one pass")
+                         "multi: several query tokens per sequence over one cache")
+    ap.add_argument("--query-tokens", type=int, default=2,
+                    help="multi: query tokens per sequence (launched in blocks of 8 / hpg)")
     return ap.parse_args()
 
 
@@ -1011,10 +1013,11 @@ def run_build_bench(args, ws_n, rank, local):
 
 
 def run_multi_bench(args, ws_n, rank, local):
-    """Multi-query decode at 128K (Llama-3-8B shape): two query tokens per
-    sequence over the same cache (sekv_decode_step_multi: each token routes
-    and attends on its own; the union of their expansion sets is loaded once
-    and each (token, head) pair is a column of the tensor-core tiles), 32
+    """Multi-query decode at 128K (Llama-3-8B shape): --query-tokens query
+    tokens per sequence over the same cache (sekv_decode_step_multi: each
+    token routes and attends on its own; each (token, head) pair is a column
+    of the tensor-core tiles, eight per launch, so the tokens go in blocks of
+    8 / hpg, and the union of a block's expansion sets is loaded once), 32
     layers in one CUDA graph.  Reported as query tokens/s, with the one-query
     step of the same run beside it."""
     import decode_attention_span_gb300 as sk
@@ -1023,13 +1026,15 @@ def run_multi_bench(args, ws_n, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.get_config(args.config, **({"layers": args.layers} if args.layers else {}))
-    nq = 2
+    nq = args.query_tokens
     cfg, ws, layers = build_workload(sk, w, dev, w.layers)
     B, Hkv, ms = cfg.batch, cfg.n_kv_heads, cfg.max_spans
+    tpb = 8 // (w.n_q_heads // w.n_kv_heads)
+    nblk = sk.query_blocks(cfg, nq)
     for l, L in enumerate(layers):
         g = gen._gen(w.seed * 4099 + 17 * l + 3, dev)
-        q2 = gen.query(g, w.batch, w.n_q_heads, dev)
-        L["qm"] = torch.stack([L["q"], q2], 1).contiguous()
+        qs = [L["q"]] + [gen.query(g, w.batch, w.n_q_heads, dev) for _ in range(nq - 1)]
+        L["qm"] = torch.stack(qs, 1).contiguous()
         L["outm"] = torch.empty(w.batch, nq, w.n_q_heads, 128, device=dev)
         L["lsem"] = torch.empty(w.batch, nq, w.n_q_heads, device=dev)
         sets = []
@@ -1037,18 +1042,22 @@ def run_multi_bench(args, ws_n, rank, local):
             lst, cnt, _ = sk.route(cfg, L["cache"], L["qm"][:, i].contiguous(), L["W"], L["theta"], ws)
             lst, cnt = lst.view(B * Hkv, ms).cpu().numpy(), cnt.cpu().numpy()
             sets.append([set(lst[gi, :cnt[gi]].tolist()) for gi in range(B * Hkv)])
-        union = [sorted(set().union(*[st[gi] for st in sets])) for gi in range(B * Hkv)]
-        both = sum(len(set.intersection(*[st[gi] for st in sets])) for gi in range(B * Hkv))
-        ulst = torch.zeros(B * Hkv, ms, dtype=torch.int32)
-        ucnt = torch.zeros(B * Hkv, dtype=torch.int32)
-        for gi, u in enumerate(union):
-            ulst[gi, :len(u)] = torch.tensor(u, dtype=torch.int32)
-            ucnt[gi] = len(u)
-        # the union's factors, and the summaries of every span that some token
-        # does not expand (expanded by all tokens: no summary)
-        L["bytes_m"] = (algorithmic_bytes(L["t"], ulst.to(dev), ucnt.to(dev), cfg)
-                        + 512 * (int(ucnt.sum()) - both))
-        L["union_frac"] = int(ucnt.sum()) / max(L["n_nonempty"], 1)
+        # per launch (block of tokens): the union's factors, and the summaries
+        # of every span that some token of the block does not expand
+        L["bytes_m"], ucount = 0, 0
+        for k in range(nblk):
+            bs = sets[k * tpb:(k + 1) * tpb]
+            union = [sorted(set().union(*[st[gi] for st in bs])) for gi in range(B * Hkv)]
+            both = sum(len(set.intersection(*[st[gi] for st in bs])) for gi in range(B * Hkv))
+            ulst = torch.zeros(B * Hkv, ms, dtype=torch.int32)
+            ucnt = torch.zeros(B * Hkv, dtype=torch.int32)
+            for gi, u in enumerate(union):
+                ulst[gi, :len(u)] = torch.tensor(u, dtype=torch.int32)
+                ucnt[gi] = len(u)
+            L["bytes_m"] += (algorithmic_bytes(L["t"], ulst.to(dev), ucnt.to(dev), cfg)
+                             + 512 * (int(ucnt.sum()) - both))
+            ucount += int(ucnt.sum())
+        L["union_frac"] = ucount / nblk / max(L["n_nonempty"], 1)
     scale = sk.default_scale()
 
     def step_m():
@@ -1069,12 +1078,12 @@ def run_multi_bench(args, ws_n, rank, local):
     ms_1 = max_over_ranks(ms_1, ws_n)
     if rank != 0:
         return
-    per_launch = ms_m / 1e3 / args.steps / len(layers)
-    nbytes = sum(L["bytes_m"] for L in layers) / len(layers)
+    per_launch = ms_m / 1e3 / args.steps / (len(layers) * nblk)
+    nbytes = sum(L["bytes_m"] for L in layers) / (len(layers) * nblk)
     peak, peak_kind = measured_peaks()
     achieved = nbytes / per_launch / 1e9
-    line = {"metric": "multi-query decode: query tokens/s at 128K ctx (2 tokens per sequence "
-                      "over one cache, one pass)",
+    line = {"metric": f"multi-query decode: query tokens/s at 128K ctx ({nq} tokens per sequence "
+                      f"over one cache, {nblk} launch{'es' if nblk > 1 else ''} per layer)",
             "value": whole_job_rate(args.steps, ms_m, ws_n) * nq * w.batch, "unit": "tokens/s",
             "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_m / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -1082,6 +1091,7 @@ def run_multi_bench(args, ws_n, rank, local):
             "config": {"workload": w.name, "layers": len(layers), "batch": w.batch,
                        "ctx": w.ctx, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
                        "query_tokens": nq, "columns": nq * w.n_q_heads // w.n_kv_heads,
+                       "launches_per_layer": nblk, "tokens_per_launch": tpb,
                        "union_expand_frac": float(np.mean([L["union_frac"] for L in layers])),
                        "graph": "one CUDA graph per step, programmatic dependent launch"},
             "one_query_ms_per_step": ms_1 / args.steps,
@@ -1090,7 +1100,7 @@ def run_multi_bench(args, ws_n, rank, local):
                          "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
                          "kernel": "sekv::decode_kernel", "bytes_per_launch": nbytes,
                          "avg_launch_us": per_launch * 1e6},
-            "clocks": ck, "gpu_launches": args.steps * len(layers)}
+            "clocks": ck, "gpu_launches": args.steps * len(layers) * nblk}
     print(json.dumps(line), flush=True)
 
 

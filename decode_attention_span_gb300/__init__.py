@@ -14,6 +14,7 @@ from .sekv import (  # noqa: F401
     decode_attention,
     decode_step,
     decode_step_multi,
+    query_blocks,
     decode_step_noalloc,
     fetch_bases,
     fetch_bases_copy,

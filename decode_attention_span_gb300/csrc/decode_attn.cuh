@@ -128,7 +128,8 @@ struct DecodeParams {
   // G: query columns of a group, mma N -- the group's heads, or (multi-query
   // decode) nq query tokens x hpg heads; column h is token h / hpg, head h % hpg
   int B, Hq, Hkv, G, n_sink, n_recent, max_spans, cg;
-  int nq, hpg;
+  int nq, hpg;    // query tokens of this launch; heads per group (column h: token h / hpg)
+  int nq_all;     // query tokens per sequence in q, out and lse (their sequence stride)
   float scale_log2;
   int fused;
   int rank_lim;                  // largest record rank the kernel instance handles (16 KS)

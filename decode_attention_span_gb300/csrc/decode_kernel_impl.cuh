@@ -366,7 +366,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     // (column h: query token h / hpg, head h % hpg; q is [B][nq][Hq][128])
     const int h = tid >> 5, d = 4 * (tid & 31);
     uint2 u = make_uint2(0u, 0u);
-    const int hq = MQ ? (C.b * P.nq + h / P.hpg) * P.Hq + C.c * P.hpg + h % P.hpg
+    const int hq = MQ ? (C.b * P.nq_all + h / P.hpg) * P.Hq + C.c * P.hpg + h % P.hpg
                       : C.b * P.Hq + C.c * G + h;
     if (h < G) u = *reinterpret_cast<const uint2*>(P.q + size_t(hq) * kHeadDim + d);
     const float th = (P.fused && tid < G) ? P.theta[C.c * P.hpg + (MQ ? tid % P.hpg : tid)] : 0.f;
@@ -664,7 +664,7 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
     const int h = hsel + 2 * i;
     if (h < G) {
       const float L = MLa[8 + h];
-      const size_t row = MQ ? (size_t(C.b) * P.nq + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg
+      const size_t row = MQ ? (size_t(C.b) * P.nq_all + h / P.hpg) * P.Hq + size_t(C.c) * P.hpg + h % P.hpg
                             : size_t(C.b) * P.Hq + size_t(C.c) * G + h;
       P.out[row * kHeadDim + d] = L > 0.f ? Oh[i] / L : 0.f;
       if (d == 0 && P.lse != nullptr) P.lse[row] = L > 0.f ? (MLa[h] + log2f(L)) * kLn2 : kNegInf;

@@ -260,6 +260,7 @@ sekv_status fill_decode_params(const sekv_config* cfg, const sekv_layer_cache* c
   P.Hkv = cfg->n_kv_heads;
   P.G = cfg->n_q_heads / cfg->n_kv_heads;
   P.nq = 1;
+  P.nq_all = 1;
   P.hpg = P.G;
   P.n_sink = cfg->n_sink;
   P.n_recent = cfg->n_recent;
@@ -285,7 +286,7 @@ sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_
   static std::once_flag once[8];
   static cudaError_t attr_err[8] = {};
   const int ks = decode_ks(cfg);
-  const int fi = ks - 1 + (P0.nq > 1 ? 4 : 0);
+  const int fi = ks - 1 + (P0.nq_all > 1 ? 4 : 0);
   const void* fn = fns[fi];
   std::call_once(once[fi], [&] {
     attr_err[fi] = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -312,6 +313,13 @@ sekv_status launch_decode(const DecodeParams& P0, const WsLayout& L, const sekv_
 }  // namespace sekv
 
 namespace {
+// Query tokens per launch of the multi-query step: the columns of one
+// launch are (token, head) pairs, at most 8.
+int query_tokens_per_block(const sekv_config* cfg) {
+  const int hpg = cfg->n_q_heads / cfg->n_kv_heads;
+  return hpg >= 1 && hpg <= 8 ? 8 / hpg : 1;
+}
+
 sekv_status decode_step_impl(const sekv_config* cfg, const sekv_layer_cache* cache,
                              const void* q, int n_q, const float* W_r, const float* theta,
                              float scale, float* out, float* lse, int32_t* expanded,
@@ -321,7 +329,7 @@ sekv_status decode_step_impl(const sekv_config* cfg, const sekv_layer_cache* cac
   sekv_status why;
   if (!config_ok(cfg, &why)) return why;
   const int hpg = cfg->n_q_heads / cfg->n_kv_heads;
-  if (n_q < 1 || n_q * hpg > 8) return SEKV_ERR_UNSUPPORTED;
+  if (n_q < 1 || n_q > SEKV_MAX_QUERY_TOKENS || hpg > 8) return SEKV_ERR_UNSUPPORTED;
   sekv_status st = check_cache(cfg, cache, true);
   if (st != SEKV_OK) return st;
   if (!q || !W_r || !theta || !out || !workspace || !cache->s_route) return SEKV_ERR_INVALID;
@@ -335,18 +343,29 @@ sekv_status decode_step_impl(const sekv_config* cfg, const sekv_layer_cache* cac
   memset(&P, 0, sizeof(P));
   st = fill_decode_params(cfg, cache, L, workspace, P, true);
   if (st != SEKV_OK) return st;
-  P.nq = n_q;
-  P.G = n_q * hpg;
   P.store = static_cast<const uint8_t*>(cache->store);
-  P.q = static_cast<const __nv_bfloat16*>(q);
   P.W_r = W_r;
   P.theta = theta;
-  P.out = out;
-  P.lse = lse;
-  P.expanded_out = expanded;
-  P.n_expanded_out = n_expanded;
   P.scale_log2 = scale * kLog2e;
-  return launch_decode(P, L, cfg, stream, (cfg->flags & SEKV_FLAG_OVERLAP_PREVIOUS) != 0);
+  P.nq_all = n_q;
+  // blocks of up to 8 / hpg tokens, one launch each (8 columns per launch);
+  // in stream order, and each may overlap the previous one's tail
+  const int tpb = query_tokens_per_block(cfg);
+  const size_t row = size_t(cfg->n_q_heads) * kHeadDim;  // elements of one token's heads
+  const size_t ng = size_t(cfg->batch) * cfg->n_kv_heads;
+  for (int k = 0, q0 = 0; q0 < n_q; ++k, q0 += tpb) {
+    P.nq = n_q - q0 < tpb ? n_q - q0 : tpb;
+    P.G = P.nq * hpg;
+    P.q = static_cast<const __nv_bfloat16*>(q) + q0 * row;
+    P.out = out + q0 * row;
+    P.lse = lse ? lse + size_t(q0) * cfg->n_q_heads : nullptr;
+    P.expanded_out = expanded ? expanded + k * ng * cfg->max_spans : nullptr;
+    P.n_expanded_out = n_expanded ? n_expanded + k * ng : nullptr;
+    const bool overlap = k > 0 || (cfg->flags & SEKV_FLAG_OVERLAP_PREVIOUS) != 0;
+    st = launch_decode(P, L, cfg, stream, overlap);
+    if (st != SEKV_OK) return st;
+  }
+  return SEKV_OK;
 }
 }  // namespace
 
@@ -357,6 +376,12 @@ extern "C" sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer
                                         size_t workspace_bytes, cudaStream_t stream) {
   return decode_step_impl(cfg, cache, q, 1, W_r, theta, scale, out, lse, expanded, n_expanded,
                           workspace, workspace_bytes, stream);
+}
+
+extern "C" int32_t sekv_query_blocks(const sekv_config* cfg, int32_t n_q) {
+  if (!cfg || n_q < 1 || cfg->n_kv_heads < 1 || cfg->n_q_heads % cfg->n_kv_heads != 0) return 0;
+  const int tpb = query_tokens_per_block(cfg);
+  return (n_q + tpb - 1) / tpb;
 }
 
 extern "C" sekv_status sekv_decode_step_multi(const sekv_config* cfg,

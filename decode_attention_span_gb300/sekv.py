@@ -30,7 +30,8 @@ STATUS = {0: "SEKV_OK", -1: "SEKV_ERR_INVALID", -2: "SEKV_ERR_CAPACITY", -3: "SE
 # every symbol include/sekv.h declares
 EXPORTS = ("sekv_record_size", "sekv_workspace_size", "sekv_workspace_init",
            "sekv_workspace_status", "sekv_route", "sekv_fetch_bases", "sekv_decode_attention",
-           "sekv_decode_step", "sekv_decode_step_multi", "sekv_decode_step_noalloc",
+           "sekv_decode_step", "sekv_decode_step_multi", "sekv_query_blocks",
+           "sekv_decode_step_noalloc",
            "sekv_noalloc_status",
            "sekv_build_spans",
            "sekv_fetch_bases_copy", "sekv_basis_cache_bytes", "sekv_basis_cache_init",
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.sekv_fetch_bases.restype = _c_i32
         L.sekv_fetch_bases.argtypes = [ctypes.POINTER(SekvConfig), ctypes.POINTER(SekvLayerCache),
                                        _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]
+        L.sekv_query_blocks.restype = _c_i32
+        L.sekv_query_blocks.argtypes = [ctypes.POINTER(SekvConfig), _c_i32]
         L.sekv_build_flops.restype = _c_i32
         L.sekv_build_flops.argtypes = [_c_vp, _c_vp, ctypes.POINTER(_c_i64)]
         L.sekv_maint_state_size.restype = _c_sz
@@ -341,11 +344,18 @@ def decode_step(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float, ws:
     return out, lse, expanded, n_expanded
 
 
+def query_blocks(cfg: Config, n_q: int) -> int:
+    """sekv_query_blocks: launches (blocks of query tokens) of the multi-query step."""
+    c = cfg.c()
+    return int(lib().sekv_query_blocks(ctypes.byref(c), int(n_q)))
+
+
 def decode_step_multi(cfg: Config, cache: LayerCache, q, W_r, theta, scale: float,
                       ws: Workspace, out=None, lse=None, want_list: bool = False, stream=None):
     """sekv_decode_step_multi: q [B][n_q][Hq][128] bf16, n_q query tokens per
-    sequence over the same cache; returns out [B][n_q][Hq][128], lse, and the
-    union expansion list and counts when want_list."""
+    sequence over the same cache; returns out [B][n_q][Hq][128], lse, and, when
+    want_list, per block of tokens the union expansion lists
+    [blocks][B*Hkv][max_spans] and counts [blocks][B*Hkv]."""
     _need(q, "q", torch.bfloat16); _need(W_r, "W_r", torch.float32)
     _need(theta, "theta", torch.float32)
     B, n_q = q.shape[0], q.shape[1]
@@ -357,8 +367,9 @@ def decode_step_multi(cfg: Config, cache: LayerCache, q, W_r, theta, scale: floa
     NG = cfg.batch * cfg.n_kv_heads
     expanded = n_expanded = None
     if want_list:
-        expanded = torch.zeros(NG * cfg.max_spans, dtype=torch.int32, device=dev)
-        n_expanded = torch.zeros(NG, dtype=torch.int32, device=dev)
+        nb = max(query_blocks(cfg, n_q), 1)
+        expanded = torch.zeros(nb * NG * cfg.max_spans, dtype=torch.int32, device=dev)
+        n_expanded = torch.zeros(nb * NG, dtype=torch.int32, device=dev)
     c = cfg.c()
     _check("sekv_decode_step_multi",
            lib().sekv_decode_step_multi(ctypes.byref(c), ctypes.byref(cache.c), _ptr(q), n_q,

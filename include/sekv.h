@@ -46,6 +46,7 @@ extern "C" {
 #define SEKV_ROUTE_DIM 64
 #define SEKV_MAX_GROUP 8
 #define SEKV_MAX_RANK 64
+#define SEKV_MAX_QUERY_TOKENS 64 /* query tokens per sequence of sekv_decode_step_multi */
 
 typedef enum sekv_status {
   SEKV_OK = 0,
@@ -358,15 +359,27 @@ sekv_status sekv_decode_step(const sekv_config* cfg, const sekv_layer_cache* cac
  * attends on its own, as [DE]/[ZH] Methodik 3 describe for one query: its
  * expansion set is the union over its GQA group's heads, its expanded spans
  * contribute their reconstructed tokens and its other spans their summaries.
- * The tokens share one pass over the cache: the union of their expansion
- * sets is loaded once, and each (token, head) pair is one column of the
- * kernel's tensor-core tiles, so n_q * (n_q_heads / n_kv_heads) <= 8 (else
- * SEKV_ERR_UNSUPPORTED).
+ * Each (token, head) pair is one column of the kernel's tensor-core tiles,
+ * eight columns per launch: the tokens go in blocks of 8 / (n_q_heads /
+ * n_kv_heads) (sekv_query_blocks(cfg, n_q) blocks), one launch per block in
+ * stream order.  The tokens of a block share one pass over the cache: the
+ * union of their expansion sets is loaded once.
+ *   n_q  1 .. SEKV_MAX_QUERY_TOKENS (else SEKV_ERR_UNSUPPORTED)
  *   q    bf16 [B][n_q][Hq][128];  out f32 [B][n_q][Hq][128];  lse f32
- *        [B][n_q][Hq] (nullable); theta, W_r, workspace and the optional
- *        expansion list (the union over the tokens) as sekv_decode_step.
+ *        [B][n_q][Hq] (nullable); theta, W_r and workspace as
+ *        sekv_decode_step.
+ *   expanded, n_expanded  optional (NULL to skip): per block k, the
+ *        ascending union over the block's tokens, at expanded[k][g][...]
+ *        ([blocks][B*Hkv][max_spans]) and n_expanded[k][g] ([blocks][B*Hkv]).
  * n_q = 1 is sekv_decode_step.
  */
+/*
+ * sekv_query_blocks -- launches (blocks of query tokens) that
+ * sekv_decode_step_multi makes for n_q tokens: ceil(n_q / (8 / (n_q_heads /
+ * n_kv_heads))); 0 for an invalid configuration.  Host only.
+ */
+int32_t sekv_query_blocks(const sekv_config* cfg, int32_t n_q);
+
 sekv_status sekv_decode_step_multi(const sekv_config* cfg, const sekv_layer_cache* cache,
                                    const void* q, int32_t n_q, const float* W_r,
                                    const float* theta, float scale, float* out, float* lse,

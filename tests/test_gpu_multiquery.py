@@ -1,6 +1,7 @@
 """GPU parity of the multi-query decode step (sekv_decode_step_multi): n_q
-query tokens per sequence over the same cache, each checked against the
-oracle's own routing and mixed-resolution attention for that query alone."""
+query tokens per sequence over the same cache (in blocks of 8 / hpg tokens,
+one launch each), each checked against the oracle's own routing and
+mixed-resolution attention for that query alone."""
 import numpy as np
 import pytest
 import torch
@@ -29,6 +30,9 @@ def sk():
     ("qwen2_7b_stress", dict(ctx=8192, batch=2, n_q_heads=8), 4),      # ranks to 64
     ("llama3_8b_32k", dict(ctx=8192, n_q_heads=8), 8),                 # 1 head x 8 tokens
     ("llama3_8b_32k", dict(ctx=8192), 1),                              # = sekv_decode_step
+    ("llama3_8b_32k", dict(ctx=8192), 5),                              # blocks of 2, 2, 1 tokens
+    ("qwen2_7b_stress", dict(ctx=8192, batch=2, n_q_heads=8), 6),      # blocks of 4, 2
+    ("qwen2_7b_stress", dict(ctx=8192, batch=1), 3),                   # 7 heads: one token a block
 ])
 def test_multi_query_matches_oracle_per_query(sk, name, over, n_q):
     w = synth.get_config(name, **over)
@@ -60,14 +64,25 @@ def test_multi_query_matches_oracle_per_query(sk, name, over, n_q):
                                             want_list=True)
     torch.cuda.synchronize()
     assert ws.status() == (0, 0)
-    cnt = cnt.cpu().numpy()
-    lst = lst.cpu().numpy().reshape(w.batch * w.n_kv_heads, -1)
+    # one launch per block of 8 / hpg tokens; each block's list is the union
+    # over its own tokens
+    hpg = w.n_q_heads // w.n_kv_heads
+    tpb = 8 // hpg
+    nb = sk.query_blocks(cfg, n_q)
+    assert nb == -(-n_q // tpb)
+    ng = w.batch * w.n_kv_heads
+    cnt = cnt.cpu().numpy().reshape(nb, ng)
+    lst = lst.cpu().numpy().reshape(nb, ng, -1)
     differ = 0
+    for k in range(nb):
+        toks = range(k * tpb, min(n_q, (k + 1) * tpb))
+        for b in range(w.batch):
+            for c in range(w.n_kv_heads):
+                union = sorted(set().union(*[set(int(x) for x in E[i][b][c]) for i in toks]))
+                gi = b * w.n_kv_heads + c
+                assert list(lst[k, gi, :cnt[k, gi]]) == union, (k, b, c)
     for b in range(w.batch):
         for c in range(w.n_kv_heads):
-            union = sorted(set().union(*[set(int(k) for k in E[i][b][c]) for i in range(n_q)]))
-            gi = b * w.n_kv_heads + c
-            assert list(lst[gi, :cnt[gi]]) == union, (b, c)
             sets = [tuple(E[i][b][c]) for i in range(n_q)]
             differ += len(set(sets)) > 1
     if n_q > 1:
