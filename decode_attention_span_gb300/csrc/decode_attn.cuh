@@ -96,10 +96,12 @@ struct Item {      // one landed (or landing) work item of a warp, 32 bytes
   int uv;          // IT_UT: byte offset of the U_V rows from the item's data
 };
 
-struct RecEntry {  // one expanded span of the CTA, 16 bytes
+// One expanded span of the CTA, 16 bytes, with what the issue logic needs
+// worked out when the entry is made (by the routing lanes, in parallel).
+struct RecEntry {
   int off_lo, off_hi;  // byte offset of its record from `store`
-  int body;            // |S| | (columns expanding the span) << 16
-  int rank;            // rK | rV << 16
+  int body;            // |S| | columns expanding the span << 16 | parts << 24 (0: skipped)
+  int rank;            // rK | (U rows per tile / 16) << 8 | rV << 16
 };
 
 struct DecodeParams {

@@ -52,6 +52,28 @@ __device__ __forceinline__ void arm_item(SmemMisc* ms, int w, int slot, const It
   mbar_arrive_expect_tx(&ms->bar[w][slot], bytes);
 }
 
+// The entry of an expanded span: its record's parts (1 if it lands whole)
+// and U rows per tile; a rank above the instance's limit is flagged here and
+// the entry gets 0 parts (skipped).
+__device__ __forceinline__ RecEntry rec_entry(const DecodeParams& P, long long off, int body,
+                                              unsigned cols, int rank, int& parts) {
+  const int rK = rank & 0xffff, rV = (rank >> 16) & 0xffff;
+  int rows16 = 0;
+  parts = 0;
+  if (rK > P.rank_lim || rV > P.rank_lim) {
+    set_device_error(P.status, DEV_BAD_RANK, rK > rV ? rK : rV);
+  } else {
+    parts = record_parts(body, rK, rV);  // no division for a record that lands whole
+    if (parts > 1) rows16 = split_rows(rK, rV) >> 4;
+  }
+  RecEntry en;
+  en.off_lo = int(uint32_t(off));
+  en.off_hi = int(off >> 32);
+  en.body = body | int(cols << 16) | (parts << 24);
+  en.rank = (rK & 0xff) | (rows16 << 8) | ((rV & 0xff) << 16);
+  return en;
+}
+
 // Issue the warp's next items while it has room (lane 0, on a register copy
 // of the warp's state): first any claim still pending, then new claims.
 // Before routing is done only the CTA's own pages, at most kPrologueItems
@@ -73,16 +95,12 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
         const int e = atomicAdd(&ms->rec_next, 1);
         if (e < n_rec) {
           const int ei = rec_slot(e, n_front);
-          const RecEntry en = ents[ei];
-          const int rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
-          if (rK > P.rank_lim || rV > P.rank_lim) {
-            set_device_error(P.status, DEV_BAD_RANK, rK > rV ? rK : rV);
-            continue;  // skipped
-          }
+          const int parts = (ents[ei].body >> 24) & 0xff;
+          if (parts == 0) continue;  // skipped (flagged when the entry was made)
           Q.pk = 2;
           Q.pidx = ei;
           Q.ppart = 0;
-          Q.pnp = record_parts(en.body & 0xffff, rK, rV);
+          Q.pnp = parts;
         } else {
           Q.rec_out = 1;
         }
@@ -126,12 +144,12 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
         bytes = full ? kFullPageBytes : kRowPageBytes;
       } else {
         const RecEntry en = ents[Q.pidx];
-        const int b = en.body & 0xffff, rK = en.rank & 0xffff, rV = (en.rank >> 16) & 0xffff;
+        const int b = en.body & 0xffff, rK = en.rank & 0xff, rV = (en.rank >> 16) & 0xff;
         const RecordLayout L = record_layout(b, rK, rV);
         roff = (int64_t(uint32_t(en.off_lo)) | (int64_t(en.off_hi) << 32));
         it.rk = rK;
         it.rv = rV;
-        it.a = en.body >> 16;  // the query columns that expand the span
+        it.a = (en.body >> 16) & 0xff;  // the query columns that expand the span
         if (Q.pnp == 1) {
           it.type = IT_REC;
           it.n = b;
@@ -140,7 +158,7 @@ __device__ __forceinline__ void issue_more(uint8_t* smem, SmemMisc* ms, const De
           it.type = IT_KEY;
           n0 = uint32_t(L.uk);
         } else if (Q.ppart < Q.pnp - 1) {
-          const int rows = split_rows(rK, rV);
+          const int rows = ((en.rank >> 8) & 0xff) << 4;
           const int i0 = (Q.ppart - 1) * rows;
           it.type = IT_UT;
           it.n = (b - i0) < rows ? (b - i0) : rows;
@@ -297,7 +315,10 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   if (MQ && valid) smem[kOffCmask + (k - k0)] = uint8_t(cm);
   // records that arrive in parts go to the front of the queue, the others to
   // its back (longest first: a split record is one warp's serial chain)
-  const bool big = ex && record_parts(body, rank & 0xffff, (rank >> 16) & 0xffff) > 1;
+  int parts = 0;
+  RecEntry en{};
+  if (ex) en = rec_entry(P, off, body, cm, rank, parts);
+  const bool big = parts > 1;
   const uint32_t bal = __ballot_sync(kFull, ex);
   const uint32_t bbig = __ballot_sync(kFull, big), bsmall = bal & ~bbig;
   int bf = 0, bb = 0;
@@ -309,11 +330,6 @@ __device__ __forceinline__ void route_page(uint8_t* smem, SmemMisc* ms, const De
   bf = __shfl_sync(kFull, bf, 0);
   bb = __shfl_sync(kFull, bb, 0);
   if (ex) {
-    RecEntry en;
-    en.off_lo = int(uint32_t(off));
-    en.off_hi = int(off >> 32);
-    en.body = body | int(cm << 16);
-    en.rank = rank;
     const uint32_t below = (1u << lane) - 1u;
     ents[big ? bf + __popc(bbig & below) : kSpanCap - 1 - (bb + __popc(bsmall & below))] = en;
   }
@@ -449,12 +465,9 @@ __device__ __forceinline__ void run_decode(uint8_t* smem, SmemMisc* ms, const De
         } else {
           const long long off = P.staged_off != nullptr ? P.staged_off[C.gs + e]
                                                         : P.rec_off[C.gs + k];
-          RecEntry en;
-          en.off_lo = int(uint32_t(off));
-          en.off_hi = int(off >> 32);
-          en.body = body | int(((1u << P.G) - 1u) << 16);  // every column
-          en.rank = rank;
-          if (record_parts(body, rank & 0xffff, (rank >> 16) & 0xffff) > 1)
+          int parts;
+          const RecEntry en = rec_entry(P, off, body, (1u << P.G) - 1u, rank, parts);  // every column
+          if (parts > 1)
             ents[atomicAdd(&ms->n_front, 1)] = en;
           else
             ents[kSpanCap - 1 - atomicAdd(&ms->n_back, 1)] = en;
