@@ -393,6 +393,7 @@ def h2d_peak_gbs(dev, nbytes: int = 1 << 30) -> float:
 
 QUERY_SETS = 8        # distinct queries per layer, used in turn by successive steps
 QUERY_DRIFT = 0.3     # q_s = sqrt(1 - d^2) q_(s-1) + d n, n ~ N(0, 1)
+SIDE_STREAMS = 3         # tiered mode: streams that route and fetch ahead of attention
 CACHE_SLOTS = 256     # residency cache slots per (sequence, KV head), 20 KB each
 CACHE_SLOT_BYTES = 20480
 STAGING_PER_GROUP = 8 << 20
@@ -425,7 +426,7 @@ def run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev):
     scale = sk.default_scale()
     cfg_t = sk.Config(**{**cfg.__dict__, "flags": 0})
     ws_main = sk.Workspace(cfg_t, dev)
-    ws_sides = [sk.Workspace(cfg_t, dev), sk.Workspace(cfg_t, dev)]
+    ws_sides = [sk.Workspace(cfg_t, dev) for _ in range(SIDE_STREAMS)]
     L_n, B, Hq = len(layers), cfg.batch, cfg.n_q_heads
     NG, ms = B * cfg.n_kv_heads, cfg.max_spans
     q_sets = drifting_queries(layers, w.seed * 31 + 5)
@@ -446,10 +447,10 @@ def run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev):
                         hits=torch.zeros(NG, dtype=torch.int32, device=dev),
                         copied=torch.zeros(NG, dtype=torch.int64, device=dev),
                         ev=torch.cuda.Event()))
-    # two side streams take the layers in turn, so that one layer's routing
-    # and planning overlap the previous layer's copies over the host link
-    sides = [torch.cuda.Stream(), torch.cuda.Stream()]
-    ev_q, ev_end = torch.cuda.Event(), [torch.cuda.Event(), torch.cuda.Event()]
+    # side streams take the layers in turn, so that one layer's routing and
+    # planning overlap the previous layers' copies over the host link
+    sides = [torch.cuda.Stream() for _ in range(SIDE_STREAMS)]
+    ev_q, ev_end = torch.cuda.Event(), [torch.cuda.Event() for _ in range(SIDE_STREAMS)]
     launches = [0]
 
     def step(s):
@@ -461,7 +462,7 @@ def run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev):
             sd.wait_event(ev_q)
         for i, L in enumerate(layers):
             X = per[i]
-            side, ws_side = sides[i % 2], ws_sides[i % 2]
+            side, ws_side = sides[i % SIDE_STREAMS], ws_sides[i % SIDE_STREAMS]
             sk.route(cfg_t, X["cache"], q_dev[i], L["W"], L["theta"], ws_side, expanded=X["lst"],
                      n_expanded=X["cnt"], stream=side)
             n += sk.last_launch_count()

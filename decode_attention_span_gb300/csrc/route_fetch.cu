@@ -31,22 +31,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (tid < 8) th[tid] = tid < G ? P.theta[c * G + tid] : 0.f;
   if (tid == 0) s_base = 0;
   __syncthreads();
+  const int lane = tid & 31, wid = tid >> 5;
   {
-    const int jr = tid & 63, hh = tid >> 6;  // heads hh, hh + 4
-    const float4* wrow = reinterpret_cast<const float4*>(P.W_r + (size_t(c) * kRouteDim + jr) * kHeadDim);
-    float a0 = 0.f, a1 = 0.f;
-    for (int d4 = 0; d4 < 32; ++d4) {
-      const float4 wv = __ldg(wrow + d4);
-      const float4 q0 = reinterpret_cast<const float4*>(qs[hh])[d4];
-      const float4 q1 = reinterpret_cast<const float4*>(qs[hh + 4])[d4];
-      a0 = fmaf(wv.x, q0.x, fmaf(wv.y, q0.y, fmaf(wv.z, q0.z, fmaf(wv.w, q0.w, a0))));
-      a1 = fmaf(wv.x, q1.x, fmaf(wv.y, q1.y, fmaf(wv.z, q1.z, fmaf(wv.w, q1.w, a1))));
+    // y = W_r q: warp w takes rows 8w .. 8w + 7; lane (r, dq) = (lane / 4,
+    // lane % 4) loads 16-byte chunks dq + 4 i (i < 8) of row 8w + r, all
+    // eight at once, multiplies them with the same chunks of every head's
+    // query and sums over dq by shuffles
+    const int r = lane >> 2, dq = lane & 3;
+    const float4* wrow =
+        reinterpret_cast<const float4*>(P.W_r + (size_t(c) * kRouteDim + 8 * wid + r) * kHeadDim);
+    float4 wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = __ldg(wrow + dq + 4 * i);
+    float acc[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) acc[h] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float4 qv = reinterpret_cast<const float4*>(qs[h])[dq + 4 * i];
+        acc[h] = fmaf(wv[i].w, qv.w, fmaf(wv[i].z, qv.z, fmaf(wv[i].y, qv.y, fmaf(wv[i].x, qv.x, acc[h]))));
+      }
     }
-    ys[hh][jr] = a0;
-    ys[hh + 4][jr] = a1;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
+      acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 2);
+    }
+    if (dq == 0) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) ys[h][8 * wid + r] = acc[h];
+    }
   }
   __syncthreads();
-  const int lane = tid & 31, wid = tid >> 5;
   for (int i = 0; i < kRouteChunk / kRouteThreads; ++i) {
     const int k = k0 + i * kRouteThreads + tid;
     bool ex = false;
@@ -211,19 +229,31 @@ namespace sekv {
 // ----------------------------------------------------------------------------
 
 // Block-wide exclusive prefix of v (256 threads); *total receives the sum.
+// Shuffle scans within the warps and over the eight warp sums: three
+// barriers.  sh holds at least 16 entries.
 __device__ __forceinline__ long long block_excl_scan(long long v, long long* sh, long long* total) {
-  const int tid = threadIdx.x;
-  sh[tid] = v;
-  __syncthreads();
-  for (int o = 1; o < 256; o <<= 1) {
-    const long long u = tid >= o ? sh[tid - o] : 0;
-    __syncthreads();
-    sh[tid] += u;
-    __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  const long long incl = sh[tid];
-  *total = sh[255];
+  if (lane == 31) sh[wid] = x;
   __syncthreads();
+  if (wid == 0) {
+    long long t = lane < 8 ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < 8) sh[8 + lane] = t;  // inclusive over the warps
+  }
+  __syncthreads();
+  const long long incl = (wid > 0 ? sh[8 + wid - 1] : 0) + x;
+  *total = sh[15];
+  __syncthreads();  // sh is free for the next scan
   return incl - v;
 }
 
