@@ -40,3 +40,28 @@ def test_record_size_matches_layout(libsekv):
 def test_status_strings(libsekv):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert libsekv.sekv_status_string(code)
+
+
+def test_query_blocks(libsekv):
+    """Multi-query decode launches blocks of 8 / (Hq / Hkv) query tokens."""
+    import decode_attention_span_gb300 as sk
+    for hq, hkv in ((32, 8), (28, 4), (8, 4), (8, 8), (16, 2)):
+        cfg = sk.Config(1, hq, hkv, 4, 64, 256, 32, 1, 64, 4.0)
+        tpb = 8 // (hq // hkv)
+        for n in (1, 2, 3, 5, 8, 17, 64):
+            assert sk.query_blocks(cfg, n) == -(-n // tpb), (hq, hkv, n)
+        assert sk.query_blocks(cfg, 0) == 0
+
+
+def test_multi_query_limits_rejected_on_host(libsekv):
+    """n_q outside 1..SEKV_MAX_QUERY_TOKENS is rejected before any device work."""
+    import ctypes
+    import decode_attention_span_gb300 as sk
+    cfg = sk.Config(1, 32, 8, 4, 64, 256, 32, 1, 64, 4.0)
+    c = cfg.c()
+    cache = sk.sekv.SekvLayerCache()
+    for n in (0, -1, 65):
+        st = libsekv.sekv_decode_step_multi(ctypes.byref(c), ctypes.byref(cache), None, n, None,
+                                            None, ctypes.c_float(1.0), None, None, None, None,
+                                            None, ctypes.c_size_t(0), None)
+        assert st == -5, (n, st)  # SEKV_ERR_UNSUPPORTED
