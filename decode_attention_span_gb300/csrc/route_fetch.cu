@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(256) fetch_kernel(const FetchParams P) {
           const long long st = carry + incl[t] - sz;
           const int4* src = reinterpret_cast<const int4*>(P.store + P.rec_off[gs + ks[t]]);
           int4* dst = reinterpret_cast<int4*>(P.staging + int64_t(g) * P.per_group + st);
-          // eight 16-byte loads in flight per thread: the host link's latency
-          // is hidden by concurrency, not by one load at a time
+          // kFetchUnroll 16-byte loads in flight per thread: the host link's
+          // latency is hidden by concurrency, not by one load at a time
           const long long n16 = sz / 16;
           for (long long i0 = 0; i0 < n16; i0 += 256 * kFetchUnroll) {
             int4 v[kFetchUnroll];

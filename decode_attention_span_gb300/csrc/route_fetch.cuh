@@ -27,7 +27,7 @@ struct RouteParams {
 };
 
 constexpr int kFetchParts = 48;
-constexpr int kFetchUnroll = 8;  // 16-byte loads in flight per thread
+constexpr int kFetchUnroll = 16;  // 16-byte loads in flight per thread
 
 struct FetchParams {
   const int32_t* n_spans;
