@@ -717,8 +717,11 @@ template <int KS, bool MQ>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned (TMA's 128-byte swizzle), by pointer arithmetic on the
+  // shared array itself: the compiler keeps every access through `smem` in
+  // the shared window (32-bit addresses, shared loads and stores) instead of
+  // generic 64-bit ones, as it would after a round trip through an integer
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   SmemMisc* ms = reinterpret_cast<SmemMisc*>(smem + kOffMisc);
   // fused mode: lane (r = lane / 4, dq = lane % 4) of warp w keeps the
   // 16-byte chunks c = dq + 4 i (i = 0..7) of W_r row 8w + r in registers
