@@ -57,7 +57,7 @@ constexpr int kMaxCg = 256;                   // CTAs per (sequence, KV head) gr
 constexpr int kStaticPages = 1;               // full-resolution pages each CTA owns
 constexpr int kPoolClaim = 1;                 // pages per claim from the group's pool
 constexpr int kMergeChunk = 32;               // partials per bulk copy in the merge
-constexpr int kPrologueItems = 2;             // items per warp issued before the query
+constexpr int kPrologueItems = 3;             // items per warp issued before the query
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffArena = 0;

@@ -3,8 +3,8 @@
 //
 // Per warp: an arena of kArenaGran granules used as a ring (items are placed
 // contiguously, wrapping to the arena start when one does not fit at the
-// end), up to kMaxItems items in flight (before routing: up to two routing
-// pages and the first own pages, kPrologueItems in all), each with its own
+// end), up to kMaxItems items in flight (before routing: its routing pages
+// and the first own pages, kPrologueItems in all), each with its own
 // mbarrier.  The
 // warp issues and consumes its items itself, in order, so no handover
 // between warps is needed; the only CTA-wide synchronisation is the routing
