@@ -63,11 +63,13 @@ def parse():
     ap.add_argument("--traffic-workload", default="llama3_8b_128k")
     ap.add_argument("--traffic-scale", type=float, default=1.0)
     ap.add_argument("--traffic-command", default="")
-    ap.add_argument("--path", default="decode", choices=["decode", "build", "fullkv", "append", "multi"],
+    ap.add_argument("--path", default="decode",
+                    choices=["decode", "build", "fullkv", "append", "multi", "e2e"],
                     help="decode: the headline decode step; build: the prefill cache build; "
                          "fullkv: the same decode step over a full-KV cache (comparator); "
                          "append: decode-time cache maintenance, one token per step; "
-                         "multi: several query tokens per sequence over one cache")
+                         "multi: several query tokens per sequence over one cache; "
+                         "e2e: the tiered end-to-end leg of the decode line alone")
     ap.add_argument("--query-tokens", type=int, default=2,
                     help="multi: query tokens per sequence (launched in blocks of 8 / hpg)")
     return ap.parse_args()
@@ -538,6 +540,52 @@ def run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev):
     return dict(ms=ms_total, steps=steps, h2d=h2d, d2h=d2h, launches=launches[0], err=err,
                 hit_frac=hits / max(1, n_exp), copied=copied, n_exp=n_exp,
                 fetch_paths=fetch_path_times(sk, cfg_t, layers, per, q_sets, dev))
+
+
+def e2e_leg(sk, cfg, w, layers, steps, warmup, ws_n, dev):
+    """The tiered end-to-end measurement (run_tiered) as the bench line's
+    `e2e` object; also returns the library launches of one step."""
+    peak_h2d = h2d_peak_gbs(dev)
+    r = run_tiered(sk, cfg, w, layers, steps, warmup, ws_n, dev)
+    ms_e = max_over_ranks(r["ms"], ws_n)
+    step_s = ms_e / steps / 1e3
+    e2e = {"value": ws_n * steps / (ms_e / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+           "path": f"tiered: q H2D; per layer route + residency-cached fetch of the bases from "
+                   f"pinned host memory on one of {SIDE_STREAMS} side streams running ahead of "
+                   f"attention; out D2H; one CUDA graph per step",
+           "queries": f"{QUERY_SETS} drifting query sets in turn (drift {QUERY_DRIFT} per step)",
+           "cache": {"slots_per_group": CACHE_SLOTS, "slot_bytes": CACHE_SLOT_BYTES,
+                     "hit_frac": r["hit_frac"], "expanded_per_step": r["n_exp"],
+                     "record_bytes_copied_per_step": r["copied"]},
+           "h2d_gbs": r["h2d"] / step_s / 1e9, "h2d_peak_gbs": peak_h2d,
+           "h2d_frac_of_peak": r["h2d"] / step_s / 1e9 / peak_h2d,
+           "fetch_paths": r["fetch_paths"],
+           "steps": steps, "max_abs_vs_resident": r["err"]}
+    return e2e, r["launches"]
+
+
+def run_e2e_bench(args, ws_n, rank, local):
+    """The tiered end-to-end leg alone (bases in pinned host memory, residency
+    cache, routing and fetch on side streams ahead of attention): the decode
+    line's `e2e` object as a line of its own, for profiling the pipeline."""
+    import decode_attention_span_gb300 as sk
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (e2e) needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.get_config(args.config, **({"layers": args.layers} if args.layers else {}))
+    cfg, _, layers = build_workload(sk, w, dev, w.layers)
+    e2e, launches = e2e_leg(sk, cfg, w, layers, args.steps, args.warmup, ws_n, dev)
+    if rank != 0:
+        return
+    line = {"metric": "tiered " + decode_metric(w).split(";")[0] + " (bases in pinned host memory)",
+            "value": e2e["value"], "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 / e2e["value"] * ws_n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": decode_config(w, ws_n), "e2e": e2e,
+            "gpu_launches": args.steps * launches}
+    print(json.dumps(line), flush=True)
 
 
 def fetch_path_times(sk, cfg, layers, per, q_sets, dev):
@@ -1193,6 +1241,8 @@ def main():
     if args.path == "fullkv":
         run_fullkv_bench(args, ws_n, rank, local)
         return
+    if args.path == "e2e":
+        return run_e2e_bench(args, ws_n, rank, local)
     w = synth.get_config(args.config)
     if args.layers:
         w = synth.get_config(args.config, layers=args.layers)
@@ -1231,25 +1281,8 @@ def main():
             "clocks": ck, "gpu_launches": args.steps * len(layers)}
     if not args.no_e2e:
         e_steps = max(16, args.steps // 4)
-        peak_h2d = h2d_peak_gbs(dev)
-        r = run_tiered(sk, cfg, w, layers, e_steps, args.warmup, ws_n, dev)
-        ms_e = max_over_ranks(r["ms"], ws_n)
-        step_s = ms_e / e_steps / 1e3
-        line["e2e"] = {"value": ws_n * e_steps / (ms_e / 1e3), "unit": UNIT,
-                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                       "path": "tiered: q H2D; per layer route + residency-cached fetch of the "
-                               "bases from pinned host memory on a side stream running ahead "
-                               "of attention; out D2H; one CUDA graph per step",
-                       "queries": f"{QUERY_SETS} drifting query sets in turn (drift "
-                                  f"{QUERY_DRIFT} per step)",
-                       "cache": {"slots_per_group": CACHE_SLOTS, "slot_bytes": CACHE_SLOT_BYTES,
-                                 "hit_frac": r["hit_frac"], "expanded_per_step": r["n_exp"],
-                                 "record_bytes_copied_per_step": r["copied"]},
-                       "h2d_gbs": r["h2d"] / step_s / 1e9, "h2d_peak_gbs": peak_h2d,
-                       "h2d_frac_of_peak": r["h2d"] / step_s / 1e9 / peak_h2d,
-                       "fetch_paths": r["fetch_paths"],
-                       "steps": e_steps, "max_abs_vs_resident": r["err"]}
-        line["gpu_launches"] += e_steps * r["launches"]
+        line["e2e"], launches = e2e_leg(sk, cfg, w, layers, e_steps, args.warmup, ws_n, dev)
+        line["gpu_launches"] += e_steps * launches
     if not args.no_cpu_baseline and rank == 0:
         line["cpu_baseline"] = cpu_baseline_leg(w, args.cpu_seconds)
         line["parity"] = parity_check(sk, cfg, ws, layers[0], w)
