@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(1024) seg_kernel(const BuildParams P) {
   const int m0 = P.n_sink, m1 = P.T - P.n_recent;
   const int n_mid = m1 > m0 ? m1 - m0 : 0;
   const int words = (n_mid + 31) / 32;
-  if (b == 0 && tid < 16) P.counters[tid] = 0;  // class counts/cursors for this build
+  if (b == 0 && tid < 16) P.counters[tid] = 0;  // class counts/cursors for this call
   const float* Hb = P.H + size_t(b) * P.T;
   for (int w = wid; w < words; w += blockDim.x / 32) {
     const int t = m0 + 32 * w + lane;

@@ -277,7 +277,7 @@ sekv_status sekv_fetch_bases_copy(const sekv_config* cfg, const sekv_layer_cache
 
 /*
  * Residency cache of basis records in device memory, kept from call to call
- * (this build's answer to the pages' CPU-GPU bandwidth limit, [DE] Bedeutung
+ * (this library's answer to the pages' CPU-GPU bandwidth limit, [DE] Bedeutung
  * / [ZH] 意义: an expanded span whose record is still resident costs no
  * host-link traffic).  Per (sequence, KV head) group: n_slots slots of
  * slot_bytes each, a table span -> slot, and for every slot its span and the

@@ -3,7 +3,7 @@ infrastructure only, like the rest of ``oracle``).
 
 The pages describe the cache built at prefill and the zoom-in during decode;
 they do not say how the cache follows the tokens that decoding appends.
-Reading taken (this build's, from the pages' own definitions):
+Reading taken here (from the pages' own definitions):
 
 * [DE] lay explainer part 2 / [ZH] 两层记忆: the GPU keeps the very last part
   of the text at full resolution.  The newest token joins that recent window,
